@@ -1,0 +1,410 @@
+"""Benchmark of the channelwise gated delta rule hot path on one GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * one decode step at B=64, H=32, dk=dv=128 (bf16 q/k/v, fp32 per-channel
+    log-decay, fp32 state of 134 MB carried from step to step), and
+  * one chunked prefill at B=1, H=32, dk=dv=128, T=4000, chunk 64 (zero
+    initial state).
+The L2 cache (129 MB) is flushed by writing a 256 MiB buffer before every
+kernel, outside the timed brackets; kernels are timed with CUDA events on the
+stream they run on.
+
+Headline value: decode state GB/s = 2*B*H*dk*dv*4 bytes per step / decode
+time.  The prefill rate (tokens/s) is reported beside it.  `roofline` is for
+the kernel with the larger share of the step (the prefill kernel); the
+decode kernel's roofline is under `decode_roofline`.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas, weak scaling, no collective on the data path); the step time is
+the max over ranks.  `--impl reference` times the fp64 CPU oracle instead,
+on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode state GB/s (% HBM peak) at B=64; prefill tokens/s at T=4000, 32 heads"
+DEC = dict(B=64, H=32, dk=128, dv=128)
+PRE = dict(B=1, H=32, T=4000, dk=128, dv=128, chunk=64)
+DEC_STATE_BYTES = 2 * DEC["B"] * DEC["H"] * DEC["dk"] * DEC["dv"] * 4           # 268,435,456
+# prefill algorithmic bytes: q,k,v bf16 + g fp32 + beta fp32 + o bf16 + state in and out fp32
+PRE_BYTES = (PRE["B"] * PRE["T"] * PRE["H"] * (3 * 128 * 2 + 128 * 4 + 4 + 128 * 2)
+             + 2 * PRE["B"] * PRE["H"] * 128 * 128 * 4)                           # 201,314,304
+# prefill tensor flops per token-head: 10*C*d (intra-chunk) + 6*dk*dv (carry)
+PRE_FLOPS = PRE["B"] * PRE["T"] * PRE["H"] * (10 * PRE["chunk"] * 128 + 6 * 128 * 128)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _traffic(kernel: str, source: str):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        sha = hashlib.sha256(open(os.path.join(ROOT, "gated_delta_rule_channelwise_gb300", "csrc", source), "rb").read()).hexdigest()
+        for line in open(path):
+            kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+            if kv.get("kernel") == kernel and kv.get("source_sha256") == sha:
+                return int(kv["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", "cgdr_clocks_%d.csv" % os.getpid())
+        try:
+            import torch
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+            sel = ["-i", "%04x:%02x:%02x.0" % (torch.cuda.get_device_properties(device_index).pci_domain_id, bus,
+                                                torch.cuda.get_device_properties(device_index).pci_device_id)]
+        except Exception:
+            sel = ["-i", str(device_index)]
+        self.cmd = ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "100", *sel]
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, x in enumerate(r) if x.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_channelwise_gb300 as cg
+    from gated_delta_rule_channelwise_gb300 import build as cbuild
+    from gated_delta_rule_channelwise_gb300.synth import WORKLOADS, make_inputs
+
+    if rank == 0 or world == 1:
+        cbuild.build()
+    if world > 1:
+        dist.barrier()
+    cbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+
+    # ---- resident inputs
+    wd, wp = WORKLOADS["decode_b64"], WORKLOADS["prefill_t4000"]
+    dsteps = 16                                   # distinct decode inputs, cycled
+    dinp = make_inputs(wd, T=dsteps, device=dev, seed=wd.seed + 97 * rank)
+    dstate = dinp["S0"].clone()
+    dout = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.bfloat16, device=dev)
+    pinp = make_inputs(wp, device=dev, seed=wp.seed + 97 * rank)
+    pstate = torch.zeros_like(pinp["S0"])
+    pout = torch.empty_like(pinp["v"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def decode(i):
+        t = i % dsteps
+        cg.decode(dinp["q"][:, t], dinp["k"][:, t], dinp["v"][:, t], dstate, dout,
+                  g=dinp["g"][:, t], beta=dinp["beta"][:, t])
+
+    def prefill():
+        pstate.zero_()                            # zero initial state (outside the timed bracket)
+        cg.prefill(pinp["q"], pinp["k"], pinp["v"], pstate, pout, g=pinp["g"], beta=pinp["beta"], chunk=64)
+
+    for i in range(args.warmup):
+        flush.zero_(); decode(i); flush.zero_(); prefill()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream); decode(i); ev[i][1].record(stream)
+            flush.zero_()
+            pstate.zero_()
+            ev[i][2].record(stream)
+            cg.prefill(pinp["q"], pinp["k"], pinp["v"], pstate, pout, g=pinp["g"], beta=pinp["beta"], chunk=64)
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    dec_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    pre_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    tot = torch.tensor([sum(dec_ms), sum(pre_ms), sum(dec_ms) + sum(pre_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+    dec_total, pre_total, step_total = (float(x) for x in tot.tolist())
+
+    # ---- end to end: host (pinned) buffers, copies inside the timed region
+    e2e = run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world)
+
+    if rank != 0:
+        return None
+    hbm, tflops, peak_kind = _peaks()
+    dec_gbs = world * K * DEC_STATE_BYTES / (dec_total / 1e3) / 1e9
+    pre_tps = world * K * PRE["B"] * PRE["T"] / (pre_total / 1e3)
+    dec_launch_s = statistics.mean(dec_ms) / 1e3
+    pre_launch_s = statistics.mean(pre_ms) / 1e3
+    pre_ach = PRE_BYTES / pre_launch_s / 1e9
+    dec_ach = DEC_STATE_BYTES / dec_launch_s / 1e9
+    tr_pre = _traffic("prefill_tc_kernel", "prefill_tc.cu")
+    tr_dec = _traffic("decode_kernel", "decode.cu")
+    out = {
+        "metric": METRIC, "value": round(dec_gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_total / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode_b64 + prefill_t4000",
+                   "decode": {"B": 64, "H": 32, "dk": 128, "dv": 128, "state": "fp32", "inputs": "bf16",
+                              "gate": "per-channel fp32"},
+                   "prefill": {"B": 1, "H": 32, "T": 4000, "dk": 128, "dv": 128, "chunk": 64, "inputs": "bf16"},
+                   "l2": "flushed (256 MiB write) before every kernel, outside the timed brackets",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_hbm_peak": round(100.0 * dec_gbs / world / hbm, 2),
+        "prefill": {"metric": "prefill tokens/s at T=4000, 32 heads", "value": round(pre_tps, 1),
+                    "unit": "tokens/s", "ms_per_launch": round(pre_launch_s * 1e3, 5)},
+        "decode_ms_per_launch": round(dec_launch_s * 1e3, 5),
+        "roofline": {"kernel": "prefill_tc_kernel", "bound": "hbm", "achieved": round(pre_ach, 2), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(pre_ach / hbm, 4),
+                     "traffic": tr_pre, "algorithmic_bytes": PRE_BYTES,
+                     "tensor_flops": PRE_FLOPS, "tensor_frac": round(PRE_FLOPS / pre_launch_s / 1e12 / tflops, 4)},
+        "decode_roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": round(dec_ach, 2), "peak": hbm,
+                            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
+                            "traffic": tr_dec, "algorithmic_bytes": DEC_STATE_BYTES},
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    out["clocks"] = clk.summary()
+    return out
+
+
+def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
+    """Decode and prefill through the public API with pinned host inputs and outputs."""
+    import torch
+    K = max(3, min(args.steps, 200))
+    # decode: per step copy q, k, v, g, beta in and o out
+    h = {k: dinp[k][:, 0].contiguous().cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    d = {k: torch.empty_like(h[k], device=dev) for k in h}
+    ho = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.bfloat16).pin_memory()
+    do = torch.empty_like(ho, device=dev)
+    h2d_dec = sum(x.numel() * x.element_size() for x in h.values())
+    d2h_dec = ho.numel() * ho.element_size()
+
+    def dstep():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        cg.decode(d["q"], d["k"], d["v"], dstate, do, g=d["g"], beta=d["beta"])
+        ho.copy_(do, non_blocking=True)
+
+    # prefill: copy q, k, v, g, beta in and o out
+    hp = {k: pinp[k].contiguous().cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    dp = {k: torch.empty_like(hp[k], device=dev) for k in hp}
+    hpo = torch.empty(pinp["v"].shape, dtype=torch.bfloat16).pin_memory()
+    dpo = torch.empty_like(hpo, device=dev)
+    ps = torch.zeros_like(pinp["S0"])
+    h2d_pre = sum(x.numel() * x.element_size() for x in hp.values())
+    d2h_pre = hpo.numel() * hpo.element_size()
+
+    def pstep():
+        for k in hp:
+            dp[k].copy_(hp[k], non_blocking=True)
+        ps.zero_()
+        cg.prefill(dp["q"], dp["k"], dp["v"], ps, dpo, g=dp["g"], beta=dp["beta"], chunk=64)
+        hpo.copy_(dpo, non_blocking=True)
+
+    for _ in range(3):
+        dstep(); pstep()
+    torch.cuda.synchronize()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record(stream)
+    for _ in range(K):
+        dstep()
+    e1.record(stream)
+    for _ in range(K):
+        pstep()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    dms, pms = e0.elapsed_time(e1) / K, e1.elapsed_time(e2) / K
+    return {"value": round(world * DEC_STATE_BYTES / (dms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d_dec + h2d_pre, "d2h_bytes_per_step": d2h_dec + d2h_pre,
+            "decode_ms": round(dms, 5), "prefill_ms": round(pms, 5),
+            "prefill_tokens_per_s": round(world * PRE["T"] / (pms / 1e3), 1),
+            "note": "decode state stays resident on the device; inputs and o cross the host link every step"}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_sample(seconds_budget: float):
+    """Time the fp64 CPU oracle, as it stands, on bounded samples of both workloads.
+
+    Decode: every (b, h) unit of a B=64, H=32 batch for one token; prefill: all
+    32 heads for the first `n_tok` tokens of the T=4000 sequence.  Returns
+    (decode GB/s of fp32-state traffic, prefill tokens/s, threads, description).
+    """
+    import oracle
+    from gated_delta_rule_channelwise_gb300.synth import WORKLOADS, make_inputs
+    threads = oracle.default_threads()
+    wd, wp = WORKLOADS["decode_b64"], WORKLOADS["prefill_t4000"]
+    di = make_inputs(wd, T=1, device="cpu")
+    t = time.perf_counter()
+    oracle.recurrence(di["q"], di["k"], di["v"], g=di["g"], beta=di["beta"], S0=di["S0"], threads=threads)
+    dsec = time.perf_counter() - t
+    n_tok = 64
+    pi = make_inputs(wp, T=n_tok, device="cpu")
+    t = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.recurrence(pi["q"], pi["k"], pi["v"], g=pi["g"], beta=pi["beta"], S0=pi["S0"], threads=threads)
+        reps += 1
+        if time.perf_counter() - t > seconds_budget / 2 or reps >= 50:
+            break
+    psec = (time.perf_counter() - t) / reps
+    desc = ("decode: all 2048 (b,h) units of B=64,H=32 for 1 token; prefill: 32 heads x %d tokens of the "
+            "T=4000 sequence, %d repeats" % (n_tok, reps))
+    return DEC_STATE_BYTES / dsec / 1e9, n_tok / psec, threads, desc
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle on the host cores, K steps of a bounded sample."""
+    import numpy as np
+    import oracle
+    from gated_delta_rule_channelwise_gb300.synth import WORKLOADS, make_inputs
+    oracle.build()
+    threads = oracle.default_threads()
+    wd, wp = WORKLOADS["decode_b64"], WORKLOADS["prefill_t4000"]
+    units = 2 * threads                          # decode units per step (a sample of the 2048)
+    di = make_inputs(wd, T=1, B=max(1, units // 32), device="cpu")
+    pi = make_inputs(wp, T=8, device="cpu")
+    pi = {k: (v[:, :, :1] if k in ("q", "k", "v", "g", "beta") else (v[:, :1] if k == "S0" else v))
+          for k, v in pi.items()}
+    bytes_per_unit = 2 * 128 * 128 * 4
+
+    def step():
+        t0 = time.perf_counter()
+        oracle.recurrence(di["q"], di["k"], di["v"], g=di["g"], beta=di["beta"], S0=di["S0"], threads=threads)
+        t1 = time.perf_counter()
+        oracle.recurrence(pi["q"], pi["k"], pi["v"], g=pi["g"], beta=pi["beta"], S0=pi["S0"], threads=1)
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
+
+    for _ in range(args.warmup):
+        step()
+    dsum = psum = 0.0
+    for _ in range(args.steps):
+        a, b = step()
+        dsum += a
+        psum += b
+    n_units = di["v"].shape[0] * di["v"].shape[2]
+    gbs = args.steps * n_units * bytes_per_unit / dsum / 1e9
+    tps = args.steps * 8 * 32 / (psum * 32)      # one head timed; 32 heads per token at this rate
+    sample = ("per step: one decode token for %d of the 2048 (b,h) units of B=64,H=32; prefill: 8 tokens of one "
+              "head of the T=4000 sequence (scaled to 32 heads)" % n_units)
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round((dsum + psum) / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode_b64 + prefill_t4000 (bounded samples)"},
+            "prefill": {"value": round(tps, 2), "unit": "tokens/s"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1:
+            dgbs, ptps, cores, desc = oracle_sample(args.cpu_baseline_seconds)
+            out["cpu_baseline"] = {"value": round(dgbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                   "sample": desc, "prefill_tokens_per_s": round(ptps, 2)}
+        else:
+            out["cpu_baseline"] = None
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

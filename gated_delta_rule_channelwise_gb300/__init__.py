@@ -1,0 +1,225 @@
+"""Channelwise gated delta rule for GB300 (sm_103a): Python binding of libcgdr.
+
+This module only marshals arguments: it turns torch tensors into the
+``cgdr_args`` block of ``include/cgdr.h`` (device pointers and element
+strides) and calls the C ABI on the current CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback.  If ``libcgdr.so`` is missing, calls raise ``RuntimeError``; build
+it with ``gated_delta_rule_channelwise_gb300.build.build()``.
+
+Public calls (same names as the C ABI without the ``cgdr_`` prefix):
+
+* :func:`decode` -- one T = 1 step for every (batch, v-head).
+* :func:`prefill` -- chunked prefill over T tokens.
+* :func:`prefill_workspace_size`, :func:`validate`, :func:`status_string`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcgdr.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+F32, BF16 = 0, 1
+GATE_CHANNEL, GATE_GDN = 0, 1
+
+
+class CgdrArgs(ctypes.Structure):
+    """Mirror of ``struct cgdr_args`` in include/cgdr.h."""
+    _i64 = ctypes.c_int64
+    _fields_ = [
+        ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32),
+        ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("gate", ctypes.c_int32), ("l2norm_qk", ctypes.c_int32),
+        ("chunk", ctypes.c_int32), ("q_scale", ctypes.c_float), ("eps", ctypes.c_float),
+        ("q", ctypes.c_void_p), ("q_sb", _i64), ("q_st", _i64), ("q_sh", _i64),
+        ("k", ctypes.c_void_p), ("k_sb", _i64), ("k_st", _i64), ("k_sh", _i64),
+        ("v", ctypes.c_void_p), ("v_sb", _i64), ("v_st", _i64), ("v_sh", _i64),
+        ("g", ctypes.c_void_p), ("g_sb", _i64), ("g_st", _i64), ("g_sh", _i64),
+        ("beta", ctypes.c_void_p), ("beta_sb", _i64), ("beta_st", _i64), ("beta_sh", _i64),
+        ("a", ctypes.c_void_p), ("a_sb", _i64), ("a_st", _i64), ("a_sh", _i64),
+        ("b", ctypes.c_void_p), ("b_sb", _i64), ("b_st", _i64), ("b_sh", _i64),
+        ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("state", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("o_sb", _i64), ("o_st", _i64), ("o_sh", _i64),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+# (name, restype, argtypes) of every symbol include/cgdr.h declares.
+_SIGNATURES = [
+    ("cgdr_abi_version", ctypes.c_int, []),
+    ("cgdr_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("cgdr_validate", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_int]),
+    ("cgdr_decode", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p]),
+    ("cgdr_prefill_workspace_size", ctypes.c_size_t, [ctypes.POINTER(CgdrArgs)]),
+    ("cgdr_prefill", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+]
+
+
+def lib():
+    """The loaded libcgdr (ctypes.CDLL).  Raises if the library was not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libcgdr.so is not built (%s); run gated_delta_rule_channelwise_gb300.build.build()"
+                                   % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            for name, res, args in _SIGNATURES:
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+class CgdrError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def status_string(status: int) -> str:
+    return lib().cgdr_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise CgdrError(status, where)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("every tensor must live on a CUDA device (the library has no CPU path)")
+
+
+def make_args(q, k, v, state, o, *, T, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
+              l2norm=True, q_scale=None, eps=None, chunk=0) -> CgdrArgs:
+    """Fill a ``cgdr_args`` block from 4-d views ``[B, T, H, d]`` (token dim included).
+
+    Gate tensors are ``g [B,T,Hv,dk]`` and ``beta [B,T,Hv]`` (channel gate) or
+    ``a, b [B,T,Hv]`` with ``A_log, dt_bias [Hv]`` (GatedDeltaNet gate).
+    """
+    A = CgdrArgs()
+    B, _, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    A.B, A.T, A.Hk, A.Hv, A.dk, A.dv = B, T, Hk, Hv, dk, dv
+    A.dtype = _dtype_code(q)
+    A.gate = GATE_CHANNEL if g is not None else GATE_GDN
+    A.l2norm_qk = 1 if l2norm else 0
+    A.chunk = int(chunk)
+    A.q_scale = float(q_scale) if q_scale is not None else 0.0
+    A.eps = float(eps) if eps is not None else -1.0
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t.stride(-1) != 1:
+            raise ValueError("%s: innermost dimension must be contiguous" % name)
+        setattr(A, name, t.data_ptr())
+        setattr(A, name + "_sb", t.stride(0))
+        setattr(A, name + "_st", t.stride(1))
+        setattr(A, name + "_sh", t.stride(2))
+    if g is not None:
+        if g.stride(-1) != 1:
+            raise ValueError("g: innermost dimension must be contiguous")
+        A.g, A.g_sb, A.g_st, A.g_sh = g.data_ptr(), g.stride(0), g.stride(1), g.stride(2)
+        A.beta, A.beta_sb, A.beta_st, A.beta_sh = beta.data_ptr(), beta.stride(0), beta.stride(1), beta.stride(2)
+    else:
+        A.a, A.a_sb, A.a_st, A.a_sh = a.data_ptr(), a.stride(0), a.stride(1), a.stride(2)
+        A.b, A.b_sb, A.b_st, A.b_sh = b.data_ptr(), b.stride(0), b.stride(1), b.stride(2)
+        A.A_log, A.dt_bias = A_log.data_ptr(), dt_bias.data_ptr()
+    if not state.is_contiguous():
+        raise ValueError("state must be a dense [B, Hv, dk, dv] fp32 tensor")
+    A.state = state.data_ptr()
+    return A
+
+
+def _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias):
+    import torch
+    _need_cuda(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
+    if k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype:
+        raise TypeError("q, k, v and o must share one dtype")
+    if state.dtype != torch.float32:
+        raise TypeError("state must be float32")
+    for name, t in (("g", g), ("beta", beta), ("A_log", A_log), ("dt_bias", dt_bias)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("%s must be float32" % name)
+    for name, t in (("a", a), ("b", b)):
+        if t is not None and t.dtype != q.dtype:
+            raise TypeError("%s must have the dtype of q" % name)
+
+
+def decode(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
+           l2norm=True, q_scale=None, eps=None, stream=None):
+    """One decode step.  q, k ``[B,Hk,dk]``; v ``[B,Hv,dv]``; state ``[B,Hv,dk,dv]`` fp32
+    (updated in place); gate ``g [B,Hv,dk]`` + ``beta [B,Hv]`` or ``a, b [B,Hv]`` +
+    ``A_log, dt_bias [Hv]``.  Returns o ``[B,Hv,dv]`` in q's dtype."""
+    import torch
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
+    u = lambda t: None if t is None else t.unsqueeze(1)
+    A = make_args(u(q), u(k), u(v), state, u(o), T=1, g=u(g), beta=u(beta), a=u(a), b=u(b),
+                  A_log=A_log, dt_bias=dt_bias, l2norm=l2norm, q_scale=q_scale, eps=eps)
+    _check(lib().cgdr_decode(ctypes.byref(A), _stream_handle(stream)), "cgdr_decode")
+    return o
+
+
+def prefill_workspace_size(q, k, v, state, o, **kw) -> int:
+    A = make_args(q, k, v, state, o, T=q.shape[1], **kw)
+    return int(lib().cgdr_prefill_workspace_size(ctypes.byref(A)))
+
+
+def prefill(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
+            l2norm=True, q_scale=None, eps=None, chunk=64, workspace=None, stream=None):
+    """Chunked prefill.  q, k ``[B,T,Hk,dk]``; v ``[B,T,Hv,dv]``; state ``[B,Hv,dk,dv]``
+    fp32 (updated in place); gate ``g [B,T,Hv,dk]`` + ``beta [B,T,Hv]`` or
+    ``a, b [B,T,Hv]`` + ``A_log, dt_bias [Hv]``.  Returns o ``[B,T,Hv,dv]``."""
+    import torch
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
+    A = make_args(q, k, v, state, o, T=q.shape[1], g=g, beta=beta, a=a, b=b, A_log=A_log, dt_bias=dt_bias,
+                  l2norm=l2norm, q_scale=q_scale, eps=eps, chunk=chunk)
+    L = lib()
+    need = int(L.cgdr_prefill_workspace_size(ctypes.byref(A)))
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if (workspace is not None and need > 0) else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if (workspace is not None and need > 0) else 0
+    _check(L.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes),
+                          _stream_handle(stream)), "cgdr_prefill")
+    return o
+
+
+def validate(A: CgdrArgs, for_prefill: bool) -> int:
+    return int(lib().cgdr_validate(ctypes.byref(A), 1 if for_prefill else 0))
+
+
+__all__ = ["decode", "prefill", "prefill_workspace_size", "validate", "status_string", "make_args",
+           "CgdrArgs", "CgdrError", "lib", "LIB_PATH"]

@@ -1,0 +1,102 @@
+// C ABI entry points of libcgdr: host-side argument checks and dispatch.
+// The operation and the argument conventions are documented in cgdr.h.
+#include "cgdr_internal.cuh"
+
+namespace {
+
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+bool aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+bool strides_ok(int64_t s0, int64_t s1, int64_t s2, int64_t mult) {
+    return s0 >= 0 && s1 >= 0 && s2 >= 0 && s0 % mult == 0 && s1 % mult == 0 && s2 % mult == 0;
+}
+
+cgdr_status check(const cgdr_args *a, bool prefill) {
+    if (!a) return CGDR_ERR_INVALID_ARG;
+    if (a->B < 0 || a->T < 0 || a->Hk <= 0 || a->Hv <= 0) return CGDR_ERR_INVALID_ARG;
+    if (a->Hv % a->Hk != 0) return CGDR_ERR_INVALID_ARG;
+    if (!prefill && a->T != 1) return CGDR_ERR_INVALID_ARG;
+    if (!dim_ok(a->dk) || !dim_ok(a->dv)) return CGDR_ERR_UNSUPPORTED;
+    if (a->dtype != CGDR_F32 && a->dtype != CGDR_BF16) return CGDR_ERR_UNSUPPORTED;
+    if (a->gate != CGDR_GATE_CHANNEL && a->gate != CGDR_GATE_GDN) return CGDR_ERR_UNSUPPORTED;
+    if (prefill && !(a->chunk == 0 || a->chunk == 16 || a->chunk == 32 || a->chunk == 64))
+        return CGDR_ERR_UNSUPPORTED;
+    if (a->B == 0 || a->T == 0) return CGDR_OK;  // nothing to do: no pointer is touched
+
+    if (!a->q || !a->k || !a->v || !a->state || !a->o) return CGDR_ERR_INVALID_ARG;
+    if (a->gate == CGDR_GATE_CHANNEL && (!a->g || !a->beta)) return CGDR_ERR_INVALID_ARG;
+    if (a->gate == CGDR_GATE_GDN && (!a->a || !a->b || !a->A_log || !a->dt_bias))
+        return CGDR_ERR_INVALID_ARG;
+
+    const size_t esz = a->dtype == CGDR_BF16 ? 2 : 4;
+    const int64_t vec = (int64_t)(16 / esz);
+    // decode ignores the token strides
+    const int64_t q_st = prefill ? a->q_st : 0, k_st = prefill ? a->k_st : 0;
+    const int64_t v_st = prefill ? a->v_st : 0, o_st = prefill ? a->o_st : 0;
+    const int64_t g_st = prefill ? a->g_st : 0, be_st = prefill ? a->beta_st : 0;
+    const int64_t a_st = prefill ? a->a_st : 0, b_st = prefill ? a->b_st : 0;
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16) ||
+        !aligned(a->state, 16))
+        return CGDR_ERR_ALIGNMENT;
+    if (!strides_ok(a->q_sb, q_st, a->q_sh, vec) || !strides_ok(a->k_sb, k_st, a->k_sh, vec) ||
+        !strides_ok(a->v_sb, v_st, a->v_sh, vec) || !strides_ok(a->o_sb, o_st, a->o_sh, vec))
+        return CGDR_ERR_ALIGNMENT;
+    if (a->gate == CGDR_GATE_CHANNEL) {
+        if (!aligned(a->g, 16) || !strides_ok(a->g_sb, g_st, a->g_sh, 4)) return CGDR_ERR_ALIGNMENT;
+        if (!aligned(a->beta, 4) || !strides_ok(a->beta_sb, be_st, a->beta_sh, 1)) return CGDR_ERR_ALIGNMENT;
+    } else {
+        if (!aligned(a->a, esz) || !aligned(a->b, esz) || !aligned(a->A_log, 4) || !aligned(a->dt_bias, 4))
+            return CGDR_ERR_ALIGNMENT;
+        if (!strides_ok(a->a_sb, a_st, a->a_sh, 1) || !strides_ok(a->b_sb, b_st, a->b_sh, 1))
+            return CGDR_ERR_ALIGNMENT;
+    }
+    return CGDR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cgdr_abi_version(void) { return CGDR_ABI_VERSION; }
+
+const char *cgdr_status_string(int s) {
+    switch (s) {
+        case CGDR_OK: return "CGDR_OK";
+        case CGDR_ERR_INVALID_ARG: return "CGDR_ERR_INVALID_ARG: null pointer, bad size, Hv % Hk != 0 or T != 1 for decode";
+        case CGDR_ERR_UNSUPPORTED: return "CGDR_ERR_UNSUPPORTED: dk/dv/chunk/dtype/gate outside the supported set";
+        case CGDR_ERR_ALIGNMENT: return "CGDR_ERR_ALIGNMENT: misaligned pointer or stride";
+        case CGDR_ERR_WORKSPACE: return "CGDR_ERR_WORKSPACE: workspace too small";
+        case CGDR_ERR_CUDA: return "CGDR_ERR_CUDA: a CUDA call or kernel launch failed";
+        case CGDR_ERR_TIMEOUT: return "CGDR_ERR_TIMEOUT: a bounded device wait gave up";
+        default: return "unknown cgdr status";
+    }
+}
+
+cgdr_status cgdr_validate(const cgdr_args *a, int for_prefill) { return check(a, for_prefill != 0); }
+
+cgdr_status cgdr_decode(const cgdr_args *a, void *stream) {
+    cgdr_status st = check(a, false);
+    if (st != CGDR_OK || a->B == 0) return st;
+    return cgdr::launch_decode(*a, static_cast<cudaStream_t>(stream));
+}
+
+size_t cgdr_prefill_workspace_size(const cgdr_args *a) {
+    if (check(a, true) != CGDR_OK) return 0;
+    if (cgdr::prefill_tc_supported(*a)) return cgdr::prefill_tc_workspace(*a);
+    return 0;
+}
+
+cgdr_status cgdr_prefill(const cgdr_args *a, void *ws, size_t ws_bytes, void *stream) {
+    cgdr_status st = check(a, true);
+    if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cgdr::prefill_tc_supported(*a)) {
+        const size_t need = cgdr::prefill_tc_workspace(*a);
+        if (need > 0 && (ws == nullptr || ws_bytes < need)) return CGDR_ERR_WORKSPACE;
+        return cgdr::launch_prefill_tc(*a, ws, ws_bytes, s);
+    }
+    return cgdr::launch_prefill_simt(*a, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Internal declarations and device helpers shared by the libcgdr kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "cgdr.h"
+
+namespace cgdr {
+
+// ---------------------------------------------------------------- host side
+cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s);
+cgdr_status launch_prefill_simt(const cgdr_args &a, cudaStream_t s);
+bool prefill_tc_supported(const cgdr_args &a);
+size_t prefill_tc_workspace(const cgdr_args &a);
+cgdr_status launch_prefill_tc(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
+
+inline float eps_of(const cgdr_args &a) { return a.eps < 0.f ? 1e-6f : a.eps; }
+inline float qscale_of(const cgdr_args &a) {
+    return a.q_scale > 0.f ? a.q_scale : 1.0f / sqrtf((float)a.dk);
+}
+inline int chunk_of(const cgdr_args &a) { return a.chunk == 0 ? 64 : a.chunk; }
+
+// ---------------------------------------------------------------- device side
+template <typename T> struct Cvt;
+template <> struct Cvt<float> {
+    static __device__ __forceinline__ float to_f(float x) { return x; }
+    static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Cvt<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// softplus with the usual threshold: x above 20 is returned unchanged.
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
+// Scalar GatedDeltaNet gate: g = -exp(A_log) * softplus(a + dt_bias).
+__device__ __forceinline__ float gdn_gate(float A_log, float a, float dt_bias) {
+    return -expf(A_log) * softplus_f(a + dt_bias);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ldmatrix: four 8x8 b16 matrices; lane l supplies the row address of
+// matrix l/8, row l%8.  Register j receives matrix j.
+__device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                        uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                          uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+}  // namespace cgdr

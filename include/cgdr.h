@@ -1,0 +1,148 @@
+/*
+ * cgdr.h -- C ABI of libcgdr, the channelwise gated delta rule for GB300 (sm_103a).
+ *
+ * The operation (per batch b and v-head h, an fp32 state S of shape dk x dv):
+ * for each token t,
+ *     qn = q_t / sqrt(|q_t|^2 + eps) * q_scale        kn = k_t / sqrt(|k_t|^2 + eps)
+ *     S  <- Diag(exp(g_t)) S                           (per key-channel decay)
+ *     S  <- S + beta_t kn (v_t - S^T kn)^T             (rank-one delta-rule write)
+ *     o_t = S^T qn                                     (read after the write)
+ * Sources: the two-traversal token recurrence of "Two-pass optimization for
+ * channelwise gated delta rule kernel" (executorch PR #21020, Summary); the
+ * fused decode of "Add fused GatedDeltaNet decode Triton kernel" (executorch
+ * PR #18865, description: Q/K/V split, L2 norm, head repeat, gating and state
+ * update in one kernel); and the routing and chunked form of "Add parallel
+ * chunked prefill for channelwise gated delta rule" (executorch PR #21061,
+ * Summary: T == 1 uses the token recurrence, T != 1 a chunkwise WY/UT form).
+ *
+ * Conventions shared by both calls
+ *  - All tensor pointers are DEVICE pointers.  Strides are in ELEMENTS; the
+ *    innermost dimension (dk or dv) must be contiguous.
+ *  - Head repeat: v-head h reads q/k head h / (Hv/Hk) (repeat-interleave;
+ *    the pages say only "head repeat").  Hv must be a multiple of Hk.
+ *  - Gate, CGDR_GATE_CHANNEL: g [B,T,Hv,dk] fp32 per-channel log-decay and
+ *    beta [B,T,Hv] fp32.  CGDR_GATE_GDN (scalar GatedDeltaNet gate):
+ *    a, b [B,T,Hv] in `dtype`, A_log and dt_bias [Hv] fp32;
+ *    g = -exp(A_log[h]) * softplus(a + dt_bias[h]) for every channel,
+ *    beta = sigmoid(b); softplus(x) = x for x > 20.
+ *  - state: fp32 [B,Hv,dk,dv], dense (dv fastest), updated in place.
+ *    A zero-filled state is the zero initial state.
+ *  - o: [B,T,Hv,dv] in `dtype`, accumulated in fp32.
+ *  - q, k, v, o: 16-byte aligned base pointers; batch/token/head strides
+ *    multiples of 8 elements (bf16) or 4 elements (fp32).  g: 16-byte
+ *    aligned, strides multiples of 4.  state: 16-byte aligned.
+ *  - No input may alias `state` or `o`.
+ *
+ * Ownership and threading: the caller owns every buffer and the stream.
+ * The library allocates nothing, keeps no mutable global state, and is safe
+ * to call from several host threads.  Calls are asynchronous on `stream`
+ * (a cudaStream_t; NULL is the legacy default stream) and launch on the
+ * calling thread's current device.
+ *
+ * Errors: arguments are checked on the host before any launch; a failing
+ * check returns its code and launches nothing.  CGDR_ERR_CUDA reports a
+ * launch error (cudaGetLastError after the launch).  Device faults surface
+ * asynchronously, as with any CUDA kernel.  No C++ exception crosses this ABI.
+ */
+#ifndef CGDR_H_
+#define CGDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CGDR_ABI_VERSION 1
+
+typedef enum cgdr_status {
+    CGDR_OK = 0,
+    CGDR_ERR_INVALID_ARG = 1,   /* null pointer, negative size, Hv % Hk != 0, T != 1 for decode */
+    CGDR_ERR_UNSUPPORTED = 2,   /* dk, dv or chunk outside the supported set, unknown dtype/gate */
+    CGDR_ERR_ALIGNMENT = 3,     /* misaligned pointer, stride or non-unit inner stride */
+    CGDR_ERR_WORKSPACE = 4,     /* workspace smaller than cgdr_prefill_workspace_size() */
+    CGDR_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    CGDR_ERR_TIMEOUT = 6        /* reserved: a bounded device-side wait gave up */
+} cgdr_status;
+
+typedef enum cgdr_dtype { CGDR_F32 = 0, CGDR_BF16 = 1 } cgdr_dtype;
+typedef enum cgdr_gate { CGDR_GATE_CHANNEL = 0, CGDR_GATE_GDN = 1 } cgdr_gate;
+
+/* One argument block for both calls.  Zero-initialise it, then fill in. */
+typedef struct cgdr_args {
+    int32_t B, T, Hk, Hv, dk, dv;   /* dk, dv in {32, 64, 128}; T == 1 for decode */
+    int32_t dtype;                  /* cgdr_dtype of q, k, v, o (and a, b) */
+    int32_t gate;                   /* cgdr_gate */
+    int32_t l2norm_qk;              /* nonzero: L2-normalise q and k (the usual setting) */
+    int32_t chunk;                  /* prefill chunk length 16, 32 or 64; 0 selects 64 */
+    float q_scale;                  /* applied to q after the norm; <= 0 selects 1/sqrt(dk) */
+    float eps;                      /* added to |x|^2 in the L2 norm; < 0 selects 1e-6 */
+    const void *q;     int64_t q_sb, q_st, q_sh;        /* [B,T,Hk,dk] */
+    const void *k;     int64_t k_sb, k_st, k_sh;        /* [B,T,Hk,dk] */
+    const void *v;     int64_t v_sb, v_st, v_sh;        /* [B,T,Hv,dv] */
+    const float *g;    int64_t g_sb, g_st, g_sh;        /* [B,T,Hv,dk] (CHANNEL) */
+    const float *beta; int64_t beta_sb, beta_st, beta_sh; /* [B,T,Hv]   (CHANNEL) */
+    const void *a;     int64_t a_sb, a_st, a_sh;        /* [B,T,Hv]    (GDN) */
+    const void *b;     int64_t b_sb, b_st, b_sh;        /* [B,T,Hv]    (GDN) */
+    const float *A_log;                                 /* [Hv]        (GDN) */
+    const float *dt_bias;                               /* [Hv]        (GDN) */
+    float *state;                                       /* [B,Hv,dk,dv] in/out */
+    void *o;           int64_t o_sb, o_st, o_sh;        /* [B,T,Hv,dv] out */
+} cgdr_args;
+
+/* ABI version of the loaded library (CGDR_ABI_VERSION it was built with). */
+int cgdr_abi_version(void);
+
+/* Static, human-readable name of a status code; never NULL. */
+const char *cgdr_status_string(int status);
+
+/*
+ * Host-only check of `args` for cgdr_decode (for_prefill == 0) or
+ * cgdr_prefill (for_prefill != 0), without touching the GPU.  Returns the
+ * status the call itself would return before launching.
+ */
+cgdr_status cgdr_validate(const cgdr_args *args, int for_prefill);
+
+/*
+ * One decode step (T == 1) for every (b, h): the fused path of "Add fused
+ * GatedDeltaNet decode Triton kernel" (Q/K/V split by strides into one packed
+ * projection row, L2 norm, head repeat, gate, state update, all in one
+ * kernel) with the two-traversal update of "Two-pass optimization for
+ * channelwise gated delta rule kernel": one pass forms S^T(exp(g) * kn) from
+ * the state as read, the other decays, writes and accumulates o.  Each
+ * state element is read once from and written once to HBM.
+ * The token-stride fields (q_st, ...) are ignored.
+ */
+cgdr_status cgdr_decode(const cgdr_args *args, void *stream);
+
+/*
+ * Bytes of device workspace cgdr_prefill needs for `args` (may be 0).
+ * The workspace plays the part of the single scratch arena of "Add parallel
+ * chunked prefill for channelwise gated delta rule" (Summary), sliced per
+ * (batch, head) unit.  Returns 0 for invalid arguments as well.
+ */
+size_t cgdr_prefill_workspace_size(const cgdr_args *args);
+
+/*
+ * Chunked prefill over T >= 0 tokens ("Add parallel chunked prefill for
+ * channelwise gated delta rule", Summary): per chunk the per-channel
+ * log-decay prefix, the causal query/key terms, the beta-folded triangular
+ * (UT) transform, WY pseudo-keys and pseudo-values, and the inter-chunk
+ * state carry, with a ragged last chunk handled by the same code.
+ * T == 0 is a no-op.  The result equals T applications of the token
+ * recurrence up to rounding, for every chunk length.  bf16 inputs with
+ * dk = dv = 128 and chunk 64 run on the tensor cores; other cases run an
+ * fp32 CUDA-core kernel of the same chunked form.
+ * `workspace` may be NULL when cgdr_prefill_workspace_size() returns 0.
+ * Numerical range: within a chunk, the log-decay summed over any 15
+ * consecutive tokens must stay above -80 on every channel (the tensor-core
+ * path forms exp of such sums); the fp32 path has no such limit.
+ */
+cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CGDR_H_ */

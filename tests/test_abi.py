@@ -1,0 +1,132 @@
+"""C-ABI checks that need no GPU: build, load, exported symbols, struct layout,
+host-side argument validation.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_delta_rule_channelwise_gb300 as cg
+from gated_delta_rule_channelwise_gb300 import build as cbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cgdr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return cg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cgdr_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted([
+        "cgdr_abi_version", "cgdr_status_string", "cgdr_validate", "cgdr_decode",
+        "cgdr_prefill_workspace_size", "cgdr_prefill"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", cg.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\b[TW] (\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_abi_version_and_status_strings(lib):
+    m = re.search(r"#define CGDR_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.cgdr_abi_version() == int(m.group(1))
+    for s in range(7):
+        assert cg.status_string(s).startswith("CGDR_")
+    assert cg.status_string(99) == "unknown cgdr status"
+
+
+def test_struct_layout_matches_c(tmp_path):
+    """ctypes mirror of cgdr_args has the size and field offsets the C compiler gives."""
+    fields = [f[0] for f in cg.CgdrArgs._fields_]
+    src = tmp_path / "layout.c"
+    body = "\n".join('printf("%s %%zu\\n", offsetof(cgdr_args, %s));' % (f, f) for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "cgdr.h"\nint main(void){\n'
+                   'printf("sizeof %zu\\n", sizeof(cgdr_args));\n' + body + "\nreturn 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n") if l)
+    assert int(got["sizeof"]) == ctypes.sizeof(cg.CgdrArgs)
+    for f in fields:
+        assert int(got[f]) == getattr(cg.CgdrArgs, f).offset, f
+
+
+def _args(**kw):
+    """A valid-looking bf16 channel-gate argument block with fake (never dereferenced) pointers."""
+    A = cg.CgdrArgs()
+    A.B, A.T, A.Hk, A.Hv, A.dk, A.dv = 2, 1, 2, 4, 128, 128
+    A.dtype, A.gate, A.l2norm_qk, A.chunk = cg.BF16, cg.GATE_CHANNEL, 1, 64
+    base = 1 << 20
+    for i, name in enumerate(["q", "k", "v", "o", "g", "beta", "state"]):
+        setattr(A, name, base * (i + 1))
+    A.q_sb, A.q_st, A.q_sh = 8 * 128, 2 * 128, 128
+    A.k_sb, A.k_st, A.k_sh = 8 * 128, 2 * 128, 128
+    A.v_sb, A.v_st, A.v_sh = 16 * 128, 4 * 128, 128
+    A.o_sb, A.o_st, A.o_sh = 16 * 128, 4 * 128, 128
+    A.g_sb, A.g_st, A.g_sh = 16 * 128, 4 * 128, 128
+    A.beta_sb, A.beta_st, A.beta_sh = 4, 4, 1
+    for k, v in kw.items():
+        setattr(A, k, v)
+    return A
+
+
+def test_validation_accepts_good_args(lib):
+    assert cg.validate(_args(), False) == cg.OK
+    assert cg.validate(_args(T=5), True) == cg.OK
+
+
+@pytest.mark.parametrize("kw,prefill,code", [
+    (dict(T=2), False, cg.ERR_INVALID_ARG),            # decode is T == 1
+    (dict(Hv=3), False, cg.ERR_INVALID_ARG),           # Hv % Hk
+    (dict(B=-1), False, cg.ERR_INVALID_ARG),
+    (dict(Hk=0), True, cg.ERR_INVALID_ARG),
+    (dict(q=0), False, cg.ERR_INVALID_ARG),
+    (dict(state=0), True, cg.ERR_INVALID_ARG),
+    (dict(g=0), False, cg.ERR_INVALID_ARG),
+    (dict(gate=cg.GATE_GDN), False, cg.ERR_INVALID_ARG),  # a, b, A_log, dt_bias missing
+    (dict(dk=96), False, cg.ERR_UNSUPPORTED),
+    (dict(dv=256), True, cg.ERR_UNSUPPORTED),
+    (dict(dtype=7), False, cg.ERR_UNSUPPORTED),
+    (dict(gate=5), False, cg.ERR_UNSUPPORTED),
+    (dict(chunk=48), True, cg.ERR_UNSUPPORTED),
+    (dict(q=(1 << 20) + 2), False, cg.ERR_ALIGNMENT),
+    (dict(state=(7 << 20) + 4), False, cg.ERR_ALIGNMENT),
+    (dict(q_sh=100), False, cg.ERR_ALIGNMENT),
+    (dict(v_st=12), True, cg.ERR_ALIGNMENT),
+    (dict(g_sb=2), False, cg.ERR_ALIGNMENT),
+    (dict(o_sb=-8), False, cg.ERR_ALIGNMENT),
+])
+def test_validation_rejects(lib, kw, prefill, code):
+    A = _args(**kw)
+    assert cg.validate(A, prefill) == code
+    # the entry points return the same code without touching the GPU
+    if prefill:
+        assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == code
+        assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 0
+    else:
+        assert lib.cgdr_decode(ctypes.byref(A), None) == code
+
+
+def test_empty_work_is_a_no_op(lib):
+    # B == 0 or T == 0: nothing to do, pointers may be NULL, no launch happens
+    A = _args(B=0, q=0, k=0, v=0, o=0, g=0, beta=0, state=0)
+    assert lib.cgdr_decode(ctypes.byref(A), None) == cg.OK
+    A = _args(T=0, q=0, k=0, v=0, o=0, g=0, beta=0, state=0)
+    assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.OK
+    assert lib.cgdr_validate(None, 0) == cg.ERR_INVALID_ARG
+
+
+def test_token_strides_ignored_by_decode(lib):
+    assert cg.validate(_args(q_st=3, v_st=5, o_st=1, g_st=7), False) == cg.OK
