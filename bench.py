@@ -39,12 +39,13 @@ METRIC = "decode state GB/s (% HBM peak) at B=64; prefill tokens/s at T=4000, 32
 DEC = dict(B=64, H=32, dk=128, dv=128)
 PRE = dict(B=1, H=32, T=4000, dk=128, dv=128, chunk=64)
 DEC_STATE_BYTES = 2 * DEC["B"] * DEC["H"] * DEC["dk"] * DEC["dv"] * 4           # 268,435,456
-# prefill algorithmic bytes: q,k,v bf16 + g fp32 + beta fp32 + o bf16 + state in and out fp32
-PRE_BYTES = (PRE["B"] * PRE["T"] * PRE["H"] * (3 * 128 * 2 + 128 * 4 + 4 + 128 * 2)
-             + 2 * PRE["B"] * PRE["H"] * 128 * 128 * 4)                           # 201,314,304
+# prefill algorithmic bytes: q,k,v bf16 + g fp32 + beta fp32 + o fp32 + state in and out fp32
+PRE_BYTES = (PRE["B"] * PRE["T"] * PRE["H"] * (3 * 128 * 2 + 128 * 4 + 4 + 128 * 4)
+             + 2 * PRE["B"] * PRE["H"] * 128 * 128 * 4)                           # 234,082,304
 # prefill tensor flops per token-head: 10*C*d (intra-chunk) + 6*dk*dv (carry)
 PRE_FLOPS = PRE["B"] * PRE["T"] * PRE["H"] * (10 * PRE["chunk"] * 128 + 6 * 128 * 128)
 L2_FLUSH_BYTES = 256 << 20
+PREFILL_KERNEL = ("prefill_simt_kernel", "prefill_simt.cu")   # (kernel name, source file)
 
 
 def _peaks():
@@ -150,10 +151,10 @@ def run_ours(args, rank, world, local_rank):
     dsteps = 16                                   # distinct decode inputs, cycled
     dinp = make_inputs(wd, T=dsteps, device=dev, seed=wd.seed + 97 * rank)
     dstate = dinp["S0"].clone()
-    dout = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.bfloat16, device=dev)
+    dout = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.float32, device=dev)
     pinp = make_inputs(wp, device=dev, seed=wp.seed + 97 * rank)
     pstate = torch.zeros_like(pinp["S0"])
-    pout = torch.empty_like(pinp["v"])
+    pout = torch.empty(pinp["v"].shape, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def decode(i):
@@ -207,7 +208,7 @@ def run_ours(args, rank, world, local_rank):
     pre_launch_s = statistics.mean(pre_ms) / 1e3
     pre_ach = PRE_BYTES / pre_launch_s / 1e9
     dec_ach = DEC_STATE_BYTES / dec_launch_s / 1e9
-    tr_pre = _traffic("prefill_tc_kernel", "prefill_tc.cu")
+    tr_pre = _traffic(*PREFILL_KERNEL)
     tr_dec = _traffic("decode_kernel", "decode.cu")
     out = {
         "metric": METRIC, "value": round(dec_gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -216,14 +217,15 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": "decode_b64 + prefill_t4000",
                    "decode": {"B": 64, "H": 32, "dk": 128, "dv": 128, "state": "fp32", "inputs": "bf16",
                               "gate": "per-channel fp32"},
-                   "prefill": {"B": 1, "H": 32, "T": 4000, "dk": 128, "dv": 128, "chunk": 64, "inputs": "bf16"},
+                   "prefill": {"B": 1, "H": 32, "T": 4000, "dk": 128, "dv": 128, "chunk": 64, "inputs": "bf16",
+                               "o": "fp32"},
                    "l2": "flushed (256 MiB write) before every kernel, outside the timed brackets",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_hbm_peak": round(100.0 * dec_gbs / world / hbm, 2),
         "prefill": {"metric": "prefill tokens/s at T=4000, 32 heads", "value": round(pre_tps, 1),
                     "unit": "tokens/s", "ms_per_launch": round(pre_launch_s * 1e3, 5)},
         "decode_ms_per_launch": round(dec_launch_s * 1e3, 5),
-        "roofline": {"kernel": "prefill_tc_kernel", "bound": "hbm", "achieved": round(pre_ach, 2), "peak": hbm,
+        "roofline": {"kernel": PREFILL_KERNEL[0], "bound": "hbm", "achieved": round(pre_ach, 2), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(pre_ach / hbm, 4),
                      "traffic": tr_pre, "algorithmic_bytes": PRE_BYTES,
                      "tensor_flops": PRE_FLOPS, "tensor_frac": round(PRE_FLOPS / pre_launch_s / 1e12 / tflops, 4)},
@@ -245,7 +247,7 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
     # decode: per step copy q, k, v, g, beta in and o out
     h = {k: dinp[k][:, 0].contiguous().cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
     d = {k: torch.empty_like(h[k], device=dev) for k in h}
-    ho = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.bfloat16).pin_memory()
+    ho = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.float32).pin_memory()
     do = torch.empty_like(ho, device=dev)
     h2d_dec = sum(x.numel() * x.element_size() for x in h.values())
     d2h_dec = ho.numel() * ho.element_size()
@@ -259,7 +261,7 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
     # prefill: copy q, k, v, g, beta in and o out
     hp = {k: pinp[k].contiguous().cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
     dp = {k: torch.empty_like(hp[k], device=dev) for k in hp}
-    hpo = torch.empty(pinp["v"].shape, dtype=torch.bfloat16).pin_memory()
+    hpo = torch.empty(pinp["v"].shape, dtype=torch.float32).pin_memory()
     dpo = torch.empty_like(hpo, device=dev)
     ps = torch.zeros_like(pinp["S0"])
     h2d_pre = sum(x.numel() * x.element_size() for x in hp.values())

@@ -34,7 +34,8 @@ class CgdrArgs(ctypes.Structure):
         ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32),
         ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("gate", ctypes.c_int32), ("l2norm_qk", ctypes.c_int32),
-        ("chunk", ctypes.c_int32), ("q_scale", ctypes.c_float), ("eps", ctypes.c_float),
+        ("chunk", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
+        ("q_scale", ctypes.c_float), ("eps", ctypes.c_float),
         ("q", ctypes.c_void_p), ("q_sb", _i64), ("q_st", _i64), ("q_sh", _i64),
         ("k", ctypes.c_void_p), ("k_sb", _i64), ("k_st", _i64), ("k_sh", _i64),
         ("v", ctypes.c_void_p), ("v_sb", _i64), ("v_st", _i64), ("v_sh", _i64),
@@ -132,6 +133,7 @@ def make_args(q, k, v, state, o, *, T, g=None, beta=None, a=None, b=None, A_log=
     Hv, dv = v.shape[2], v.shape[3]
     A.B, A.T, A.Hk, A.Hv, A.dk, A.dv = B, T, Hk, Hv, dk, dv
     A.dtype = _dtype_code(q)
+    A.o_dtype = _dtype_code(o)
     A.gate = GATE_CHANNEL if g is not None else GATE_GDN
     A.l2norm_qk = 1 if l2norm else 0
     A.chunk = int(chunk)
@@ -162,8 +164,10 @@ def make_args(q, k, v, state, o, *, T, g=None, beta=None, a=None, b=None, A_log=
 def _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias):
     import torch
     _need_cuda(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
-    if k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype:
-        raise TypeError("q, k, v and o must share one dtype")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if o.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("o must be float32 or bfloat16")
     if state.dtype != torch.float32:
         raise TypeError("state must be float32")
     for name, t in (("g", g), ("beta", beta), ("A_log", A_log), ("dt_bias", dt_bias)):
@@ -178,10 +182,11 @@ def decode(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=N
            l2norm=True, q_scale=None, eps=None, stream=None):
     """One decode step.  q, k ``[B,Hk,dk]``; v ``[B,Hv,dv]``; state ``[B,Hv,dk,dv]`` fp32
     (updated in place); gate ``g [B,Hv,dk]`` + ``beta [B,Hv]`` or ``a, b [B,Hv]`` +
-    ``A_log, dt_bias [Hv]``.  Returns o ``[B,Hv,dv]`` in q's dtype."""
+    ``A_log, dt_bias [Hv]``.  Returns o ``[B,Hv,dv]``: the given ``o`` (fp32 or bf16) or a
+    new fp32 tensor."""
     import torch
     if o is None:
-        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+        o = torch.empty(v.shape, dtype=torch.float32, device=v.device)
     _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
     u = lambda t: None if t is None else t.unsqueeze(1)
     A = make_args(u(q), u(k), u(v), state, u(o), T=1, g=u(g), beta=u(beta), a=u(a), b=u(b),
@@ -199,10 +204,11 @@ def prefill(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=
             l2norm=True, q_scale=None, eps=None, chunk=64, workspace=None, stream=None):
     """Chunked prefill.  q, k ``[B,T,Hk,dk]``; v ``[B,T,Hv,dv]``; state ``[B,Hv,dk,dv]``
     fp32 (updated in place); gate ``g [B,T,Hv,dk]`` + ``beta [B,T,Hv]`` or
-    ``a, b [B,T,Hv]`` + ``A_log, dt_bias [Hv]``.  Returns o ``[B,T,Hv,dv]``."""
+    ``a, b [B,T,Hv]`` + ``A_log, dt_bias [Hv]``.  Returns o ``[B,T,Hv,dv]``: the given ``o``
+    (fp32 or bf16) or a new fp32 tensor."""
     import torch
     if o is None:
-        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+        o = torch.empty(v.shape, dtype=torch.float32, device=v.device)
     _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
     A = make_args(q, k, v, state, o, T=q.shape[1], g=g, beta=beta, a=a, b=b, A_log=A_log, dt_bias=dt_bias,
                   l2norm=l2norm, q_scale=q_scale, eps=eps, chunk=chunk)

@@ -19,6 +19,7 @@ cgdr_status check(const cgdr_args *a, bool prefill) {
     if (!prefill && a->T != 1) return CGDR_ERR_INVALID_ARG;
     if (!dim_ok(a->dk) || !dim_ok(a->dv)) return CGDR_ERR_UNSUPPORTED;
     if (a->dtype != CGDR_F32 && a->dtype != CGDR_BF16) return CGDR_ERR_UNSUPPORTED;
+    if (a->o_dtype != CGDR_F32 && a->o_dtype != CGDR_BF16) return CGDR_ERR_UNSUPPORTED;
     if (a->gate != CGDR_GATE_CHANNEL && a->gate != CGDR_GATE_GDN) return CGDR_ERR_UNSUPPORTED;
     if (prefill && !(a->chunk == 0 || a->chunk == 16 || a->chunk == 32 || a->chunk == 64))
         return CGDR_ERR_UNSUPPORTED;
@@ -31,6 +32,7 @@ cgdr_status check(const cgdr_args *a, bool prefill) {
 
     const size_t esz = a->dtype == CGDR_BF16 ? 2 : 4;
     const int64_t vec = (int64_t)(16 / esz);
+    const int64_t ovec = a->o_dtype == CGDR_BF16 ? 8 : 4;
     // decode ignores the token strides
     const int64_t q_st = prefill ? a->q_st : 0, k_st = prefill ? a->k_st : 0;
     const int64_t v_st = prefill ? a->v_st : 0, o_st = prefill ? a->o_st : 0;
@@ -40,7 +42,7 @@ cgdr_status check(const cgdr_args *a, bool prefill) {
         !aligned(a->state, 16))
         return CGDR_ERR_ALIGNMENT;
     if (!strides_ok(a->q_sb, q_st, a->q_sh, vec) || !strides_ok(a->k_sb, k_st, a->k_sh, vec) ||
-        !strides_ok(a->v_sb, v_st, a->v_sh, vec) || !strides_ok(a->o_sb, o_st, a->o_sh, vec))
+        !strides_ok(a->v_sb, v_st, a->v_sh, vec) || !strides_ok(a->o_sb, o_st, a->o_sh, ovec))
         return CGDR_ERR_ALIGNMENT;
     if (a->gate == CGDR_GATE_CHANNEL) {
         if (!aligned(a->g, 16) || !strides_ok(a->g_sb, g_st, a->g_sh, 4)) return CGDR_ERR_ALIGNMENT;
@@ -83,20 +85,15 @@ cgdr_status cgdr_decode(const cgdr_args *a, void *stream) {
 
 size_t cgdr_prefill_workspace_size(const cgdr_args *a) {
     if (check(a, true) != CGDR_OK) return 0;
-    if (cgdr::prefill_tc_supported(*a)) return cgdr::prefill_tc_workspace(*a);
     return 0;
 }
 
 cgdr_status cgdr_prefill(const cgdr_args *a, void *ws, size_t ws_bytes, void *stream) {
     cgdr_status st = check(a, true);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cgdr::prefill_tc_supported(*a)) {
-        const size_t need = cgdr::prefill_tc_workspace(*a);
-        if (need > 0 && (ws == nullptr || ws_bytes < need)) return CGDR_ERR_WORKSPACE;
-        return cgdr::launch_prefill_tc(*a, ws, ws_bytes, s);
-    }
-    return cgdr::launch_prefill_simt(*a, s);
+    (void)ws;
+    (void)ws_bytes;
+    return cgdr::launch_prefill_simt(*a, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -19,7 +19,7 @@ namespace cgdr {
 namespace {
 
 struct DecodeParams {
-    int Hk, Hv, l2norm, gate;
+    int Hk, Hv, l2norm, gate, o_f32;
     float q_scale, eps;
     const void *q, *k, *v;
     int64_t q_sb, q_sh, k_sb, k_sh, v_sb, v_sh;
@@ -193,7 +193,11 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 2) decode_kernel(cons
             const float4 y = s_red[w][c];
             t.x += y.x; t.y += y.y; t.z += y.z; t.w += y.w;
         }
-        store4<T>(static_cast<T *>(p.o) + b * p.o_sb + h * p.o_sh + 4 * c, t);
+        const int64_t off = b * p.o_sb + h * p.o_sh + 4 * c;
+        if (p.o_f32)
+            store4<float>(static_cast<float *>(p.o) + off, t);
+        else
+            store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(p.o) + off, t);
     }
 }
 
@@ -219,7 +223,7 @@ cgdr_status launch_dtype(const DecodeParams &p, int dk, int dv, int units, cudaS
 
 cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s) {
     DecodeParams p;
-    p.Hk = a.Hk; p.Hv = a.Hv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate;
+    p.Hk = a.Hk; p.Hv = a.Hv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate; p.o_f32 = a.o_dtype == CGDR_F32;
     p.q_scale = qscale_of(a); p.eps = eps_of(a);
     p.q = a.q; p.k = a.k; p.v = a.v;
     p.q_sb = a.q_sb; p.q_sh = a.q_sh; p.k_sb = a.k_sb; p.k_sh = a.k_sh; p.v_sb = a.v_sb; p.v_sh = a.v_sh;

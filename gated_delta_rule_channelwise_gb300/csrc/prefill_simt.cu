@@ -25,7 +25,7 @@ constexpr int SIMT_WS = 32;     // dv columns per CTA
 constexpr int SIMT_NT = 256;
 
 struct PrefillParams {
-    int T, Hk, Hv, dv, l2norm, gate;
+    int T, Hk, Hv, dv, l2norm, gate, o_f32;
     float q_scale, eps;
     const void *q, *k, *v;
     int64_t q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh;
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(SIMT_NT) prefill_simt_kernel(const PrefillPara
     const T *qb = static_cast<const T *>(p.q) + b * p.q_sb + hk * p.q_sh;
     const T *kb = static_cast<const T *>(p.k) + b * p.k_sb + hk * p.k_sh;
     const T *vb = static_cast<const T *>(p.v) + b * p.v_sb + h * p.v_sh + col0;
-    T *ob = static_cast<T *>(p.o) + b * p.o_sb + h * p.o_sh + col0;
+    const int64_t obase = b * p.o_sb + h * p.o_sh + col0;
 
     for (int t0 = 0; t0 < p.T; t0 += C) {
         const int L = min(C, p.T - t0);
@@ -211,7 +211,11 @@ __global__ void __launch_bounds__(SIMT_NT) prefill_simt_kernel(const PrefillPara
             float acc = 0.f;
             for (int i = 0; i < DK; ++i) acc = fmaf(sQ[r * DK + i], sS[i * WS + j], acc);
             for (int s = 0; s <= r; ++s) acc = fmaf(sP[r * LC + s], sV[s * WS + j], acc);
-            ob[(int64_t)(t0 + r) * p.o_st + j] = Cvt<T>::from_f(acc);
+            const int64_t off = obase + (int64_t)(t0 + r) * p.o_st + j;
+            if (p.o_f32)
+                static_cast<float *>(p.o)[off] = acc;
+            else
+                static_cast<__nv_bfloat16 *>(p.o)[off] = __float2bfloat16_rn(acc);
         }
         __syncthreads();
         // ---- S = e^gamma_C S + (K e^(gamma_C - gamma))^T U
@@ -256,6 +260,7 @@ cgdr_status launch_dtype(const PrefillParams &p, int B, int dk, int C, cudaStrea
 cgdr_status launch_prefill_simt(const cgdr_args &a, cudaStream_t s) {
     PrefillParams p;
     p.T = a.T; p.Hk = a.Hk; p.Hv = a.Hv; p.dv = a.dv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate;
+    p.o_f32 = a.o_dtype == CGDR_F32;
     p.q_scale = qscale_of(a); p.eps = eps_of(a);
     p.q = a.q; p.k = a.k; p.v = a.v;
     p.q_sb = a.q_sb; p.q_st = a.q_st; p.q_sh = a.q_sh;

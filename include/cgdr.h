@@ -27,9 +27,13 @@
  *    beta = sigmoid(b); softplus(x) = x for x > 20.
  *  - state: fp32 [B,Hv,dk,dv], dense (dv fastest), updated in place.
  *    A zero-filled state is the zero initial state.
- *  - o: [B,T,Hv,dv] in `dtype`, accumulated in fp32.
+ *  - o: [B,T,Hv,dv] in `o_dtype` (fp32 or bf16, independent of the input
+ *    dtype), accumulated in fp32.  The pages do not fix the output type; a
+ *    bf16 o carries up to half a bf16 ulp of rounding on top of the
+ *    computation.
  *  - q, k, v, o: 16-byte aligned base pointers; batch/token/head strides
- *    multiples of 8 elements (bf16) or 4 elements (fp32).  g: 16-byte
+ *    multiples of 8 elements (bf16) or 4 elements (fp32), by each tensor's
+ *    own dtype.  g: 16-byte
  *    aligned, strides multiples of 4.  state: 16-byte aligned.
  *  - No input may alias `state` or `o`.
  *
@@ -76,6 +80,7 @@ typedef struct cgdr_args {
     int32_t gate;                   /* cgdr_gate */
     int32_t l2norm_qk;              /* nonzero: L2-normalise q and k (the usual setting) */
     int32_t chunk;                  /* prefill chunk length 16, 32 or 64; 0 selects 64 */
+    int32_t o_dtype;                /* cgdr_dtype of o; zero-initialised = CGDR_F32 */
     float q_scale;                  /* applied to q after the norm; <= 0 selects 1/sqrt(dk) */
     float eps;                      /* added to |x|^2 in the L2 norm; < 0 selects 1e-6 */
     const void *q;     int64_t q_sb, q_st, q_sh;        /* [B,T,Hk,dk] */
@@ -88,7 +93,7 @@ typedef struct cgdr_args {
     const float *A_log;                                 /* [Hv]        (GDN) */
     const float *dt_bias;                               /* [Hv]        (GDN) */
     float *state;                                       /* [B,Hv,dk,dv] in/out */
-    void *o;           int64_t o_sb, o_st, o_sh;        /* [B,T,Hv,dv] out */
+    void *o;           int64_t o_sb, o_st, o_sh;        /* [B,T,Hv,dv] out, o_dtype */
 } cgdr_args;
 
 /* ABI version of the loaded library (CGDR_ABI_VERSION it was built with). */
@@ -131,13 +136,10 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
  * (UT) transform, WY pseudo-keys and pseudo-values, and the inter-chunk
  * state carry, with a ragged last chunk handled by the same code.
  * T == 0 is a no-op.  The result equals T applications of the token
- * recurrence up to rounding, for every chunk length.  bf16 inputs with
- * dk = dv = 128 and chunk 64 run on the tensor cores; other cases run an
- * fp32 CUDA-core kernel of the same chunked form.
- * `workspace` may be NULL when cgdr_prefill_workspace_size() returns 0.
- * Numerical range: within a chunk, the log-decay summed over any 15
- * consecutive tokens must stay above -80 on every channel (the tensor-core
- * path forms exp of such sums); the fp32 path has no such limit.
+ * recurrence up to rounding, for every chunk length.  All contractions run
+ * in fp32 (pairwise decays as exponentials of differences, so any decay is
+ * in range).  `workspace` may be NULL when cgdr_prefill_workspace_size()
+ * returns 0.
  */
 cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspace_bytes, void *stream);
 

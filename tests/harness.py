@@ -76,10 +76,11 @@ def gather_units(x: torch.Tensor, units, head_dim: int):
     return torch.cat(out).cpu()
 
 
-def decode_steps(cg, inp: dict, steps: int, state: torch.Tensor, *, l2norm=True, q_scale=None):
+def decode_steps(cg, inp: dict, steps: int, state: torch.Tensor, *, l2norm=True, q_scale=None,
+                 o_dtype=torch.float32):
     """Run `steps` decode calls over the token axis of `inp`; returns o [B, steps, Hv, dv]."""
     B, _, Hv, dv = inp["v"].shape
-    o = torch.empty(B, steps, Hv, dv, dtype=inp["v"].dtype, device=inp["v"].device)
+    o = torch.empty(B, steps, Hv, dv, dtype=o_dtype, device=inp["v"].device)
     for t in range(steps):
         kw = {}
         if "g" in inp:

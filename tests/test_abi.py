@@ -101,6 +101,8 @@ def test_validation_accepts_good_args(lib):
     (dict(dtype=7), False, cg.ERR_UNSUPPORTED),
     (dict(gate=5), False, cg.ERR_UNSUPPORTED),
     (dict(chunk=48), True, cg.ERR_UNSUPPORTED),
+    (dict(o_dtype=3), False, cg.ERR_UNSUPPORTED),
+    (dict(o_dtype=cg.BF16, o_sh=132), False, cg.ERR_ALIGNMENT),   # bf16 o: strides of 8 elements
     (dict(q=(1 << 20) + 2), False, cg.ERR_ALIGNMENT),
     (dict(state=(7 << 20) + 4), False, cg.ERR_ALIGNMENT),
     (dict(q_sh=100), False, cg.ERR_ALIGNMENT),
@@ -126,6 +128,11 @@ def test_empty_work_is_a_no_op(lib):
     A = _args(T=0, q=0, k=0, v=0, o=0, g=0, beta=0, state=0)
     assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.OK
     assert lib.cgdr_validate(None, 0) == cg.ERR_INVALID_ARG
+
+
+def test_output_dtype_strides(lib):
+    assert cg.validate(_args(o_dtype=cg.F32, o_sh=132), False) == cg.OK     # fp32 o: 4-element strides
+    assert cg.validate(_args(o_dtype=cg.BF16, o_sh=136), False) == cg.OK
 
 
 def test_token_strides_ignored_by_decode(lib):

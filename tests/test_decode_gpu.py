@@ -32,6 +32,7 @@ def _run_and_compare(w: Workload, steps: int, units=None, l2norm=True, q_scale=N
         state = torch.cat([state[b:b + 1, h:h + 1] for b, h in units])
     tol = TOL[w.torch_dtype]
     eo, es = rel_err(o, o_ref), rel_err(state, S_ref)
+    print("[parity] %s steps=%d dk=%d dv=%d err_o=%.3e err_S=%.3e" % (w.name, steps, w.dk, w.dv, eo, es))
     assert eo <= tol, ("o", eo)
     assert es <= tol, ("state", es)
     return eo, es
@@ -96,3 +97,16 @@ def test_identity_gate_keeps_state_exactly():
               g=torch.zeros_like(inp["g"][:, 0]), beta=torch.zeros_like(inp["beta"][:, 0]))
     torch.cuda.synchronize()
     assert torch.equal(state, inp["S0"])
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (32, 64)])
+def test_bf16_output_is_the_rounded_fp32_output(dk, dv):
+    """o in bf16 is exactly the fp32 result rounded to nearest (same kernel, same inputs)."""
+    w = Workload("obf", B=5, Hk=2, Hv=4, dk=dk, dv=dv, T=3, dtype="bf16", gate="channel", seed=19)
+    inp = make_inputs(w, device="cuda")
+    s1, s2 = inp["S0"].clone(), inp["S0"].clone()
+    o32 = decode_steps(cg, inp, 3, s1)
+    o16 = decode_steps(cg, inp, 3, s2, o_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s2)
+    assert torch.equal(o16, o32.to(torch.bfloat16))

@@ -37,6 +37,7 @@ def _check(w, inp, o, state, units=None, tol=None):
         state = torch.cat([state[b:b + 1, h:h + 1] for b, h in units])
     tol = tol or TOL[w.torch_dtype]
     eo, es = rel_err(o, o_ref), rel_err(state, S_ref)
+    print("[parity] %s T=%d dv=%d err_o=%.3e err_S=%.3e" % (w.name, o.shape[1], w.dv, eo, es))
     assert eo <= tol, ("o", eo)
     assert es <= tol, ("state", es)
     return eo, es
@@ -122,6 +123,8 @@ def test_prefill_long_then_decode_sampled():
     got_t = torch.cat([o_tail[b:b + 1, :, h:h + 1] for b, h in units])
     got_S = torch.cat([s[b:b + 1, h:h + 1] for b, h in units])
     tol = TOL[torch.bfloat16]
+    print("[parity] prefill_long err_o=%.3e tail_o=%.3e S=%.3e" % (
+        rel_err(got_o, o_ref), rel_err(got_t, tail_ref_o), rel_err(got_S, tail_ref_S)))
     assert rel_err(got_o, o_ref) <= tol
     assert rel_err(got_t, tail_ref_o) <= tol
     assert rel_err(got_S, tail_ref_S) <= tol
@@ -156,3 +159,16 @@ def test_zero_length_is_noop():
     s = inp["S0"].clone()
     _prefill(inp, 64, state=s)
     assert torch.equal(s, inp["S0"])
+
+
+@pytest.mark.parametrize("dtype,chunk", [("bf16", 64), ("bf16", 32), ("f32", 16)])
+def test_bf16_output_is_the_rounded_fp32_output(dtype, chunk):
+    w = Workload("obf", B=1, Hk=2, Hv=2, dk=128, dv=128, T=77, dtype=dtype, gate="channel", seed=23)
+    inp = make_inputs(w, device="cuda")
+    o32, s1 = _prefill(inp, chunk)
+    o16 = torch.empty(o32.shape, dtype=torch.bfloat16, device="cuda")
+    s2 = inp["S0"].clone()
+    cg.prefill(inp["q"], inp["k"], inp["v"], s2, o16, chunk=chunk, **gate_kwargs(inp))
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s2)
+    assert torch.equal(o16, o32.to(torch.bfloat16))
