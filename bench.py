@@ -45,7 +45,7 @@ PRE_BYTES = (PRE["B"] * PRE["T"] * PRE["H"] * (3 * 128 * 2 + 128 * 4 + 4 + 128 *
 # prefill tensor flops per token-head: 10*C*d (intra-chunk) + 6*dk*dv (carry)
 PRE_FLOPS = PRE["B"] * PRE["T"] * PRE["H"] * (10 * PRE["chunk"] * 128 + 6 * 128 * 128)
 L2_FLUSH_BYTES = 256 << 20
-PREFILL_KERNEL = ("prefill_simt_kernel", "prefill_simt.cu")   # (kernel name, source file)
+PREFILL_KERNEL = ("prefill_tc05_kernel", "prefill_tc05.cu")   # (kernel name, source file)
 
 
 def _peaks():

@@ -60,6 +60,7 @@ _SIGNATURES = [
     ("cgdr_decode", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p]),
     ("cgdr_prefill_workspace_size", ctypes.c_size_t, [ctypes.POINTER(CgdrArgs)]),
     ("cgdr_prefill", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    ("cgdr_workspace_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
 ]
 
 
@@ -223,9 +224,14 @@ def prefill(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=
     return o
 
 
+def workspace_status(workspace, stream=None) -> int:
+    """Device-side status word a prefill left in its workspace (synchronises the stream)."""
+    return int(lib().cgdr_workspace_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(stream)))
+
+
 def validate(A: CgdrArgs, for_prefill: bool) -> int:
     return int(lib().cgdr_validate(ctypes.byref(A), 1 if for_prefill else 0))
 
 
-__all__ = ["decode", "prefill", "prefill_workspace_size", "validate", "status_string", "make_args",
+__all__ = ["decode", "prefill", "prefill_workspace_size", "workspace_status", "validate", "status_string", "make_args",
            "CgdrArgs", "CgdrError", "lib", "LIB_PATH"]

@@ -84,16 +84,31 @@ cgdr_status cgdr_decode(const cgdr_args *a, void *stream) {
 }
 
 size_t cgdr_prefill_workspace_size(const cgdr_args *a) {
-    if (check(a, true) != CGDR_OK) return 0;
+    if (check(a, true) != CGDR_OK || a->B == 0 || a->T == 0) return 0;
+    if (cgdr::prefill_tc05_supported(*a)) return cgdr::prefill_tc05_workspace(*a);
     return 0;
 }
 
 cgdr_status cgdr_prefill(const cgdr_args *a, void *ws, size_t ws_bytes, void *stream) {
     cgdr_status st = check(a, true);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
-    (void)ws;
-    (void)ws_bytes;
-    return cgdr::launch_prefill_simt(*a, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cgdr::prefill_tc05_supported(*a)) {
+        const size_t need = cgdr::prefill_tc05_workspace(*a);
+        if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
+        return cgdr::launch_prefill_tc05(*a, ws, s);
+    }
+    return cgdr::launch_prefill_simt(*a, s);
+}
+
+cgdr_status cgdr_workspace_status(const void *ws, void *stream) {
+    if (ws == nullptr) return CGDR_ERR_INVALID_ARG;
+    int word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CGDR_ERR_CUDA;
+    return word == 0 ? CGDR_OK : static_cast<cgdr_status>(word);
 }
 
 }  // extern "C"

@@ -136,12 +136,24 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
  * (UT) transform, WY pseudo-keys and pseudo-values, and the inter-chunk
  * state carry, with a ragged last chunk handled by the same code.
  * T == 0 is a no-op.  The result equals T applications of the token
- * recurrence up to rounding, for every chunk length.  All contractions run
- * in fp32 (pairwise decays as exponentials of differences, so any decay is
- * in range).  `workspace` may be NULL when cgdr_prefill_workspace_size()
- * returns 0.
+ * recurrence up to rounding, for every chunk length.
+ * Paths: bf16 inputs with dk = dv = 128 and chunk 64 run the tensor-core
+ * kernel (tcgen05, TF32 operands, fp32 accumulation and state; one CTA per
+ * (batch, v-head)); every other case runs an fp32 CUDA-core kernel.
+ * Workspace: the tensor-core path needs cgdr_prefill_workspace_size() bytes
+ * (16-byte aligned); its first int32 is set to CGDR_ERR_TIMEOUT if a bounded
+ * device wait gave up (see cgdr_workspace_status).  `workspace` may be NULL
+ * when the size is 0.  Returns CGDR_ERR_WORKSPACE if it is too small.
  */
 cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Waits for `stream`, then reports the device-side status a cgdr_prefill
+ * call left in `workspace`: CGDR_OK, or CGDR_ERR_TIMEOUT if one of its
+ * bounded waits on the tensor core gave up (its outputs are then invalid).
+ * Returns CGDR_ERR_CUDA if the copy or the synchronisation fails.
+ */
+cgdr_status cgdr_workspace_status(const void *workspace, void *stream);
 
 #ifdef __cplusplus
 }

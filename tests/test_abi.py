@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     assert declared_functions() == sorted([
         "cgdr_abi_version", "cgdr_status_string", "cgdr_validate", "cgdr_decode",
-        "cgdr_prefill_workspace_size", "cgdr_prefill"])
+        "cgdr_prefill_workspace_size", "cgdr_prefill", "cgdr_workspace_status"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -128,6 +128,18 @@ def test_empty_work_is_a_no_op(lib):
     A = _args(T=0, q=0, k=0, v=0, o=0, g=0, beta=0, state=0)
     assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.OK
     assert lib.cgdr_validate(None, 0) == cg.ERR_INVALID_ARG
+
+
+def test_workspace_rules(lib):
+    A = _args(T=100)
+    assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 256     # tensor-core path: error word
+    assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
+    assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(1 << 30), 64, None) == cg.ERR_WORKSPACE
+    assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p((1 << 30) + 4), 256, None) == cg.ERR_WORKSPACE
+    A32 = _args(T=100, dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128)
+    assert lib.cgdr_prefill_workspace_size(ctypes.byref(A32)) == 0      # fp32 inputs: CUDA-core path
+    assert lib.cgdr_prefill_workspace_size(ctypes.byref(_args(T=100, chunk=32))) == 0
+    assert lib.cgdr_workspace_status(None, None) == cg.ERR_INVALID_ARG
 
 
 def test_output_dtype_strides(lib):

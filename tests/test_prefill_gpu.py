@@ -172,3 +172,27 @@ def test_bf16_output_is_the_rounded_fp32_output(dtype, chunk):
     torch.cuda.synchronize()
     assert torch.equal(s1, s2)
     assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+def test_tensor_core_path_reports_ok_status():
+    """The tensor-core prefill leaves CGDR_OK in its workspace status word."""
+    w = Workload("st", B=1, Hk=1, Hv=1, dk=128, dv=128, T=70, dtype="bf16", gate="channel", seed=4)
+    inp = make_inputs(w, device="cuda")
+    state = inp["S0"].clone()
+    n = cg.prefill_workspace_size(inp["q"], inp["k"], inp["v"], state, torch.empty(inp["v"].shape, device="cuda"),
+                                  **gate_kwargs(inp))
+    assert n == 256
+    ws = torch.full((n,), 0x7F, dtype=torch.uint8, device="cuda")
+    cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, workspace=ws, **gate_kwargs(inp))
+    assert cg.workspace_status(ws) == cg.OK
+
+
+def test_mixed_wide_and_narrow_chunks():
+    """Decay that switches between mild and extreme across chunks (both A/P paths in one call)."""
+    w = Workload("mix", B=1, Hk=2, Hv=2, dk=128, dv=128, T=260, dtype="bf16", gate="channel", seed=31)
+    inp = make_inputs(w, device="cuda")
+    g = inp["g"].clone()
+    g[:, 64:128] *= 12.0          # second chunk: ~ -5 per token on average
+    inp["g"] = g
+    o, s = _prefill(inp, 64)
+    _check(w, inp, o, s)
