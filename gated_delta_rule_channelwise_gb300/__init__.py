@@ -61,6 +61,7 @@ _SIGNATURES = [
     ("cgdr_prefill_workspace_size", ctypes.c_size_t, [ctypes.POINTER(CgdrArgs)]),
     ("cgdr_prefill", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("cgdr_workspace_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("cgdr_prefill_noalloc", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p]),
 ]
 
 
@@ -224,6 +225,20 @@ def prefill(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=
     return o
 
 
+def prefill_noalloc(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
+                    l2norm=True, q_scale=None, eps=None, chunk=64, stream=None):
+    """`prefill` with the library's static scratch instead of a workspace (allocates nothing
+    on the device when ``o`` is given).  Calls that overlap on the GPU race on that scratch."""
+    import torch
+    if o is None:
+        o = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
+    A = make_args(q, k, v, state, o, T=q.shape[1], g=g, beta=beta, a=a, b=b, A_log=A_log, dt_bias=dt_bias,
+                  l2norm=l2norm, q_scale=q_scale, eps=eps, chunk=chunk)
+    _check(lib().cgdr_prefill_noalloc(ctypes.byref(A), _stream_handle(stream)), "cgdr_prefill_noalloc")
+    return o
+
+
 def workspace_status(workspace, stream=None) -> int:
     """Device-side status word a prefill left in its workspace (synchronises the stream)."""
     return int(lib().cgdr_workspace_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(stream)))
@@ -233,5 +248,5 @@ def validate(A: CgdrArgs, for_prefill: bool) -> int:
     return int(lib().cgdr_validate(ctypes.byref(A), 1 if for_prefill else 0))
 
 
-__all__ = ["decode", "prefill", "prefill_workspace_size", "workspace_status", "validate", "status_string", "make_args",
+__all__ = ["decode", "prefill", "prefill_noalloc", "prefill_workspace_size", "workspace_status", "validate", "status_string", "make_args",
            "CgdrArgs", "CgdrError", "lib", "LIB_PATH"]

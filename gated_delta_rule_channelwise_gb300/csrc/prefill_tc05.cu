@@ -23,6 +23,8 @@
 // the CUDA cores from exponentials of differences instead (exact for any
 // decay).  TF32 operands (rounded to nearest) with fp32 accumulation keep the
 // error near 1e-2 of the output RMS or below; the state is carried in fp32.
+#include <mutex>
+
 #include "cgdr_internal.cuh"
 #include "tc05.cuh"
 
@@ -508,3 +510,45 @@ cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s) {
 }
 
 }  // namespace cgdr
+
+// ---------------------------------------------------------------------------
+// Allocation-free prefill: the scratch is this file's static device array.
+namespace cgdr {
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[CGDR_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Address of this device's copy of the static scratch; looked up once per
+// device, with that device current (the caller's current device).
+cgdr_status noalloc_scratch(int dev, void **out) {
+    if (dev < 0 || dev >= kMaxDevices) return CGDR_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return CGDR_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return CGDR_OK;
+}
+
+}  // namespace
+}  // namespace cgdr
+
+extern "C" cgdr_status cgdr_prefill_noalloc(const cgdr_args *a, void *stream) {
+    const cgdr_status st = cgdr_validate(a, 1);
+    if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
+    const size_t need = cgdr_prefill_workspace_size(a);
+    if (need > CGDR_NOALLOC_SCRATCH_BYTES) return CGDR_ERR_WORKSPACE;
+    if (need == 0) return cgdr_prefill(a, nullptr, 0, stream);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CGDR_ERR_CUDA;
+    void *scratch = nullptr;
+    const cgdr_status s2 = cgdr::noalloc_scratch(dev, &scratch);
+    if (s2 != CGDR_OK) return s2;
+    return cgdr_prefill(a, scratch, CGDR_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -155,6 +155,39 @@ cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspac
  */
 cgdr_status cgdr_workspace_status(const void *workspace, void *stream);
 
+/*
+ * Size, in bytes, of the library's static device scratch area used by
+ * cgdr_prefill_noalloc.  Every GPU that loads the library holds this much
+ * device memory until the process exits.
+ */
+#define CGDR_NOALLOC_SCRATCH_BYTES 4096
+
+/*
+ * cgdr_prefill without a caller-provided workspace, for callers that cannot
+ * allocate device memory: runtimes that plan every device buffer ahead of
+ * time and forbid allocation while a model runs, or code on a latency path
+ * where a cudaMalloc (which may synchronise the device) is not acceptable.
+ * This entry point has no counterpart in the method's description; it only
+ * changes where the scratch memory comes from.
+ *
+ * The scratch lives in one file-scope static __device__ array of
+ * CGDR_NOALLOC_SCRATCH_BYTES bytes.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.  The first call on
+ * each device looks up that device's copy of the array (cudaGetSymbolAddress,
+ * with the device current) and caches it; make that first call before any
+ * stream capture.  Every call on a device shares the one array, which keeps
+ * the last call's contents; the call clears what must start at zero before
+ * its kernel runs.  Calls whose kernels overlap on the GPU (other streams,
+ * other host threads) race on the array: serialise them.  A device-side
+ * wait that gives up is recorded only in the static area, so use cgdr_prefill
+ * with a workspace when that status must be read back.
+ *
+ * Arguments and results are those of cgdr_prefill.  Returns
+ * CGDR_ERR_WORKSPACE if the problem needs more scratch than
+ * CGDR_NOALLOC_SCRATCH_BYTES, and CGDR_ERR_CUDA if the set-up lookup fails.
+ */
+cgdr_status cgdr_prefill_noalloc(const cgdr_args *args, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     assert declared_functions() == sorted([
         "cgdr_abi_version", "cgdr_status_string", "cgdr_validate", "cgdr_decode",
-        "cgdr_prefill_workspace_size", "cgdr_prefill", "cgdr_workspace_status"])
+        "cgdr_prefill_workspace_size", "cgdr_prefill", "cgdr_workspace_status", "cgdr_prefill_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(lib):
