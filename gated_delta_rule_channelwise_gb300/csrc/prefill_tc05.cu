@@ -33,7 +33,7 @@ namespace {
 
 using namespace tc05;
 
-constexpr int C = 64, DK = 128, DV = 128, NT = 256;
+constexpr int C = 64, DK = 128, DV = 128, NT = 512;
 constexpr float kRange = 80.f;           // max |gamma_r - gamma_mid| for the tensor-core causal terms
 constexpr uint32_t kSpin = 1u << 20;     // bounded mbarrier wait (iterations)
 
@@ -47,7 +47,7 @@ constexpr int R_G = 180224;              // 16 KB: Xs fp32 [64][64] | Tb [64 x 6
 constexpr int R_MISC = 196608;
 // misc (fp32 unless noted)
 constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BETA + 256;
-constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 512, M_GC = M_GM + 512, M_DEC = M_GC + 512;
+constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = M_GC + 512;
 constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_END = M_TMEM + 8;
 constexpr int SMEM_BYTES = M_END + 1024;                 // + alignment slack
 constexpr int LDA = 65;                  // fp32 A rows (padded)
@@ -78,6 +78,11 @@ __device__ __forceinline__ float *f32p(char *base, int off) { return reinterpret
 __device__ __forceinline__ void st_tile(char *base, int region, int R, int r, int k, float x) {
     *reinterpret_cast<float *>(base + region + sw_off(R, r, k)) = tf32r(x);
 }
+// Four consecutive K elements (k0 % 4 == 0) of row r: one 16-byte chunk of the swizzled tile.
+__device__ __forceinline__ void st_tile4(char *base, int region, int R, int r, int k0, float a, float b, float c,
+                                         float d) {
+    *reinterpret_cast<float4 *>(base + region + sw_off(R, r, k0)) = make_float4(tf32r(a), tf32r(b), tf32r(c), tf32r(d));
+}
 __device__ __forceinline__ float ld_tile(const char *base, int region, int R, int r, int k) {
     return *reinterpret_cast<const float *>(base + region + sw_off(R, r, k));
 }
@@ -87,7 +92,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
     char *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sbase = smem_u32(sm);
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
-    float *sH0 = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
+    float *sQt = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
     float *sA = f32p(sm, A1_A32), *sY = f32p(sm, A1_Y), *sXs = f32p(sm, R_G);
     const uint32_t mbar = sbase + M_MBAR;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + M_TMEM);
@@ -95,8 +100,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
     const int h = blockIdx.x, b = blockIdx.y;
     const int hk = h / (p.Hv / p.Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wq = warp & 3, wh = warp >> 2;                 // TMEM lane quarter, column half
-    const int ci = tid & 127, chalf = tid >> 7;              // channel (or column) and row half
+    const int wq = warp & 3, wc = warp >> 2;                 // TMEM lane quarter, column quarter
+    const int ci = tid & 127, cq = tid >> 7;                 // channel (or column), row quarter (16 rows)
     const __nv_bfloat16 *qb = p.q + b * p.q_sb + hk * p.q_sh;
     const __nv_bfloat16 *kb = p.k + b * p.k_sb + hk * p.k_sh;
     const __nv_bfloat16 *vb = p.v + b * p.v_sb + h * p.v_sh;
@@ -114,17 +119,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    const int trow = 32 * wq + lane;                         // this thread's TMEM lane / tile row
 
-    // state -> D0 = S^T: thread owns row j = 32 wq + lane, columns i in [64 wh, 64 wh + 64)
+    // state -> D0 = S^T: row j = trow, columns i in [32 wc, 32 wc + 32)
     {
-        const int j = 32 * wq + lane;
+        float v[32];
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float v[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(64 * wh + 32 * part + c) * DV + j];
-            tmem_st32(tmem + lane_off + T_D0 + 64 * wh + 32 * part, v);
-        }
+        for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(32 * wc + c) * DV + trow];
+        tmem_st32(tmem + lane_off + T_D0 + 32 * wc, v);
     }
     fence_before_sync();
     __syncthreads();
@@ -156,27 +158,37 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
                 if (ptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
             }
         }
-        // row norms, beta, scalar gate
-#pragma unroll 2
-        for (int jj = 0; jj < 8; ++jj) {
-            const int r = 8 * warp + jj;
-            float sq = 0.f, sk = 0.f;
-            if (r < L) {
-                const int64_t t = t0 + r;
-                const uint2 qr = *reinterpret_cast<const uint2 *>(qb + t * p.q_st + 4 * lane);
-                const uint2 kr = *reinterpret_cast<const uint2 *>(kb + t * p.k_st + 4 * lane);
-                const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr.x));
-                const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr.y));
-                const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.x));
-                const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.y));
-                sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
-                sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+        // row norms (a warp per 4 rows); raw q/k rows staged (bf16) in regions F and G
+        {
+            uint2 qr[4], kr[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int r = 4 * warp + jj;
+                qr[jj] = make_uint2(0u, 0u);
+                kr[jj] = make_uint2(0u, 0u);
+                if (r < L) {
+                    const int64_t t = t0 + r;
+                    qr[jj] = *reinterpret_cast<const uint2 *>(qb + t * p.q_st + 4 * lane);
+                    kr[jj] = *reinterpret_cast<const uint2 *>(kb + t * p.k_st + 4 * lane);
+                }
             }
-            sq = warp_sum(sq);
-            sk = warp_sum(sk);
-            if (lane == 0) {
-                sRq[r] = (p.l2norm ? rsqrtf(sq + p.eps) : 1.f) * p.q_scale;
-                sRk[r] = p.l2norm ? rsqrtf(sk + p.eps) : 1.f;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int r = 4 * warp + jj;
+                *reinterpret_cast<uint2 *>(sm + R_F + r * 256 + 8 * lane) = qr[jj];
+                *reinterpret_cast<uint2 *>(sm + R_G + r * 256 + 8 * lane) = kr[jj];
+                const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].x));
+                const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].y));
+                const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].x));
+                const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].y));
+                float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+                float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+                sq = warp_sum(sq);
+                sk = warp_sum(sk);
+                if (lane == 0) {
+                    sRq[r] = (p.l2norm ? rsqrtf(sq + p.eps) : 1.f) * p.q_scale;
+                    sRk[r] = p.l2norm ? rsqrtf(sk + p.eps) : 1.f;
+                }
             }
         }
         if (tid < C) {
@@ -195,60 +207,70 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             sGs[r] = gs;
         }
         __syncthreads();
-        // per-channel log-decay prefix: thread (channel ci, rows 32 chalf .. +31)
-        float lam[32];
+        // per-channel log-decay prefix: thread (channel ci, rows 16 cq .. +15)
+        float lam[16];
         {
             float run = 0.f;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int r = 32 * chalf + jj;
+            for (int jj = 0; jj < 16; ++jj) {
+                const int r = 16 * cq + jj;
                 float gv = 0.f;
                 if (r < L) gv = p.gate == CGDR_GATE_CHANNEL ? gbase[(int64_t)(t0 + r) * p.g_st + ci] : sGs[r];
                 run += gv;
                 lam[jj] = run;
             }
-            if (chalf == 0) sH0[ci] = run;
+            sQt[cq * DK + ci] = run;
         }
         __syncthreads();
-        if (chalf == 1) {
-            const float h0 = sH0[ci];
+        {
+            float off = 0.f;
+            for (int qq = 0; qq < cq; ++qq) off += sQt[qq * DK + ci];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) lam[jj] += h0;
-            sGm[ci] = lam[0];      // gamma at row 32 (the anchor)
-            sGc[ci] = lam[31];     // gamma at the end of the chunk
+            for (int jj = 0; jj < 16; ++jj) lam[jj] += off;
+            if (cq == 2) sGm[ci] = lam[0];       // gamma at row 32 (the anchor)
+            if (cq == 3) sGc[ci] = lam[15];      // gamma at the end of the chunk
         }
         __syncthreads();
         const float gm = sGm[ci], gcv = sGc[ci];
         bool wide_local = false;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) wide_local |= fabsf(lam[jj] - gm) > kRange;
+        for (int jj = 0; jj < 16; ++jj) wide_local |= fabsf(lam[jj] - gm) > kRange;
         const bool wide = __syncthreads_or(wide_local) != 0;
         // decay-scaled operands
+        {
+            const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + R_F);
+            const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + R_G);
+            float kg4[4];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int r = 32 * chalf + jj;
-            float kt = 0.f, qt = 0.f;
-            if (r < L) {
-                const int64_t t = t0 + r;
-                kt = __bfloat162float(kb[t * p.k_st + ci]) * sRk[r];
-                qt = __bfloat162float(qb[t * p.q_st + ci]) * sRq[r];
-            }
-            const float eg = __expf(lam[jj]);
-            st_tile(sm, R_B, 64, r, ci, qt * eg);             // Qg [r][i]
-            st_tile(sm, R_C, 128, ci, r, kt * eg);            // Kg^T [i][s]
-            if (!wide) {
-                const float d = lam[jj] - gm;
-                const float e1 = __expf(d), e2 = __expf(-d);
-                st_tile(sm, R_A1, 128, r, ci, sBeta[r] * kt * e1);   // X1 rows 0..63
-                st_tile(sm, R_A1, 128, 64 + r, ci, qt * e1);         // X1 rows 64..127
-                st_tile(sm, R_A2, 64, r, ci, kt * e2);               // X2
-            } else {
-                f32p(sm, R_A1)[r * DK + ci] = qt;
-                f32p(sm, R_A1 + 32768)[r * DK + ci] = kt;
-                f32p(sm, R_A2)[r * DK + ci] = lam[jj];
+            for (int jj = 0; jj < 16; ++jj) {
+                const int r = 16 * cq + jj;
+                const float kt = __bfloat162float(ks[r * DK + ci]) * sRk[r];
+                const float qt = __bfloat162float(qs[r * DK + ci]) * sRq[r];
+                const float eg = __expf(lam[jj]);
+                st_tile(sm, R_B, 64, r, ci, qt * eg);             // Qg [r][i]
+                kg4[jj & 3] = kt * eg;
+                if ((jj & 3) == 3) st_tile4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);   // Kg^T [i][s]
+                if (!wide) {
+                    const float d = lam[jj] - gm;
+                    const float e1 = __expf(d), e2 = __expf(-d);
+                    st_tile(sm, R_A1, 128, r, ci, sBeta[r] * kt * e1);   // X1 rows 0..63
+                    st_tile(sm, R_A1, 128, 64 + r, ci, qt * e1);         // X1 rows 64..127
+                    st_tile(sm, R_A2, 64, r, ci, kt * e2);               // X2
+                } else {
+                    f32p(sm, R_A1)[r * DK + ci] = qt;
+                    f32p(sm, R_A1 + 32768)[r * DK + ci] = kt;
+                    f32p(sm, R_A2)[r * DK + ci] = lam[jj];
+                }
             }
         }
         if (tid < DK) sDec[tid] = expf(sGc[tid]);
+        // v column ci for this thread's 16 rows, loaded while the tensor core works
+        float vreg[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int srow = 16 * cq + jj;
+            vreg[jj] = srow < L ? __bfloat162float(vb[(int64_t)(t0 + srow) * p.v_st + ci]) : 0.f;
+        }
         fence_smem_to_async();
         fence_before_sync();
         __syncthreads();
@@ -260,58 +282,65 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
                 commit(mbar);
             }
             if (!(ok = mma_wait())) break;
-            const int m = 32 * wq + lane;
-            float v[32];
-            tmem_ld32(tmem + lane_off + T_D1 + 32 * wh, v);
+            float v[16];
+            tmem_ld16(tmem + lane_off + T_D1 + 16 * wc, v);
+            if (trow < 64) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const int s = 32 * wh + c;
-                if (m < 64) sA[m * LDA + s] = s < m ? v[c] : 0.f;
-                else st_tile(sm, R_F, 64, m - 64, s, s <= m - 64 ? v[c] : 0.f);
+                for (int c = 0; c < 16; ++c) {
+                    const int s = 16 * wc + c;
+                    sA[trow * LDA + s] = s < trow ? v[c] : 0.f;
+                }
+            } else {
+                const int r = trow - 64;
+#pragma unroll
+                for (int c = 0; c < 16; c += 4) {
+                    const int s = 16 * wc + c;
+                    st_tile4(sm, R_F, 64, r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
+                             s + 2 <= r ? v[c + 2] : 0.f, s + 3 <= r ? v[c + 3] : 0.f);
+                }
             }
         } else {
             // exact form for a chunk with a wide decay range: exponentials of differences
             const float *qt = f32p(sm, R_A1), *kt = f32p(sm, R_A1 + 32768), *gg = f32p(sm, R_A2);
-            float ra[16], rp[16];
+            float ra[8], rp[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
+            for (int e = 0; e < 8; ++e) {
                 const int idx = tid + NT * e, r = idx >> 6, s = idx & 63;
                 float sa = 0.f, sp = 0.f;
                 if (s <= r) {
 #pragma unroll 1
                     for (int i = 0; i < DK; ++i) {
                         const float d = expf(gg[r * DK + i] - gg[s * DK + i]);
-                        const float ks = kt[s * DK + i] * d;
-                        sa = fmaf(kt[r * DK + i], ks, sa);
-                        sp = fmaf(qt[r * DK + i], ks, sp);
+                        const float ksd = kt[s * DK + i] * d;
+                        sa = fmaf(kt[r * DK + i], ksd, sa);
+                        sp = fmaf(qt[r * DK + i], ksd, sp);
                     }
                 }
                 ra[e] = s < r ? sBeta[r] * sa : 0.f;
                 rp[e] = sp;
             }
             // Kend source in A2 (overwrites gamma once every thread is past the sums)
-            float ksrc[32];
+            float ksrc[16];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int r = 32 * chalf + jj;
+            for (int jj = 0; jj < 16; ++jj) {
+                const int r = 16 * cq + jj;
                 ksrc[jj] = kt[r * DK + ci] * expf(gcv - lam[jj]);
             }
             __syncthreads();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) st_tile(sm, R_A2, 64, 32 * chalf + jj, ci, ksrc[jj]);
+            for (int jj = 0; jj < 16; ++jj) st_tile(sm, R_A2, 64, 16 * cq + jj, ci, ksrc[jj]);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
+            for (int e = 0; e < 8; ++e) {
                 const int idx = tid + NT * e, r = idx >> 6, s = idx & 63;
                 sA[r * LDA + s] = ra[e];
                 st_tile(sm, R_F, 64, r, s, rp[e]);
             }
         }
         // V^T [j][s] (exact: bf16 values are TF32 values)
-        for (int jj = 0; jj < 32; ++jj) {
-            const int s = 32 * chalf + jj;
-            const float vv = s < L ? __bfloat162float(vb[(int64_t)(t0 + s) * p.v_st + ci]) : 0.f;
-            *reinterpret_cast<float *>(sm + A1_VT + sw_off(128, ci, s)) = vv;
-        }
+#pragma unroll
+        for (int jj = 0; jj < 16; jj += 4)
+            *reinterpret_cast<float4 *>(sm + A1_VT + sw_off(128, ci, 16 * cq + jj)) =
+                make_float4(vreg[jj], vreg[jj + 1], vreg[jj + 2], vreg[jj + 3]);
         __syncthreads();
         // ------------------------------------------------------------ Tb = (I + A)^-1 Diag(beta)
         if (tid < 64) {
@@ -321,7 +350,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             for (int r = 0; r < 16; ++r) {
                 float acc = r == jc ? 1.f : 0.f;
 #pragma unroll
-                for (int s = 0; s < r; ++s) acc = fmaf(-sA[(16 * Rb + r) * LDA + 16 * Rb + s], x[s], acc);
+                for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-sA[(16 * Rb + r) * LDA + 16 * Rb + s2], x[s2], acc);
                 x[r] = acc;
             }
 #pragma unroll
@@ -353,18 +382,16 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             __syncthreads();
         }
         {
-            float tv[16];
+            float tv[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int idx = tid * 16 + e, r = idx >> 6, s = idx & 63;
-                tv[e] = s <= r ? sXs[r * 64 + s] * sBeta[s] : 0.f;
+            for (int e = 0; e < 8; ++e) {
+                const int idx = tid * 8 + e, r = idx >> 6, s2 = idx & 63;
+                tv[e] = s2 <= r ? sXs[r * 64 + s2] * sBeta[s2] : 0.f;
             }
             __syncthreads();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int idx = tid * 16 + e, r = idx >> 6, s = idx & 63;
-                st_tile(sm, R_G, 64, r, s, tv[e]);
-            }
+            const int idx = tid * 8, r = idx >> 6, s2 = idx & 63;
+            st_tile4(sm, R_G, 64, r, s2, tv[0], tv[1], tv[2], tv[3]);
+            st_tile4(sm, R_G, 64, r, s2 + 4, tv[4], tv[5], tv[6], tv[7]);
         }
         fence_smem_to_async();
         fence_before_sync();
@@ -379,22 +406,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         if (!(ok = mma_wait())) break;
         // -W [r][i] from D2; S^T copy [j][i] from D0, then D0 <- D0 Diag(e^gC)
         {
-            const int row = 32 * wq + lane;
+            float w16[16];
+            tmem_ld16(tmem + lane_off + T_D2 + 16 * wc, w16);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) st_tile(sm, R_C, 64, 16 * wc + c, trow, -w16[c]);
             float v[32];
-            tmem_ld32(tmem + lane_off + T_D2 + 32 * wh, v);
+            const int i0 = 32 * wc;
+            tmem_ld32(tmem + lane_off + T_D0 + i0, v);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) st_tile(sm, R_C, 64, 32 * wh + c, row, -v[c]);
+            for (int c = 0; c < 32; c += 4) st_tile4(sm, R_A1, 128, trow, i0 + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const int i0 = 64 * wh + 32 * part;
-                tmem_ld32(tmem + lane_off + T_D0 + i0, v);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    st_tile(sm, R_A1, 128, row, i0 + c, v[c]);
-                    v[c] *= sDec[i0 + c];
-                }
-                tmem_st32(tmem + lane_off + T_D0 + i0, v);
-            }
+            for (int c = 0; c < 32; ++c) v[c] *= sDec[i0 + c];
+            tmem_st32(tmem + lane_off + T_D0 + i0, v);
         }
         fence_smem_to_async();
         fence_before_sync();
@@ -408,16 +431,17 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         }
         if (!(ok = mma_wait())) break;
         {
-            const int row = 32 * wq + lane;
-            float v[32];
-            tmem_ld32(tmem + lane_off + T_D3 + 32 * wh, v);
+            float v[16];
+            tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, v);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) st_tile(sm, R_A1, 128, row, 32 * wh + c, v[c]);   // U^T [j][s]
+            for (int c = 0; c < 16; c += 4)                                                  // U^T [j][s]
+                st_tile4(sm, R_A1, 128, trow, 16 * wc + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
             const float sc = wide ? 1.f : __expf(gcv - gm);
-#pragma unroll 8
-            for (int jj = 0; jj < 32; ++jj) {
-                const int s = 32 * chalf + jj;
-                st_tile(sm, R_C, 128, ci, s, ld_tile(sm, R_A2, 64, s, ci) * sc);           // Kend^T [i][s]
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4) {                                             // Kend^T [i][s]
+                const int s0 = 16 * cq + jj;
+                st_tile4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc,
+                         ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc);
             }
         }
         fence_smem_to_async();
@@ -432,14 +456,13 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         }
         if (!(ok = mma_wait())) break;
         {
-            const int j = 32 * wq + lane;
-            float v[32];
-            tmem_ld32(tmem + lane_off + T_D4 + 32 * wh, v);
+            float v[16];
+            tmem_ld16(tmem + lane_off + T_D4 + 16 * wc, v);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const int r = 32 * wh + c;
+            for (int c = 0; c < 16; ++c) {
+                const int r = 16 * wc + c;
                 if (r < L) {
-                    const int64_t off = obase + (int64_t)(t0 + r) * p.o_st + j;
+                    const int64_t off = obase + (int64_t)(t0 + r) * p.o_st + trow;
                     if (p.o_f32) static_cast<float *>(p.o)[off] = v[c];
                     else static_cast<__nv_bfloat16 *>(p.o)[off] = __float2bfloat16_rn(v[c]);
                 }
@@ -450,14 +473,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
     }
 
     if (ok) {
-        const int j = 32 * wq + lane;
+        float v[32];
+        tmem_ld32(tmem + lane_off + T_D0 + 32 * wc, v);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float v[32];
-            tmem_ld32(tmem + lane_off + T_D0 + 64 * wh + 32 * part, v);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) state[(size_t)(64 * wh + 32 * part + c) * DV + j] = v[c];
-        }
+        for (int c = 0; c < 32; ++c) state[(size_t)(32 * wc + c) * DV + trow] = v[c];
     } else {
         // a wait gave up: record it, give the tensor core a bounded chance to finish, release TMEM
         if (tid == 0) {
