@@ -51,8 +51,12 @@ constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = 
 constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_END = M_TMEM + 8;
 constexpr int SMEM_BYTES = M_END + 1024;                 // + alignment slack
 constexpr int LDA = 65;                  // fp32 A rows (padded)
-constexpr int A1_A32 = R_A1, A1_Y = R_A1 + 64 * LDA * 4, A1_VT = R_A1 + 32768;
-static_assert(A1_Y + 3 * 256 * 4 <= A1_VT, "A1 overflow");
+constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_VT = R_A1 + 32768;
+static_assert(A1_Z + 6 * 256 * 4 <= A1_VT, "A1 overflow");
+// Staged raw inputs of a chunk (written by cp.async during the previous chunk's last MMAs):
+// q rows -> F, k rows -> G (bf16 [64][128]); g rows -> A2 (fp32 [64][128]);
+// v rows -> B (bf16 [64][128]); beta -> B + 16 KB (fp32 [64]).
+constexpr int ST_Q = R_F, ST_K = R_G, ST_G = R_A2, ST_V = R_B, ST_BETA = R_B + 16384;
 static_assert(SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 
 // tensor memory columns
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
     const uint32_t sbase = smem_u32(sm);
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
     float *sQt = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
-    float *sA = f32p(sm, A1_A32), *sY = f32p(sm, A1_Y), *sXs = f32p(sm, R_G);
+    float *sA = f32p(sm, A1_A32), *sZ = f32p(sm, A1_Z), *sXs = f32p(sm, R_G);
     const uint32_t mbar = sbase + M_MBAR;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + M_TMEM);
 
@@ -128,6 +132,44 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(32 * wc + c) * DV + trow];
         tmem_st32(tmem + lane_off + T_D0 + 32 * wc, v);
     }
+    // cp.async staging of a chunk's raw rows: part 0 = v, beta, k; part 1 = q, g.
+    auto stage = [&](int part, int tn) {
+        const int Ln = min(C, p.T - tn);
+        if (part == 0) {
+            for (int idx = tid; idx < C * 16; idx += NT) {
+                const int r = idx >> 4, c16 = idx & 15;
+                const bool ok_row = r < Ln;
+                const int64_t t = tn + (ok_row ? r : 0);
+                cp_async16(sbase + ST_V + r * 256 + c16 * 16, vb + t * p.v_st + 8 * c16, ok_row);
+                cp_async16(sbase + ST_K + r * 256 + c16 * 16, kb + t * p.k_st + 8 * c16, ok_row);
+            }
+            if (p.gate == CGDR_GATE_CHANNEL && tid < C) {
+                const bool ok_row = tid < Ln;
+                const int64_t t = tn + (ok_row ? tid : 0);
+                cp_async4(sbase + ST_BETA + 4 * tid, p.beta + b * p.beta_sb + t * p.beta_st + h * p.beta_sh, ok_row);
+            }
+        } else {
+            for (int idx = tid; idx < C * 16; idx += NT) {
+                const int r = idx >> 4, c16 = idx & 15;
+                const bool ok_row = r < Ln;
+                const int64_t t = tn + (ok_row ? r : 0);
+                cp_async16(sbase + ST_Q + r * 256 + c16 * 16, qb + t * p.q_st + 8 * c16, ok_row);
+            }
+            if (p.gate == CGDR_GATE_CHANNEL) {
+                for (int idx = tid; idx < C * 32; idx += NT) {
+                    const int r = idx >> 5, c16 = idx & 31;
+                    const bool ok_row = r < Ln;
+                    const int64_t t = tn + (ok_row ? r : 0);
+                    cp_async16(sbase + ST_G + r * 512 + c16 * 16, gbase + t * p.g_st + 4 * c16, ok_row);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    if (p.T > 0) {
+        stage(0, 0);
+        stage(1, 0);
+    }
     fence_before_sync();
     __syncthreads();
 
@@ -143,6 +185,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
 
     for (int t0 = 0; t0 < p.T && ok; t0 += C) {
         const int L = min(C, p.T - t0);
+        cp_async_wait_all();
+        __syncthreads();
         // ------------------------------------------------------------ P1
         // prefetch the next chunk's rows into L2
         if (t0 + C < p.T) {
@@ -158,25 +202,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
                 if (ptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
             }
         }
-        // row norms (a warp per 4 rows); raw q/k rows staged (bf16) in regions F and G
+        // row norms (a warp per 4 rows) from the staged raw q/k rows
         {
             uint2 qr[4], kr[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int r = 4 * warp + jj;
-                qr[jj] = make_uint2(0u, 0u);
-                kr[jj] = make_uint2(0u, 0u);
-                if (r < L) {
-                    const int64_t t = t0 + r;
-                    qr[jj] = *reinterpret_cast<const uint2 *>(qb + t * p.q_st + 4 * lane);
-                    kr[jj] = *reinterpret_cast<const uint2 *>(kb + t * p.k_st + 4 * lane);
-                }
+                qr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_Q + r * 256 + 8 * lane);
+                kr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_K + r * 256 + 8 * lane);
             }
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int r = 4 * warp + jj;
-                *reinterpret_cast<uint2 *>(sm + R_F + r * 256 + 8 * lane) = qr[jj];
-                *reinterpret_cast<uint2 *>(sm + R_G + r * 256 + 8 * lane) = kr[jj];
                 const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].x));
                 const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].y));
                 const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].x));
@@ -197,7 +234,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             if (r < L) {
                 const int64_t t = t0 + r;
                 if (p.gate == CGDR_GATE_CHANNEL) {
-                    be = p.beta[b * p.beta_sb + t * p.beta_st + h * p.beta_sh];
+                    be = f32p(sm, ST_BETA)[r];
                 } else {
                     be = sigmoid_f(__bfloat162float(p.gb[b * p.b_sb + t * p.b_st + h * p.b_sh]));
                     gs = gdn_gate(p.A_log[h], __bfloat162float(p.ga[b * p.a_sb + t * p.a_st + h * p.a_sh]), p.dt_bias[h]);
@@ -215,7 +252,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             for (int jj = 0; jj < 16; ++jj) {
                 const int r = 16 * cq + jj;
                 float gv = 0.f;
-                if (r < L) gv = p.gate == CGDR_GATE_CHANNEL ? gbase[(int64_t)(t0 + r) * p.g_st + ci] : sGs[r];
+                if (r < L) gv = p.gate == CGDR_GATE_CHANNEL ? f32p(sm, ST_G)[r * DK + ci] : sGs[r];
                 run += gv;
                 lam[jj] = run;
             }
@@ -232,6 +269,13 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         }
         __syncthreads();
         const float gm = sGm[ci], gcv = sGc[ci];
+        // v column ci for this thread's 16 rows (staged), read before B is reused for Qg
+        float vreg[16];
+        {
+            const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_V);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) vreg[jj] = __bfloat162float(vs[(16 * cq + jj) * DK + ci]);
+        }
         bool wide_local = false;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) wide_local |= fabsf(lam[jj] - gm) > kRange;
@@ -264,13 +308,6 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             }
         }
         if (tid < DK) sDec[tid] = expf(sGc[tid]);
-        // v column ci for this thread's 16 rows, loaded while the tensor core works
-        float vreg[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const int srow = 16 * cq + jj;
-            vreg[jj] = srow < L ? __bfloat162float(vb[(int64_t)(t0 + srow) * p.v_st + ci]) : 0.f;
-        }
         fence_smem_to_async();
         fence_before_sync();
         __syncthreads();
@@ -357,6 +394,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             for (int r = 0; r < 16; ++r) sXs[(16 * Rb + r) * 64 + 16 * Rb + jc] = x[r];
         }
         __syncthreads();
+        // Z_Rm = X_RR A_Rm for the six block pairs m < R (pair index R(R-1)/2 + m)
+        for (int idx = tid; idx < 6 * 256; idx += NT) {
+            const int pi = idx >> 8, rho = (idx >> 4) & 15, c = idx & 15;
+            const int Rb = pi == 0 ? 1 : (pi < 3 ? 2 : 3), mb = pi - Rb * (Rb - 1) / 2;
+            float acc = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                acc = fmaf(sXs[(16 * Rb + rho) * 64 + 16 * Rb + u], sA[(16 * Rb + u) * LDA + 16 * mb + c], acc);
+            sZ[idx] = acc;
+        }
+        __syncthreads();
+        // X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS, one block diagonal at a time
 #pragma unroll 1
         for (int d = 1; d < 4; ++d) {
             const int nblk = 4 - d;
@@ -364,19 +413,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
                 const int blk = idx >> 8, Rb = d + blk, Sb = Rb - d, rho = (idx >> 4) & 15, c = idx & 15;
                 float acc = 0.f;
                 for (int mm = Sb; mm < Rb; ++mm) {
+                    const float *z = sZ + (Rb * (Rb - 1) / 2 + mm) * 256 + rho * 16;
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        acc = fmaf(sA[(16 * Rb + rho) * LDA + 16 * mm + u], sXs[(16 * mm + u) * 64 + 16 * Sb + c], acc);
+                    for (int u = 0; u < 16; ++u) acc = fmaf(z[u], sXs[(16 * mm + u) * 64 + 16 * Sb + c], acc);
                 }
-                sY[blk * 256 + rho * 16 + c] = acc;
-            }
-            __syncthreads();
-            for (int idx = tid; idx < nblk * 256; idx += NT) {
-                const int blk = idx >> 8, Rb = d + blk, Sb = Rb - d, rho = (idx >> 4) & 15, c = idx & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    acc = fmaf(sXs[(16 * Rb + rho) * 64 + 16 * Rb + u], sY[blk * 256 + u * 16 + c], acc);
                 sXs[(16 * Rb + rho) * 64 + 16 * Sb + c] = -acc;
             }
             __syncthreads();
@@ -430,6 +470,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             commit(mbar);
         }
         if (!(ok = mma_wait())) break;
+        if (t0 + C < p.T) stage(0, t0 + C);          // B and G are free: next chunk's v, beta, k
         {
             float v[16];
             tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, v);
@@ -455,6 +496,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             commit(mbar);
         }
         if (!(ok = mma_wait())) break;
+        if (t0 + C < p.T) stage(1, t0 + C);          // F and A2 are free: next chunk's q, g
         {
             float v[16];
             tmem_ld16(tmem + lane_off + T_D4 + 16 * wc, v);
