@@ -190,10 +190,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         // ------------------------------------------------------------ P1
         // prefetch the next chunk's rows into L2
         if (t0 + C < p.T) {
-            for (int idx = tid; idx < C * 10; idx += NT) {
-                const int r = idx / 10, part = idx % 10;
+            for (int idx = tid; idx < C * 16; idx += NT) {
+                const int r = idx >> 4, part = idx & 15;
                 const int64_t t = t0 + C + r;
-                if (t >= p.T) continue;
+                if (t >= p.T || part >= 10) continue;
                 const void *ptr;
                 if (part < 2) ptr = qb + t * p.q_st + 64 * part;
                 else if (part < 4) ptr = kb + t * p.k_st + 64 * (part - 2);
@@ -211,21 +211,29 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
                 qr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_Q + r * 256 + 8 * lane);
                 kr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_K + r * 256 + 8 * lane);
             }
+            float ss[8];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                const int r = 4 * warp + jj;
                 const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].x));
                 const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].y));
                 const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].x));
                 const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].y));
-                float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
-                float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
-                sq = warp_sum(sq);
-                sk = warp_sum(sk);
-                if (lane == 0) {
-                    sRq[r] = (p.l2norm ? rsqrtf(sq + p.eps) : 1.f) * p.q_scale;
-                    sRk[r] = p.l2norm ? rsqrtf(sk + p.eps) : 1.f;
-                }
+                ss[2 * jj] = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+                ss[2 * jj + 1] = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss[e] += __shfl_xor_sync(0xffffffffu, ss[e], o);
+            }
+            if (lane < 4) {
+                const int r = 4 * warp + lane;
+                float sq = ss[0], sk = ss[1];
+#pragma unroll
+                for (int jj = 1; jj < 4; ++jj)
+                    if (lane == jj) { sq = ss[2 * jj]; sk = ss[2 * jj + 1]; }
+                sRq[r] = (p.l2norm ? rsqrtf(sq + p.eps) : 1.f) * p.q_scale;
+                sRk[r] = p.l2norm ? rsqrtf(sk + p.eps) : 1.f;
             }
         }
         if (tid < C) {
@@ -282,6 +290,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         const bool wide = __syncthreads_or(wide_local) != 0;
         // decay-scaled operands
         {
+            // e^gm when it is a normal fp32 number (gm > -80): then e^g = e^gm e^(g - gm) without a third exp
+            const float emv = gm > -80.f ? __expf(gm) : 0.f;
             const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + R_F);
             const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + R_G);
             float kg4[4];
@@ -290,13 +300,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
                 const int r = 16 * cq + jj;
                 const float kt = __bfloat162float(ks[r * DK + ci]) * sRk[r];
                 const float qt = __bfloat162float(qs[r * DK + ci]) * sRq[r];
-                const float eg = __expf(lam[jj]);
+                float eg, e1 = 0.f;
+                if (!wide) e1 = __expf(lam[jj] - gm);
+                eg = (!wide && emv > 0.f) ? emv * e1 : __expf(lam[jj]);
                 st_tile(sm, R_B, 64, r, ci, qt * eg);             // Qg [r][i]
                 kg4[jj & 3] = kt * eg;
                 if ((jj & 3) == 3) st_tile4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);   // Kg^T [i][s]
                 if (!wide) {
-                    const float d = lam[jj] - gm;
-                    const float e1 = __expf(d), e2 = __expf(-d);
+                    const float e2 = __expf(gm - lam[jj]);
                     st_tile(sm, R_A1, 128, r, ci, sBeta[r] * kt * e1);   // X1 rows 0..63
                     st_tile(sm, R_A1, 128, 64 + r, ci, qt * e1);         // X1 rows 64..127
                     st_tile(sm, R_A2, 64, r, ci, kt * e2);               // X2
@@ -398,11 +409,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         for (int idx = tid; idx < 6 * 256; idx += NT) {
             const int pi = idx >> 8, rho = (idx >> 4) & 15, c = idx & 15;
             const int Rb = pi == 0 ? 1 : (pi < 3 ? 2 : 3), mb = pi - Rb * (Rb - 1) / 2;
-            float acc = 0.f;
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < 16; ++u)
-                acc = fmaf(sXs[(16 * Rb + rho) * 64 + 16 * Rb + u], sA[(16 * Rb + u) * LDA + 16 * mb + c], acc);
-            sZ[idx] = acc;
+                a4[u & 3] = fmaf(sXs[(16 * Rb + rho) * 64 + 16 * Rb + u], sA[(16 * Rb + u) * LDA + 16 * mb + c], a4[u & 3]);
+            sZ[idx] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
         }
         __syncthreads();
         // X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS, one block diagonal at a time
@@ -411,27 +422,33 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             const int nblk = 4 - d;
             for (int idx = tid; idx < nblk * 256; idx += NT) {
                 const int blk = idx >> 8, Rb = d + blk, Sb = Rb - d, rho = (idx >> 4) & 15, c = idx & 15;
-                float acc = 0.f;
+                float a4[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int mm = Sb; mm < Rb; ++mm) {
                     const float *z = sZ + (Rb * (Rb - 1) / 2 + mm) * 256 + rho * 16;
+                    const float *xs = sXs + (16 * mm) * 64 + 16 * Sb + c;
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) acc = fmaf(z[u], sXs[(16 * mm + u) * 64 + 16 * Sb + c], acc);
+                    for (int u = 0; u < 16; ++u) a4[u & 3] = fmaf(z[u], xs[u * 64], a4[u & 3]);
                 }
-                sXs[(16 * Rb + rho) * 64 + 16 * Sb + c] = -acc;
+                sXs[(16 * Rb + rho) * 64 + 16 * Sb + c] = -((a4[0] + a4[1]) + (a4[2] + a4[3]));
             }
             __syncthreads();
         }
         {
-            float tv[8];
+            // thread t converts elements [4t, 4t+4) and [2048 + 4t, 2048 + 4t + 4): 16-byte reads, no conflicts
+            float4 tv[2];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int idx = tid * 8 + e, r = idx >> 6, s2 = idx & 63;
-                tv[e] = s2 <= r ? sXs[r * 64 + s2] * sBeta[s2] : 0.f;
+            for (int e = 0; e < 2; ++e) {
+                const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
+                const float4 x = *reinterpret_cast<const float4 *>(sXs + idx);
+                tv[e] = make_float4(s2 <= r ? x.x * sBeta[s2] : 0.f, s2 + 1 <= r ? x.y * sBeta[s2 + 1] : 0.f,
+                                    s2 + 2 <= r ? x.z * sBeta[s2 + 2] : 0.f, s2 + 3 <= r ? x.w * sBeta[s2 + 3] : 0.f);
             }
             __syncthreads();
-            const int idx = tid * 8, r = idx >> 6, s2 = idx & 63;
-            st_tile4(sm, R_G, 64, r, s2, tv[0], tv[1], tv[2], tv[3]);
-            st_tile4(sm, R_G, 64, r, s2 + 4, tv[4], tv[5], tv[6], tv[7]);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
+                st_tile4(sm, R_G, 64, r, s2, tv[e].x, tv[e].y, tv[e].z, tv[e].w);
+            }
         }
         fence_smem_to_async();
         fence_before_sync();
@@ -500,14 +517,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         {
             float v[16];
             tmem_ld16(tmem + lane_off + T_D4 + 16 * wc, v);
+            const int64_t off0 = obase + (int64_t)(t0 + 16 * wc) * p.o_st + trow;
+            const int nv = min(16, L - 16 * wc);
+            if (p.o_f32) {
+                float *op = static_cast<float *>(p.o) + off0;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int r = 16 * wc + c;
-                if (r < L) {
-                    const int64_t off = obase + (int64_t)(t0 + r) * p.o_st + trow;
-                    if (p.o_f32) static_cast<float *>(p.o)[off] = v[c];
-                    else static_cast<__nv_bfloat16 *>(p.o)[off] = __float2bfloat16_rn(v[c]);
-                }
+                for (int c = 0; c < 16; ++c)
+                    if (c < nv) op[c * p.o_st] = v[c];
+            } else {
+                __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    if (c < nv) op[c * p.o_st] = __float2bfloat16_rn(v[c]);
             }
         }
         fence_before_sync();
