@@ -1,4 +1,5 @@
-// Decode (T = 1): one CTA per (batch, v-head) state tile, held in registers.
+// Decode (T = 1): each (batch, v-head) state tile is read once, updated in
+// registers and written once.
 //
 // "Add fused GatedDeltaNet decode Triton kernel" (executorch PR #18865) fuses
 // the Q/K/V split, the q/k L2 norm, the head repeat, the gating and the state
@@ -72,139 +73,270 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v
     *reinterpret_cast<uint2 *>(p) = raw;
 }
 
+// Persistent form: one CTA per SM walks its (batch, head) units; state tiles
+// stream through a ring of NS shared-memory stages filled by TMA bulk copies
+// (cp.async.bulk, completion on an mbarrier), the small per-unit rows (q, k,
+// v, g) by cp.async, so the next tiles are already in flight while the
+// current one is updated and written back with 16-byte streaming stores.
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 2) decode_kernel(const DecodeParams p) {
+struct PipeShape {
+    static constexpr int NS = 3;
+    static constexpr int TILE = DK * DV * 4;
+    static constexpr int ROWQ = ((DK * (int)sizeof(T) + 15) / 16) * 16;
+    static constexpr int ROWV = ((DV * (int)sizeof(T) + 15) / 16) * 16;
+    static constexpr int ROWG = DK * 4;
+    static constexpr int SMALL = 2 * ROWQ + ROWV + ROWG;
+    static constexpr int STAGE = ((TILE + SMALL + 127) / 128) * 128;
+    static constexpr int BYTES = NS * STAGE + 64 + 128;   // stages, mbarriers, alignment slack
+};
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait_parity(uint32_t mbar, uint32_t parity, uint32_t max_iters) {
+    for (uint32_t it = 0; it < max_iters; ++it) {
+        uint32_t done;
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_groups() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(const DecodeParams p, int units) {
     using Sh = DecodeShape<DK, DV>;
-    constexpr int CL = Sh::CL, RW = Sh::RW, NW = Sh::NW, RPT = Sh::RPT;
+    using Ps = PipeShape<DK, DV, T>;
+    constexpr int CL = Sh::CL, RW = Sh::RW, NW = Sh::NW, RPT = Sh::RPT, NT = Sh::NT, NS = Ps::NS;
+    constexpr uint32_t kSpin = 1u << 20;
+    extern __shared__ __align__(128) char dsm_raw[];
+    char *dsm = dsm_raw + ((128 - (smem_u32(dsm_raw) & 127)) & 127);
+    const uint32_t sb = smem_u32(dsm);
+    const uint32_t mbar0 = sb + NS * Ps::STAGE;
     __shared__ float s_kn[DK], s_qn[DK], s_alpha[DK];
     __shared__ float4 s_red[NW][CL];
     __shared__ float s_beta;
 
-    const int bh = blockIdx.x;
-    const int b = bh / p.Hv, h = bh % p.Hv;
-    const int hk = h / (p.Hv / p.Hk);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = lane % CL, r = lane / CL;
-    float *S = p.state + (size_t)bh * DK * DV;
+    const int G = gridDim.x;
 
-    // 1. Issue every state load first so the whole tile is in flight while
-    //    the norms and the gate are computed.
-    float4 s[RPT];
-#pragma unroll
-    for (int ii = 0; ii < RPT; ++ii) {
-        const int row = (warp * RPT + ii) * RW + r;
-        s[ii] = ld_stream(S + (size_t)row * DV + 4 * c);
+    if (tid == 0) {
+        for (int st = 0; st < NS; ++st) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * st));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
 
-    // 2. q/k L2 norm (a warp each), per-channel decay alpha and beta.
-    const T *q = static_cast<const T *>(p.q) + b * p.q_sb + hk * p.q_sh;
-    const T *k = static_cast<const T *>(p.k) + b * p.k_sb + hk * p.k_sh;
-    for (int which = warp; which < 2; which += NW) {
-        const T *x = which == 0 ? q : k;
-        float vals[DK / 32];
-        float ss = 0.f;
-#pragma unroll
-        for (int j = 0; j < DK / 32; ++j) {
-            vals[j] = Cvt<T>::to_f(x[lane + 32 * j]);
-            ss += vals[j] * vals[j];
+    // Issue the copies of unit u into stage st (every thread commits one cp.async group).
+    auto issue = [&](int u, int st) {
+        if (u < units) {
+            const int b = u / p.Hv, h = u % p.Hv, hk = h / (p.Hv / p.Hk);
+            const uint32_t base = sb + st * Ps::STAGE;
+            if (tid == 0) bulk_g2s(base, p.state + (size_t)u * DK * DV, Ps::TILE, mbar0 + 8 * st);
+            const char *qsrc = reinterpret_cast<const char *>(static_cast<const T *>(p.q) + b * p.q_sb + hk * p.q_sh);
+            const char *ksrc = reinterpret_cast<const char *>(static_cast<const T *>(p.k) + b * p.k_sb + hk * p.k_sh);
+            const char *vsrc = reinterpret_cast<const char *>(static_cast<const T *>(p.v) + b * p.v_sb + h * p.v_sh);
+            const char *gsrc = reinterpret_cast<const char *>(p.g + b * p.g_sb + h * p.g_sh);
+            constexpr int nq = Ps::ROWQ / 16, nv = Ps::ROWV / 16, ng = Ps::ROWG / 16;
+            const int total = 2 * nq + nv + (p.gate == CGDR_GATE_CHANNEL ? ng : 0);
+            const uint32_t sm0 = base + Ps::TILE;
+            for (int x = tid; x < total; x += NT) {
+                if (x < nq) cp_async16(sm0 + 16 * x, qsrc + 16 * x, true);
+                else if (x < 2 * nq) cp_async16(sm0 + Ps::ROWQ + 16 * (x - nq), ksrc + 16 * (x - nq), true);
+                else if (x < 2 * nq + nv) cp_async16(sm0 + 2 * Ps::ROWQ + 16 * (x - 2 * nq), vsrc + 16 * (x - 2 * nq), true);
+                else cp_async16(sm0 + 2 * Ps::ROWQ + Ps::ROWV + 16 * (x - 2 * nq - nv), gsrc + 16 * (x - 2 * nq - nv), true);
+            }
         }
-        ss = warp_sum(ss);
-        float scale = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
-        if (which == 0) scale *= p.q_scale;
-        float *dst = which == 0 ? s_qn : s_kn;
-#pragma unroll
-        for (int j = 0; j < DK / 32; ++j) dst[lane + 32 * j] = vals[j] * scale;
-    }
-    if (p.gate == CGDR_GATE_CHANNEL) {
-        const float *g = p.g + b * p.g_sb + h * p.g_sh;
-        for (int i = threadIdx.x; i < DK; i += blockDim.x) s_alpha[i] = expf(g[i]);
-        if (threadIdx.x == 0) s_beta = p.beta[b * p.beta_sb + h * p.beta_sh];
-    } else {
-        const float av = Cvt<T>::to_f(static_cast<const T *>(p.ga)[b * p.a_sb + h * p.a_sh]);
-        const float alpha = expf(gdn_gate(p.A_log[h], av, p.dt_bias[h]));
-        for (int i = threadIdx.x; i < DK; i += blockDim.x) s_alpha[i] = alpha;
-        if (threadIdx.x == 0)
-            s_beta = sigmoid_f(Cvt<T>::to_f(static_cast<const T *>(p.gb)[b * p.b_sb + h * p.b_sh]));
-    }
-    __syncthreads();
+        cp_async_commit();
+    };
+    // Per-unit scalars (beta, or a and b of the scalar gate), kept two units ahead in registers of thread 0.
+    auto scalars = [&](int u) -> float2 {
+        float2 x = make_float2(0.f, 0.f);
+        if (tid == 0 && u < units) {
+            const int b = u / p.Hv, h = u % p.Hv;
+            if (p.gate == CGDR_GATE_CHANNEL) x.x = p.beta[b * p.beta_sb + h * p.beta_sh];
+            else {
+                x.x = Cvt<T>::to_f(static_cast<const T *>(p.ga)[b * p.a_sb + h * p.a_sh]);
+                x.y = Cvt<T>::to_f(static_cast<const T *>(p.gb)[b * p.b_sb + h * p.b_sh]);
+            }
+        }
+        return x;
+    };
 
-    // 3. Sweep 1: vh = S^T (alpha * kn) over this thread's rows.
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int ii = 0; ii < RPT; ++ii) {
-        const int row = (warp * RPT + ii) * RW + r;
-        const float ak = s_alpha[row] * s_kn[row];
-        acc.x = fmaf(ak, s[ii].x, acc.x);
-        acc.y = fmaf(ak, s[ii].y, acc.y);
-        acc.z = fmaf(ak, s[ii].z, acc.z);
-        acc.w = fmaf(ak, s[ii].w, acc.w);
-    }
-#pragma unroll
-    for (int off = CL; off < 32; off <<= 1) {
-        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
-    }
-    if (r == 0) s_red[warp][c] = acc;
-    __syncthreads();
-    float4 vh = s_red[0][c];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) {
-        const float4 t = s_red[w][c];
-        vh.x += t.x; vh.y += t.y; vh.z += t.z; vh.w += t.w;
-    }
-    const float4 vv = load4<T>(static_cast<const T *>(p.v) + b * p.v_sb + h * p.v_sh + 4 * c);
-    const float beta = s_beta;
-    const float4 u = make_float4(beta * (vv.x - vh.x), beta * (vv.y - vh.y), beta * (vv.z - vh.z),
-                                 beta * (vv.w - vh.w));
-    __syncthreads();  // s_red is reused below
+    const int u0 = blockIdx.x;
+    for (int st = 0; st < NS - 1; ++st) issue(u0 + st * G, st);
+    float2 sc0 = scalars(u0), sc1 = scalars(u0 + G);
+    bool failed = false;
 
-    // 4. Sweep 2: decay + rank-one write, accumulate o, store the tile once.
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0;; ++k) {
+        const int u = u0 + k * G;
+        if (u >= units) break;
+        const int st = k % NS;
+        issue(u0 + (k + NS - 1) * G, (k + NS - 1) % NS);
+        const float2 sc = sc0;
+        sc0 = sc1;
+        sc1 = scalars(u0 + (k + 2) * G);
+
+        const bool got = mbar_wait_parity(mbar0 + 8 * st, (uint32_t)((k / NS) & 1), kSpin);
+        cp_async_wait_groups<NS - 1>();
+        const int b = u / p.Hv, h = u % p.Hv;
+        if (__syncthreads_or(!got)) {
+            failed = true;
+            break;
+        }
+        const char *stage = dsm + st * Ps::STAGE;
+        const float *S = reinterpret_cast<const float *>(stage);
+        const T *sq = reinterpret_cast<const T *>(stage + Ps::TILE);
+        const T *sk = reinterpret_cast<const T *>(stage + Ps::TILE + Ps::ROWQ);
+        const T *sv = reinterpret_cast<const T *>(stage + Ps::TILE + 2 * Ps::ROWQ);
+        const float *sg = reinterpret_cast<const float *>(stage + Ps::TILE + 2 * Ps::ROWQ + Ps::ROWV);
+
+        float4 s[RPT];
 #pragma unroll
-    for (int ii = 0; ii < RPT; ++ii) {
-        const int row = (warp * RPT + ii) * RW + r;
-        const float al = s_alpha[row], kn = s_kn[row], qn = s_qn[row];
-        float4 x = s[ii];
-        x.x = fmaf(al, x.x, kn * u.x);
-        x.y = fmaf(al, x.y, kn * u.y);
-        x.z = fmaf(al, x.z, kn * u.z);
-        x.w = fmaf(al, x.w, kn * u.w);
-        o.x = fmaf(qn, x.x, o.x);
-        o.y = fmaf(qn, x.y, o.y);
-        o.z = fmaf(qn, x.z, o.z);
-        o.w = fmaf(qn, x.w, o.w);
-        st_stream(S + (size_t)row * DV + 4 * c, x);
-    }
+        for (int ii = 0; ii < RPT; ++ii) {
+            const int row = (warp * RPT + ii) * RW + r;
+            s[ii] = *reinterpret_cast<const float4 *>(S + row * DV + 4 * c);
+        }
+        // q/k L2 norm (a warp each), decay alpha, beta
+        for (int which = warp; which < 2; which += NW) {
+            const T *x = which == 0 ? sq : sk;
+            float vals[DK / 32];
+            float ss = 0.f;
 #pragma unroll
-    for (int off = CL; off < 32; off <<= 1) {
-        o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
-        o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
-        o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
-        o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
-    }
-    if (r == 0) s_red[warp][c] = o;
-    __syncthreads();
-    if (warp == 0 && r == 0) {
-        float4 t = s_red[0][c];
+            for (int j = 0; j < DK / 32; ++j) {
+                vals[j] = Cvt<T>::to_f(x[lane + 32 * j]);
+                ss += vals[j] * vals[j];
+            }
+            ss = warp_sum(ss);
+            float scale = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
+            if (which == 0) scale *= p.q_scale;
+            float *dst = which == 0 ? s_qn : s_kn;
+#pragma unroll
+            for (int j = 0; j < DK / 32; ++j) dst[lane + 32 * j] = vals[j] * scale;
+        }
+        if (p.gate == CGDR_GATE_CHANNEL) {
+            for (int i = tid; i < DK; i += NT) s_alpha[i] = expf(sg[i]);
+            if (tid == 0) s_beta = sc.x;
+        } else {
+            if (tid == 0) {
+                s_alpha[0] = expf(gdn_gate(p.A_log[h], sc.x, p.dt_bias[h]));
+                s_beta = sigmoid_f(sc.y);
+            }
+            __syncthreads();
+            const float al = s_alpha[0];
+            __syncthreads();
+            for (int i = tid; i < DK; i += NT) s_alpha[i] = al;
+        }
+        __syncthreads();
+
+        // sweep 1: vh = S^T (alpha * kn)
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int ii = 0; ii < RPT; ++ii) {
+            const int row = (warp * RPT + ii) * RW + r;
+            const float ak = s_alpha[row] * s_kn[row];
+            acc.x = fmaf(ak, s[ii].x, acc.x);
+            acc.y = fmaf(ak, s[ii].y, acc.y);
+            acc.z = fmaf(ak, s[ii].z, acc.z);
+            acc.w = fmaf(ak, s[ii].w, acc.w);
+        }
+#pragma unroll
+        for (int off = CL; off < 32; off <<= 1) {
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+        }
+        if (r == 0) s_red[warp][c] = acc;
+        __syncthreads();
+        float4 vh = s_red[0][c];
 #pragma unroll
         for (int w = 1; w < NW; ++w) {
-            const float4 y = s_red[w][c];
-            t.x += y.x; t.y += y.y; t.z += y.z; t.w += y.w;
+            const float4 t = s_red[w][c];
+            vh.x += t.x; vh.y += t.y; vh.z += t.z; vh.w += t.w;
         }
-        const int64_t off = b * p.o_sb + h * p.o_sh + 4 * c;
-        if (p.o_f32)
-            store4<float>(static_cast<float *>(p.o) + off, t);
-        else
-            store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(p.o) + off, t);
+        const float4 vv = load4<T>(sv + 4 * c);
+        const float beta = s_beta;
+        const float4 uu = make_float4(beta * (vv.x - vh.x), beta * (vv.y - vh.y), beta * (vv.z - vh.z),
+                                      beta * (vv.w - vh.w));
+        __syncthreads();  // s_red is reused below
+
+        // sweep 2: decay + rank-one write, o accumulated, the tile stored once
+        float *Sg = p.state + (size_t)u * DK * DV;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int ii = 0; ii < RPT; ++ii) {
+            const int row = (warp * RPT + ii) * RW + r;
+            const float al = s_alpha[row], kn = s_kn[row], qn = s_qn[row];
+            float4 x = s[ii];
+            x.x = fmaf(al, x.x, kn * uu.x);
+            x.y = fmaf(al, x.y, kn * uu.y);
+            x.z = fmaf(al, x.z, kn * uu.z);
+            x.w = fmaf(al, x.w, kn * uu.w);
+            o.x = fmaf(qn, x.x, o.x);
+            o.y = fmaf(qn, x.y, o.y);
+            o.z = fmaf(qn, x.z, o.z);
+            o.w = fmaf(qn, x.w, o.w);
+            st_stream(Sg + (size_t)row * DV + 4 * c, x);
+        }
+#pragma unroll
+        for (int off = CL; off < 32; off <<= 1) {
+            o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+            o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+            o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+            o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+        }
+        if (r == 0) s_red[warp][c] = o;
+        __syncthreads();
+        if (warp == 0 && r == 0) {
+            float4 t = s_red[0][c];
+#pragma unroll
+            for (int w = 1; w < NW; ++w) {
+                const float4 y = s_red[w][c];
+                t.x += y.x; t.y += y.y; t.z += y.z; t.w += y.w;
+            }
+            const int64_t off = b * p.o_sb + h * p.o_sh + 4 * c;
+            if (p.o_f32) store4<float>(static_cast<float *>(p.o) + off, t);
+            else store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(p.o) + off, t);
+        }
+        __syncthreads();  // the stage and s_red are free again
     }
+
+    if (failed) {
+        // A tile never arrived: mark this CTA's remaining outputs with NaN, then give the
+        // copies in flight a bounded chance to land before the CTA's shared memory is released.
+        for (int k = 0;; ++k) {
+            const int u = u0 + k * G;
+            if (u >= units) break;
+            const int b = u / p.Hv, h = u % p.Hv;
+            for (int j = tid; j < DV; j += NT) {
+                const int64_t off = b * p.o_sb + h * p.o_sh + j;
+                if (p.o_f32) static_cast<float *>(p.o)[off] = __int_as_float(0x7fc00000);
+                else static_cast<__nv_bfloat16 *>(p.o)[off] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
+            }
+        }
+        for (int st = 0; st < NS; ++st) mbar_wait_parity(mbar0 + 8 * st, 0u, kSpin);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <int DK, int DV, typename T>
 cgdr_status launch_t(const DecodeParams &p, int units, cudaStream_t s) {
     using Sh = DecodeShape<DK, DV>;
-    decode_kernel<DK, DV, T><<<units, Sh::NT, 0, s>>>(p);
+    using Ps = PipeShape<DK, DV, T>;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // units per CTA as even as the SM count allows
+    const int per = (units + sms - 1) / sms;
+    const int grid = (units + per - 1) / per;
+    if (cudaFuncSetAttribute(decode_kernel<DK, DV, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ps::BYTES) !=
+        cudaSuccess)
+        return CGDR_ERR_CUDA;
+    decode_kernel<DK, DV, T><<<grid, Sh::NT, Ps::BYTES, s>>>(p, units);
     return cudaGetLastError() == cudaSuccess ? CGDR_OK : CGDR_ERR_CUDA;
 }
 
