@@ -205,6 +205,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end: host (pinned) buffers, copies inside the timed region
     e2e = run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world)
+    secondary = run_secondary(cg, dev, stream, flush_l2) if (rank == 0 and not args.no_secondary) else None
 
     if rank != 0:
         return None
@@ -240,10 +241,72 @@ def run_ours(args, rank, world, local_rank):
                             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
                             "traffic": tr_dec, "algorithmic_bytes": DEC_STATE_BYTES},
         "e2e": e2e,
+        "secondary": secondary,
         "gpu_launches": 2 * K,
         "wall_s_timed_region": round(t_wall, 3),
     }
     out["clocks"] = clk.summary()
+    return out
+
+
+def run_secondary(cg, dev, stream, flush_l2):
+    """The other workloads, timed once each: the fused GatedDeltaNet decode at B=1
+    (256 steps, eager and as one CUDA graph) and the long prefill (B=4, T=16411)."""
+    import torch
+    from gated_delta_rule_channelwise_gb300.synth import WORKLOADS, gate_kwargs, make_inputs
+    out = {}
+    w = WORKLOADS["gdn_decode_b1"]
+    inp = make_inputs(w, device=dev)
+    st = inp["S0"].clone()
+    o = torch.empty(w.T, 1, w.Hv, w.dv, dtype=torch.float32, device=dev)
+
+    def steps():
+        for t in range(w.T):
+            cg.decode(inp["q"][:, t], inp["k"][:, t], inp["v"][:, t], st, o[t], a=inp["a"][:, t], b=inp["b"][:, t],
+                      A_log=inp["A_log"], dt_bias=inp["dt_bias"])
+
+    steps()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream); steps(); e1.record(stream); torch.cuda.synchronize()
+    eager_us = e0.elapsed_time(e1) * 1e3 / w.T
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            steps()
+        g.replay(); torch.cuda.synchronize()
+        e0.record(stream); g.replay(); e1.record(stream); torch.cuda.synchronize()
+        graph_us = e0.elapsed_time(e1) * 1e3 / w.T
+    except Exception as exc:  # pragma: no cover - reported, not hidden
+        graph_us = "capture failed: %s" % exc
+    state_bytes = 2 * w.B * w.Hv * w.dk * w.dv * 4
+    out["gdn_decode_b1"] = {"workload": "fused GatedDeltaNet decode B=1, 16 k-heads -> 32 v-heads, packed bf16 qkv",
+                            "us_per_step_eager": round(eager_us, 3),
+                            "us_per_step_cuda_graph": round(graph_us, 3) if isinstance(graph_us, float) else graph_us,
+                            "state_bytes_per_step": state_bytes, "steps": w.T}
+    del inp, st, o
+    w = WORKLOADS["prefill_long"]
+    inp = make_inputs(w, device=dev)
+    st = torch.empty_like(inp["S0"])
+    o = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
+    ms = []
+    for _ in range(3):
+        st.copy_(inp["S0"])
+        flush_l2()
+        e0.record(stream)
+        cg.prefill(inp["q"], inp["k"], inp["v"], st, o, chunk=64, **gate_kwargs(inp))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    t = min(ms[1:])
+    nbytes = w.B * w.T * w.Hv * (3 * 128 * 2 + 128 * 4 + 4 + 128 * 4) + 2 * w.B * w.Hv * 128 * 128 * 4
+    hbm, _, _ = _peaks()
+    out["prefill_long"] = {"workload": "prefill B=4 H=32 T=16411 chunk 64, g = -softplus(N(1,1))",
+                           "ms_per_launch": round(t, 4), "tokens_per_s": round(w.B * w.T / (t / 1e3), 1),
+                           "algorithmic_bytes": nbytes, "roofline_frac": round(nbytes / (t / 1e3) / 1e9 / hbm, 4)}
+    del inp, st, o
+    torch.cuda.empty_cache()
     return out
 
 
@@ -384,6 +447,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
+    ap.add_argument("--no-secondary", action="store_true", help="skip the B=1 decode and T=16411 prefill timings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
