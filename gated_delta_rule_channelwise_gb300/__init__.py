@@ -123,44 +123,47 @@ def _need_cuda(*ts):
             raise ValueError("every tensor must live on a CUDA device (the library has no CPU path)")
 
 
+def _ptr_strides(t, name):
+    """(data pointer, batch, token, head strides) of a 4-d view with a contiguous last dimension."""
+    st = t.stride()
+    if st[3] != 1:
+        raise ValueError("%s: innermost dimension must be contiguous" % name)
+    return (t.data_ptr(), st[0], st[1], st[2])
+
+
+_NONE4 = (None, 0, 0, 0)
+
+
 def make_args(q, k, v, state, o, *, T, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
               l2norm=True, q_scale=None, eps=None, chunk=0) -> CgdrArgs:
     """Fill a ``cgdr_args`` block from 4-d views ``[B, T, H, d]`` (token dim included).
 
     Gate tensors are ``g [B,T,Hv,dk]`` and ``beta [B,T,Hv]`` (channel gate) or
     ``a, b [B,T,Hv]`` with ``A_log, dt_bias [Hv]`` (GatedDeltaNet gate).
+    The block is built in one constructor call (field order of ``struct cgdr_args``).
     """
-    A = CgdrArgs()
     B, _, Hk, dk = q.shape
-    Hv, dv = v.shape[2], v.shape[3]
-    A.B, A.T, A.Hk, A.Hv, A.dk, A.dv = B, T, Hk, Hv, dk, dv
-    A.dtype = _dtype_code(q)
-    A.o_dtype = _dtype_code(o)
-    A.gate = GATE_CHANNEL if g is not None else GATE_GDN
-    A.l2norm_qk = 1 if l2norm else 0
-    A.chunk = int(chunk)
-    A.q_scale = float(q_scale) if q_scale is not None else 0.0
-    A.eps = float(eps) if eps is not None else -1.0
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
-        if t.stride(-1) != 1:
-            raise ValueError("%s: innermost dimension must be contiguous" % name)
-        setattr(A, name, t.data_ptr())
-        setattr(A, name + "_sb", t.stride(0))
-        setattr(A, name + "_st", t.stride(1))
-        setattr(A, name + "_sh", t.stride(2))
-    if g is not None:
-        if g.stride(-1) != 1:
-            raise ValueError("g: innermost dimension must be contiguous")
-        A.g, A.g_sb, A.g_st, A.g_sh = g.data_ptr(), g.stride(0), g.stride(1), g.stride(2)
-        A.beta, A.beta_sb, A.beta_st, A.beta_sh = beta.data_ptr(), beta.stride(0), beta.stride(1), beta.stride(2)
-    else:
-        A.a, A.a_sb, A.a_st, A.a_sh = a.data_ptr(), a.stride(0), a.stride(1), a.stride(2)
-        A.b, A.b_sb, A.b_st, A.b_sh = b.data_ptr(), b.stride(0), b.stride(1), b.stride(2)
-        A.A_log, A.dt_bias = A_log.data_ptr(), dt_bias.data_ptr()
+    _, _, Hv, dv = v.shape
     if not state.is_contiguous():
         raise ValueError("state must be a dense [B, Hv, dk, dv] fp32 tensor")
-    A.state = state.data_ptr()
-    return A
+    if g is not None:
+        gate = GATE_CHANNEL
+        gg = _ptr_strides(g, "g")
+        bs = beta.stride()
+        bb = (beta.data_ptr(), bs[0], bs[1], bs[2])
+        aa = ab = _NONE4
+        alog = dtb = None
+    else:
+        gate = GATE_GDN
+        gg = bb = _NONE4
+        sa, sb = a.stride(), b.stride()
+        aa = (a.data_ptr(), sa[0], sa[1], sa[2])
+        ab = (b.data_ptr(), sb[0], sb[1], sb[2])
+        alog, dtb = A_log.data_ptr(), dt_bias.data_ptr()
+    return CgdrArgs(B, T, Hk, Hv, dk, dv, _dtype_code(q), gate, 1 if l2norm else 0, int(chunk), _dtype_code(o),
+                    float(q_scale) if q_scale is not None else 0.0, float(eps) if eps is not None else -1.0,
+                    *_ptr_strides(q, "q"), *_ptr_strides(k, "k"), *_ptr_strides(v, "v"), *gg, *bb, *aa, *ab,
+                    alog, dtb, state.data_ptr(), *_ptr_strides(o, "o"))
 
 
 def _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias):
