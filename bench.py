@@ -440,6 +440,29 @@ def run_reference(args):
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_case(name):
+    """One small case of a kernel, run twice, for a profiler to capture (prints 'ok')."""
+    import torch
+    import gated_delta_rule_channelwise_gb300 as cg
+    from gated_delta_rule_channelwise_gb300 import build as cbuild
+    from gated_delta_rule_channelwise_gb300.synth import Workload, gate_kwargs, make_inputs
+    cbuild.build()
+    if name == "prefill_t1024":
+        w = Workload("p", B=1, Hk=32, Hv=32, dk=128, dv=128, T=1024, dtype="bf16", gate="channel", seed=1)
+        inp = make_inputs(w, device="cuda")
+        for _ in range(2):
+            st = torch.zeros_like(inp["S0"])
+            cg.prefill(inp["q"], inp["k"], inp["v"], st, chunk=64, **gate_kwargs(inp))
+    elif name == "decode_b16":
+        w = Workload("d", B=16, Hk=32, Hv=32, dk=128, dv=128, T=2, dtype="bf16", gate="channel", seed=1)
+        inp = make_inputs(w, device="cuda")
+        st = inp["S0"].clone()
+        for t in range(2):
+            cg.decode(inp["q"][:, t], inp["k"][:, t], inp["v"][:, t], st, g=inp["g"][:, t], beta=inp["beta"][:, t])
+    torch.cuda.synchronize()
+    print("ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -448,7 +471,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the B=1 decode and T=16411 prefill timings")
+    ap.add_argument("--case", choices=["prefill_t1024", "decode_b16"],
+                    help="run one small case twice (for a profiler) and exit")
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
