@@ -47,7 +47,10 @@ PRE_BYTES = (PRE["B"] * PRE["T"] * PRE["H"] * (3 * 128 * 2 + 128 * 4 + 4 + 128 *
 # prefill tensor flops per token-head: 10*C*d (intra-chunk) + 6*dk*dv (carry)
 PRE_FLOPS = PRE["B"] * PRE["T"] * PRE["H"] * (10 * PRE["chunk"] * 128 + 6 * 128 * 128)
 L2_FLUSH_BYTES = 256 << 20
-PREFILL_KERNEL = ("prefill_tc05_kernel", "prefill_tc05.cu")   # (kernel name, source file)
+# kernel name and the sources that define it, per prefill path (1 = per head, 2 = cluster)
+PREFILL_KERNELS = {1: ("prefill_tc05_kernel", ["prefill_tc05.cu", "prefill_tc05_chunk.cuh", "tc05.cuh"]),
+                   2: ("prefill_cluster_kernel", ["prefill_cluster.cu", "prefill_tc05_chunk.cuh", "tc05.cuh"])}
+DECODE_KERNEL = ("decode_kernel", ["decode.cu", "cgdr_internal.cuh"])
 
 
 def _peaks():
@@ -59,11 +62,20 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def _traffic(kernel: str, source: str):
-    """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
+def sources_sha256(sources) -> str:
+    """sha256 of the concatenated kernel sources (csrc/), in the order listed."""
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, "gated_delta_rule_channelwise_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic(kernel: str, sources):
+    """DRAM bytes per launch from the committed ncu summary, if it is for these sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
-        sha = hashlib.sha256(open(os.path.join(ROOT, "gated_delta_rule_channelwise_gb300", "csrc", source), "rb").read()).hexdigest()
+        sha = sources_sha256(sources)
         for line in open(path):
             kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
             if kv.get("kernel") == kernel and kv.get("source_sha256") == sha:
@@ -158,7 +170,7 @@ def run_ours(args, rank, world, local_rank):
     pstate = torch.zeros_like(pinp["S0"])
     pout = torch.empty(pinp["v"].shape, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty(1, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush_l2():
         flush.zero_()                         # write > L2 ...
@@ -173,6 +185,9 @@ def run_ours(args, rank, world, local_rank):
         pstate.zero_()                            # zero initial state (outside the timed bracket)
         cg.prefill(pinp["q"], pinp["k"], pinp["v"], pstate, pout, g=pinp["g"], beta=pinp["beta"], chunk=64)
 
+    pre_path = cg.prefill_path_for(pinp["q"], pinp["k"], pinp["v"], pstate, pout, g=pinp["g"], beta=pinp["beta"],
+                                   chunk=64)
+    pre_kernel = PREFILL_KERNELS[pre_path]
     for i in range(args.warmup):
         flush_l2(); decode(i); flush_l2(); prefill()
     torch.cuda.synchronize()
@@ -216,8 +231,8 @@ def run_ours(args, rank, world, local_rank):
     pre_launch_s = statistics.mean(pre_ms) / 1e3
     pre_ach = PRE_BYTES / pre_launch_s / 1e9
     dec_ach = DEC_STATE_BYTES / dec_launch_s / 1e9
-    tr_pre = _traffic(*PREFILL_KERNEL)
-    tr_dec = _traffic("decode_kernel", "decode.cu")
+    tr_pre = _traffic(*pre_kernel)
+    tr_dec = _traffic(*DECODE_KERNEL)
     out = {
         "metric": METRIC, "value": round(dec_gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_total / K, 5), "higher_is_better": True,
@@ -231,9 +246,9 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_hbm_peak": round(100.0 * dec_gbs / world / hbm, 2),
         "prefill": {"metric": "prefill tokens/s at T=4000, 32 heads", "value": round(pre_tps, 1),
-                    "unit": "tokens/s", "ms_per_launch": round(pre_launch_s * 1e3, 5)},
+                    "unit": "tokens/s", "ms_per_launch": round(pre_launch_s * 1e3, 5), "kernel": pre_kernel[0]},
         "decode_ms_per_launch": round(dec_launch_s * 1e3, 5),
-        "roofline": {"kernel": PREFILL_KERNEL[0], "bound": "hbm", "achieved": round(pre_ach, 2), "peak": hbm,
+        "roofline": {"kernel": pre_kernel[0], "bound": "hbm", "achieved": round(pre_ach, 2), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(pre_ach / hbm, 4),
                      "traffic": tr_pre, "algorithmic_bytes": PRE_BYTES,
                      "tensor_flops": PRE_FLOPS, "tensor_frac": round(PRE_FLOPS / pre_launch_s / 1e12 / tflops, 4)},
@@ -305,6 +320,31 @@ def run_secondary(cg, dev, stream, flush_l2):
     out["prefill_long"] = {"workload": "prefill B=4 H=32 T=16411 chunk 64, g = -softplus(N(1,1))",
                            "ms_per_launch": round(t, 4), "tokens_per_s": round(w.B * w.T / (t / 1e3), 1),
                            "algorithmic_bytes": nbytes, "roofline_frac": round(nbytes / (t / 1e3) / 1e9 / hbm, 4)}
+    def time_prefill(inp, st, o, path):
+        cg.set_prefill_path(path)
+        try:
+            ms = []
+            for _ in range(3):
+                st.copy_(inp["S0"])
+                flush_l2()
+                e0.record(stream)
+                cg.prefill(inp["q"], inp["k"], inp["v"], st, o, chunk=64, **gate_kwargs(inp))
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms.append(e0.elapsed_time(e1))
+        finally:
+            cg.set_prefill_path(cg.PREFILL_AUTO)
+        return round(min(ms[1:]), 4)
+
+    out["prefill_long"]["ms_per_launch_cluster_kernel"] = time_prefill(inp, st, o, cg.PREFILL_CLUSTER)
+    out["prefill_long"]["ms_per_launch_per_head_kernel"] = time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)
+    del inp, st, o
+    w = WORKLOADS["prefill_t4000"]
+    inp = make_inputs(w, device=dev)
+    st = torch.empty_like(inp["S0"])
+    o = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
+    out["prefill_t4000_by_kernel"] = {"ms_per_launch_cluster_kernel": time_prefill(inp, st, o, cg.PREFILL_CLUSTER),
+                                      "ms_per_launch_per_head_kernel": time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)}
     del inp, st, o
     torch.cuda.empty_cache()
     return out
@@ -447,7 +487,9 @@ def run_case(name):
     from gated_delta_rule_channelwise_gb300 import build as cbuild
     from gated_delta_rule_channelwise_gb300.synth import Workload, gate_kwargs, make_inputs
     cbuild.build()
-    if name == "prefill_t1024":
+    if name.startswith("prefill_t1024"):
+        if name == "prefill_t1024_per_head":
+            cg.set_prefill_path(cg.PREFILL_PER_HEAD)
         w = Workload("p", B=1, Hk=32, Hv=32, dk=128, dv=128, T=1024, dtype="bf16", gate="channel", seed=1)
         inp = make_inputs(w, device="cuda")
         for _ in range(2):
@@ -471,7 +513,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the B=1 decode and T=16411 prefill timings")
-    ap.add_argument("--case", choices=["prefill_t1024", "decode_b16"],
+    ap.add_argument("--case", choices=["prefill_t1024", "prefill_t1024_per_head", "decode_b16"],
                     help="run one small case twice (for a profiler) and exit")
     args = ap.parse_args()
     if args.case:

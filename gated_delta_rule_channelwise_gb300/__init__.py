@@ -12,6 +12,7 @@ Public calls (same names as the C ABI without the ``cgdr_`` prefix):
 * :func:`decode` -- one T = 1 step for every (batch, v-head).
 * :func:`prefill` -- chunked prefill over T tokens.
 * :func:`prefill_workspace_size`, :func:`validate`, :func:`status_string`.
+* :func:`set_prefill_path`, :func:`prefill_path_for` -- which prefill kernel runs.
 """
 from __future__ import annotations
 
@@ -25,6 +26,7 @@ LIB_PATH = os.path.join(_PKG, "libcgdr.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 F32, BF16 = 0, 1
 GATE_CHANNEL, GATE_GDN = 0, 1
+PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT = range(4)
 
 
 class CgdrArgs(ctypes.Structure):
@@ -62,6 +64,8 @@ _SIGNATURES = [
     ("cgdr_prefill", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("cgdr_workspace_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("cgdr_prefill_noalloc", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p]),
+    ("cgdr_set_prefill_path", ctypes.c_int, [ctypes.c_int]),
+    ("cgdr_prefill_path_for", ctypes.c_int, [ctypes.POINTER(CgdrArgs)]),
 ]
 
 
@@ -242,6 +246,18 @@ def prefill_noalloc(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None
     return o
 
 
+def set_prefill_path(path: int) -> None:
+    """Process-wide prefill kernel choice: PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER or PREFILL_SIMT."""
+    _check(lib().cgdr_set_prefill_path(int(path)), "cgdr_set_prefill_path")
+
+
+def prefill_path_for(q, k, v, state, o, **kw) -> int:
+    """The kernel (PREFILL_PER_HEAD, PREFILL_CLUSTER or PREFILL_SIMT) a prefill with these arguments
+    runs under the current choice; PREFILL_AUTO if the arguments are invalid or there is no work."""
+    A = make_args(q, k, v, state, o, T=q.shape[1], **kw)
+    return int(lib().cgdr_prefill_path_for(ctypes.byref(A)))
+
+
 def workspace_status(workspace, stream=None) -> int:
     """Device-side status word a prefill left in its workspace (synchronises the stream)."""
     return int(lib().cgdr_workspace_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(stream)))
@@ -252,4 +268,5 @@ def validate(A: CgdrArgs, for_prefill: bool) -> int:
 
 
 __all__ = ["decode", "prefill", "prefill_noalloc", "prefill_workspace_size", "workspace_status", "validate", "status_string", "make_args",
+           "set_prefill_path", "prefill_path_for",
            "CgdrArgs", "CgdrError", "lib", "LIB_PATH"]

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcgdr.so")
-SOURCES = ["api.cu", "decode.cu", "prefill_simt.cu", "prefill_tc05.cu"]
+SOURCES = ["api.cu", "decode.cu", "prefill_simt.cu", "prefill_tc05.cu", "prefill_cluster.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

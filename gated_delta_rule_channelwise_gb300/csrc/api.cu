@@ -1,8 +1,12 @@
 // C ABI entry points of libcgdr: host-side argument checks and dispatch.
 // The operation and the argument conventions are documented in cgdr.h.
+#include <atomic>
+
 #include "cgdr_internal.cuh"
 
 namespace {
+
+std::atomic<int> g_prefill_path{CGDR_PREFILL_AUTO};
 
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
@@ -89,16 +93,33 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *a) {
     return 0;
 }
 
+cgdr_status cgdr_set_prefill_path(int path) {
+    if (path < CGDR_PREFILL_AUTO || path > CGDR_PREFILL_SIMT) return CGDR_ERR_INVALID_ARG;
+    g_prefill_path.store(path);
+    return CGDR_OK;
+}
+
+int cgdr_prefill_path_for(const cgdr_args *a) {
+    if (check(a, true) != CGDR_OK || a->B == 0 || a->T == 0) return CGDR_PREFILL_AUTO;
+    const int choice = g_prefill_path.load();
+    if (choice == CGDR_PREFILL_SIMT || !cgdr::prefill_tc05_supported(*a)) return CGDR_PREFILL_SIMT;
+    if (choice != CGDR_PREFILL_AUTO) return choice;
+    const int64_t units = (int64_t)a->B * a->Hv;
+    const int cap = cgdr::prefill_cluster_capacity();
+    return (cap > 0 && units <= cap) ? CGDR_PREFILL_CLUSTER : CGDR_PREFILL_PER_HEAD;
+}
+
 cgdr_status cgdr_prefill(const cgdr_args *a, void *ws, size_t ws_bytes, void *stream) {
     cgdr_status st = check(a, true);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cgdr::prefill_tc05_supported(*a)) {
-        const size_t need = cgdr::prefill_tc05_workspace(*a);
-        if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
-        return cgdr::launch_prefill_tc05(*a, ws, s);
-    }
-    return cgdr::launch_prefill_simt(*a, s);
+    if (g_prefill_path.load() == CGDR_PREFILL_SIMT || !cgdr::prefill_tc05_supported(*a))
+        return cgdr::launch_prefill_simt(*a, s);
+    const size_t need = cgdr::prefill_tc05_workspace(*a);
+    if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
+    const int path = cgdr_prefill_path_for(a);
+    if (path == CGDR_PREFILL_SIMT) return cgdr::launch_prefill_simt(*a, s);
+    return path == CGDR_PREFILL_CLUSTER ? cgdr::launch_prefill_cluster(*a, ws, s) : cgdr::launch_prefill_tc05(*a, ws, s);
 }
 
 cgdr_status cgdr_workspace_status(const void *ws, void *stream) {

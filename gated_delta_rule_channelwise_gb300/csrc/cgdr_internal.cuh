@@ -15,6 +15,8 @@ cgdr_status launch_prefill_simt(const cgdr_args &a, cudaStream_t s);
 bool prefill_tc05_supported(const cgdr_args &a);
 size_t prefill_tc05_workspace(const cgdr_args &a);
 cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s);
+int prefill_cluster_capacity();
+cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s);
 
 inline float eps_of(const cgdr_args &a) { return a.eps < 0.f ? 1e-6f : a.eps; }
 inline float qscale_of(const cgdr_args &a) {

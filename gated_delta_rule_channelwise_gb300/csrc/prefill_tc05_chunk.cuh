@@ -1,0 +1,493 @@
+// Per-chunk phases of the tcgen05 chunked prefill (TF32 operands, fp32
+// accumulators in tensor memory), dk = dv = 128, chunk 64, 512 threads.
+//
+// The chunkwise WY/UT form of "Add parallel chunked prefill for channelwise
+// gated delta rule" (executorch PR #21061, Summary).  These are the steps of
+// one chunk that do not touch the recurrent state: the per-channel log-decay
+// prefix, the decay-scaled operand tiles, the causal query/key terms A and P
+// and the beta-folded triangular transform Tb = (I + A)^-1 Diag(beta).  The
+// one-CTA-per-head kernel runs them in line with its state carry; the cluster
+// kernel runs them on the producer CTAs.  A ragged last chunk runs through the
+// same code (rows past the end are identity tokens: q = k = v = 0, g = 0,
+// beta = 0).
+//
+// Every contraction has one of the 128-wide dimensions as its rows (M = 128):
+//   D1 [A;P]^T-free form:  [beta kn e^(g-gm) ; qn e^(g-gm)] . (kn e^(gm-g))^T   (128 x 64, K = dk)
+//   D2 = W^T   = (kn e^g)^T . Tb^T          (dk x C,  K = C)
+//   D3 = U^T   = V^T . Tb^T - S^T . W^T     (dv x C,  K = C then dk)
+//   D4 = O^T   = S^T . (qn e^g)^T + U^T . P^T   (dv x C)
+//   D0 = S^T  <- S^T Diag(e^gC) + U^T . Kend,   Kend = kn e^(gC - g)   (dv x dk, K = C)
+// gm is the log-decay prefix at the chunk's middle row: with it both factors
+// of e^(g_r - g_s) stay finite while 32 tokens of log-decay stay within 80 in
+// magnitude on every channel.  A chunk outside that range forms A and P on
+// the CUDA cores from exponentials of differences instead (exact for any
+// decay).
+#pragma once
+
+#include "cgdr_internal.cuh"
+#include "tc05.cuh"
+
+namespace cgdr {
+namespace tc05c {
+
+using namespace tc05;
+
+constexpr int C = 64, DK = 128, DV = 128, NT = 512;
+constexpr float kRange = 80.f;           // max |gamma_r - gamma_mid| for the tensor-core causal terms
+constexpr uint32_t kSpin = 1u << 20;     // bounded mbarrier wait (iterations)
+
+// shared memory map of a CTA that prepares chunks (bytes from a 1024-aligned base)
+constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, V^T | S^T copy | U^T ; wide: q~, k~
+constexpr int R_A2 = 65536;              // 32 KB: X2 (kn e^(gm-g)), the source of Kend ; wide: gamma
+constexpr int R_B = 98304;               // 32 KB: Qg = qn e^g            [64 x 128]
+constexpr int R_C = 131072;              // 32 KB: Kg^T [128 x 64] | -W [64 x 128] | Kend^T [128 x 64]
+constexpr int R_F = 163840;              // 16 KB: P  [64 x 64]
+constexpr int R_G = 180224;              // 16 KB: Xs fp32 [64][64] | Tb [64 x 64]
+constexpr int R_MISC = 196608;
+// misc (fp32 unless noted)
+constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BETA + 256;
+constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = M_GC + 512;
+constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_FREE_A = M_TMEM + 8, M_FREE_B = M_FREE_A + 8;
+constexpr int M_END = M_FREE_B + 8;
+constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
+constexpr int LDA = 65;                  // fp32 A rows (padded)
+constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_VT = R_A1 + 32768;
+static_assert(A1_Z + 6 * 256 * 4 <= A1_VT, "A1 overflow");
+// Staged raw inputs of a chunk (cp.async, issued while an earlier chunk is finishing):
+// q rows -> F, k rows -> G (bf16 [64][128]); g rows -> A2 (fp32 [64][128]);
+// v rows -> B (bf16 [64][128]); beta -> B + 16 KB (fp32 [64]).
+constexpr int ST_Q = R_F, ST_K = R_G, ST_G = R_A2, ST_V = R_B, ST_BETA = R_B + 16384;
+static_assert(PREP_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
+
+// tensor memory columns
+constexpr uint32_t T_D0 = 0, T_D1 = 128, T_D2 = 192, T_D3 = 256, T_D4 = 320, T_D4B = 384, T_COLS = 512;
+
+struct Tc05Params {
+    int T, Hk, Hv, l2norm, gate, o_f32;
+    float q_scale, eps;
+    const __nv_bfloat16 *q, *k, *v;
+    int64_t q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh;
+    const float *g, *beta;
+    int64_t g_sb, g_st, g_sh, beta_sb, beta_st, beta_sh;
+    const __nv_bfloat16 *ga, *gb;
+    int64_t a_sb, a_st, a_sh, b_sb, b_st, b_sh;
+    const float *A_log, *dt_bias;
+    float *state;
+    void *o;
+    int64_t o_sb, o_st, o_sh;
+    int *err;                            // device word set to CGDR_ERR_TIMEOUT if a wait gives up
+};
+
+Tc05Params make_params(const cgdr_args &a, void *ws);
+
+__device__ __forceinline__ float *f32p(char *base, int off) { return reinterpret_cast<float *>(base + off); }
+__device__ __forceinline__ void st_tile(char *base, int region, int R, int r, int k, float x) {
+    *reinterpret_cast<float *>(base + region + sw_off(R, r, k)) = tf32r(x);
+}
+// Four consecutive K elements (k0 % 4 == 0) of row r: one 16-byte chunk of the swizzled tile.
+__device__ __forceinline__ void st_tile4(char *base, int region, int R, int r, int k0, float a, float b, float c,
+                                         float d) {
+    *reinterpret_cast<float4 *>(base + region + sw_off(R, r, k0)) = make_float4(tf32r(a), tf32r(b), tf32r(c), tf32r(d));
+}
+__device__ __forceinline__ float ld_tile(const char *base, int region, int R, int r, int k) {
+    return *reinterpret_cast<const float *>(base + region + sw_off(R, r, k));
+}
+
+// This CTA's (batch, v-head) and the bases of its input rows.
+struct Head {
+    int b, h;
+    const __nv_bfloat16 *qb, *kb, *vb;
+    const float *gbase;
+};
+
+__device__ __forceinline__ Head head_of(const Tc05Params &p, int b, int h) {
+    const int hk = h / (p.Hv / p.Hk);
+    Head hd;
+    hd.b = b;
+    hd.h = h;
+    hd.qb = p.q + b * p.q_sb + hk * p.q_sh;
+    hd.kb = p.k + b * p.k_sb + hk * p.k_sh;
+    hd.vb = p.v + b * p.v_sb + h * p.v_sh;
+    hd.gbase = p.g + b * p.g_sb + h * p.g_sh;
+    return hd;
+}
+
+// cp.async staging of the raw rows of the chunk starting at token tn; rows past
+// the end are zero-filled.  One commit group per call.
+enum : int { STG_Q = 1, STG_K = 2, STG_V = 4, STG_G = 8 };
+template <int PARTS>
+__device__ __forceinline__ void stage_rows(const Tc05Params &p, const Head &hd, uint32_t sbase, int tn) {
+    const int tid = threadIdx.x;
+    const int Ln = min(C, p.T - tn);
+    if (PARTS & (STG_V | STG_K | STG_Q)) {
+        for (int idx = tid; idx < C * 16; idx += NT) {
+            const int r = idx >> 4, c16 = idx & 15;
+            const bool ok_row = r < Ln;
+            const int64_t t = tn + (ok_row ? r : 0);
+            if (PARTS & STG_V) cp_async16(sbase + ST_V + r * 256 + c16 * 16, hd.vb + t * p.v_st + 8 * c16, ok_row);
+            if (PARTS & STG_K) cp_async16(sbase + ST_K + r * 256 + c16 * 16, hd.kb + t * p.k_st + 8 * c16, ok_row);
+            if (PARTS & STG_Q) cp_async16(sbase + ST_Q + r * 256 + c16 * 16, hd.qb + t * p.q_st + 8 * c16, ok_row);
+        }
+    }
+    if ((PARTS & STG_V) && p.gate == CGDR_GATE_CHANNEL && tid < C) {
+        const bool ok_row = tid < Ln;
+        const int64_t t = tn + (ok_row ? tid : 0);
+        cp_async4(sbase + ST_BETA + 4 * tid, p.beta + hd.b * p.beta_sb + t * p.beta_st + hd.h * p.beta_sh, ok_row);
+    }
+    if ((PARTS & STG_G) && p.gate == CGDR_GATE_CHANNEL) {
+        for (int idx = tid; idx < C * 32; idx += NT) {
+            const int r = idx >> 5, c16 = idx & 31;
+            const bool ok_row = r < Ln;
+            const int64_t t = tn + (ok_row ? r : 0);
+            cp_async16(sbase + ST_G + r * 512 + c16 * 16, hd.gbase + t * p.g_st + 4 * c16, ok_row);
+        }
+    }
+    cp_async_commit();
+}
+
+// The CTA's tensor-core completion barrier and the parity it waits for next.
+struct MmaBar {
+    uint32_t mbar;
+    uint32_t phase;
+};
+
+// Every thread waits (bounded) for the committed MMAs; false if any thread gave up.
+__device__ __forceinline__ bool mma_wait(MmaBar &mb) {
+    const bool done = mbar_wait(mb.mbar, mb.phase, kSpin);
+    mb.phase ^= 1u;
+    const bool bad = __syncthreads_or(!done) != 0;
+    fence_after_sync();
+    return !bad;
+}
+
+// Per-thread values that live across the phases of one chunk: thread (channel
+// ci = tid % 128, row quarter cq = tid / 128).
+struct ChunkRegs {
+    float lam[16];                       // log-decay prefix of channel ci at rows 16 cq .. 16 cq + 15
+    float vreg[16];                      // v column ci at those rows
+    float gm, gcv;                       // prefix at the anchor row 32 and at the chunk's end
+    bool wide;                           // the chunk's decay range is beyond kRange
+};
+
+// Row norms, beta, the log-decay prefix and the decay-scaled operand tiles of
+// the chunk at t0 (L valid rows) from its staged raw rows; also prefetches the
+// rows at t_pf into L2.  Ends with the operand tiles fenced for the tensor core.
+__device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L, int t_pf,
+                                           ChunkRegs &cr) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ci = tid & 127, cq = tid >> 7;
+    float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
+    float *sQt = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
+    if (t_pf < p.T) {
+        for (int idx = tid; idx < C * 16; idx += NT) {
+            const int r = idx >> 4, part = idx & 15;
+            const int64_t t = t_pf + r;
+            if (t >= p.T || part >= 10) continue;
+            const void *ptr;
+            if (part < 2) ptr = hd.qb + t * p.q_st + 64 * part;
+            else if (part < 4) ptr = hd.kb + t * p.k_st + 64 * (part - 2);
+            else if (part < 6) ptr = hd.vb + t * p.v_st + 64 * (part - 4);
+            else ptr = p.gate == CGDR_GATE_CHANNEL ? (const void *)(hd.gbase + t * p.g_st + 32 * (part - 6)) : nullptr;
+            if (ptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+        }
+    }
+    // row norms (a warp per 4 rows) from the staged raw q/k rows
+    {
+        uint2 qr[4], kr[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int r = 4 * warp + jj;
+            qr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_Q + r * 256 + 8 * lane);
+            kr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_K + r * 256 + 8 * lane);
+        }
+        float ss[8];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].x));
+            const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].y));
+            const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].x));
+            const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].y));
+            ss[2 * jj] = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+            ss[2 * jj + 1] = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss[e] += __shfl_xor_sync(0xffffffffu, ss[e], o);
+        }
+        if (lane < 4) {
+            const int r = 4 * warp + lane;
+            float sq = ss[0], sk = ss[1];
+#pragma unroll
+            for (int jj = 1; jj < 4; ++jj)
+                if (lane == jj) { sq = ss[2 * jj]; sk = ss[2 * jj + 1]; }
+            sRq[r] = (p.l2norm ? rsqrtf(sq + p.eps) : 1.f) * p.q_scale;
+            sRk[r] = p.l2norm ? rsqrtf(sk + p.eps) : 1.f;
+        }
+    }
+    if (tid < C) {
+        const int r = tid;
+        float be = 0.f, gs = 0.f;
+        if (r < L) {
+            const int64_t t = t0 + r;
+            if (p.gate == CGDR_GATE_CHANNEL) {
+                be = f32p(sm, ST_BETA)[r];
+            } else {
+                be = sigmoid_f(__bfloat162float(p.gb[hd.b * p.b_sb + t * p.b_st + hd.h * p.b_sh]));
+                gs = gdn_gate(p.A_log[hd.h], __bfloat162float(p.ga[hd.b * p.a_sb + t * p.a_st + hd.h * p.a_sh]),
+                              p.dt_bias[hd.h]);
+            }
+        }
+        sBeta[r] = be;
+        sGs[r] = gs;
+    }
+    __syncthreads();
+    // per-channel log-decay prefix: thread (channel ci, rows 16 cq .. +15)
+    {
+        float run = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int r = 16 * cq + jj;
+            float gv = 0.f;
+            if (r < L) gv = p.gate == CGDR_GATE_CHANNEL ? f32p(sm, ST_G)[r * DK + ci] : sGs[r];
+            run += gv;
+            cr.lam[jj] = run;
+        }
+        sQt[cq * DK + ci] = run;
+    }
+    __syncthreads();
+    {
+        float off = 0.f;
+        for (int qq = 0; qq < cq; ++qq) off += sQt[qq * DK + ci];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) cr.lam[jj] += off;
+        if (cq == 2) sGm[ci] = cr.lam[0];    // gamma at row 32 (the anchor)
+        if (cq == 3) sGc[ci] = cr.lam[15];   // gamma at the end of the chunk
+    }
+    __syncthreads();
+    cr.gm = sGm[ci];
+    cr.gcv = sGc[ci];
+    const float gm = cr.gm;
+    // v column ci for this thread's 16 rows (staged), read before B is reused for Qg
+    {
+        const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_V);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) cr.vreg[jj] = __bfloat162float(vs[(16 * cq + jj) * DK + ci]);
+    }
+    bool wide_local = false;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) wide_local |= fabsf(cr.lam[jj] - gm) > kRange;
+    const bool wide = __syncthreads_or(wide_local) != 0;
+    cr.wide = wide;
+    // decay-scaled operands
+    {
+        // e^gm when it is a normal fp32 number (gm > -80): then e^g = e^gm e^(g - gm) without a third exp
+        const float emv = gm > -80.f ? __expf(gm) : 0.f;
+        const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_Q);
+        const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_K);
+        float kg4[4];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int r = 16 * cq + jj;
+            const float kt = __bfloat162float(ks[r * DK + ci]) * sRk[r];
+            const float qt = __bfloat162float(qs[r * DK + ci]) * sRq[r];
+            float eg, e1 = 0.f;
+            if (!wide) e1 = __expf(cr.lam[jj] - gm);
+            eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
+            st_tile(sm, R_B, 64, r, ci, qt * eg);             // Qg [r][i]
+            kg4[jj & 3] = kt * eg;
+            if ((jj & 3) == 3) st_tile4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);   // Kg^T [i][s]
+            if (!wide) {
+                const float e2 = __expf(gm - cr.lam[jj]);
+                st_tile(sm, R_A1, 128, r, ci, sBeta[r] * kt * e1);   // X1 rows 0..63
+                st_tile(sm, R_A1, 128, 64 + r, ci, qt * e1);         // X1 rows 64..127
+                st_tile(sm, R_A2, 64, r, ci, kt * e2);               // X2
+            } else {
+                f32p(sm, R_A1)[r * DK + ci] = qt;
+                f32p(sm, R_A1 + 32768)[r * DK + ci] = kt;
+                f32p(sm, R_A2)[r * DK + ci] = cr.lam[jj];
+            }
+        }
+    }
+    if (tid < DK) sDec[tid] = expf(sGc[tid]);
+    fence_smem_to_async();
+    fence_before_sync();
+    __syncthreads();
+}
+
+// The causal terms: A (fp32, strictly lower, beta-folded) into A1_A32, P (tile,
+// lower with diagonal) into R_F, the Kend source into R_A2 for a wide chunk,
+// and V^T into A1_VT.  False if a tensor-core wait gave up.
+__device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, const ChunkRegs &cr) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3, wc = warp >> 2;
+    const int ci = tid & 127, cq = tid >> 7;
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    const int trow = 32 * wq + lane;
+    float *sA = f32p(sm, A1_A32), *sBeta = f32p(sm, M_BETA);
+    if (!cr.wide) {
+        if (tid == 0) {
+            fence_after_sync();
+            gemm<64, 128>(tmem + T_D1, sbase + R_A1, sbase + R_A2, false);
+            commit(mb.mbar);
+        }
+        if (!mma_wait(mb)) return false;
+        float v[16];
+        tmem_ld16(tmem + lane_off + T_D1 + 16 * wc, v);
+        if (trow < 64) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int s = 16 * wc + c;
+                sA[trow * LDA + s] = s < trow ? v[c] : 0.f;
+            }
+        } else {
+            const int r = trow - 64;
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) {
+                const int s = 16 * wc + c;
+                st_tile4(sm, R_F, 64, r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
+                         s + 2 <= r ? v[c + 2] : 0.f, s + 3 <= r ? v[c + 3] : 0.f);
+            }
+        }
+    } else {
+        // exact form for a chunk with a wide decay range: exponentials of differences
+        const float *qt = f32p(sm, R_A1), *kt = f32p(sm, R_A1 + 32768), *gg = f32p(sm, R_A2);
+        float ra[8], rp[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int idx = tid + NT * e, r = idx >> 6, s = idx & 63;
+            float sa = 0.f, sp = 0.f;
+            if (s <= r) {
+#pragma unroll 1
+                for (int i = 0; i < DK; ++i) {
+                    const float d = expf(gg[r * DK + i] - gg[s * DK + i]);
+                    const float ksd = kt[s * DK + i] * d;
+                    sa = fmaf(kt[r * DK + i], ksd, sa);
+                    sp = fmaf(qt[r * DK + i], ksd, sp);
+                }
+            }
+            ra[e] = s < r ? sBeta[r] * sa : 0.f;
+            rp[e] = sp;
+        }
+        // Kend source in A2 (overwrites gamma once every thread is past the sums)
+        float ksrc[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int r = 16 * cq + jj;
+            ksrc[jj] = kt[r * DK + ci] * expf(cr.gcv - cr.lam[jj]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) st_tile(sm, R_A2, 64, 16 * cq + jj, ci, ksrc[jj]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int idx = tid + NT * e, r = idx >> 6, s = idx & 63;
+            sA[r * LDA + s] = ra[e];
+            st_tile(sm, R_F, 64, r, s, rp[e]);
+        }
+    }
+    // V^T [j][s] (exact: bf16 values are TF32 values)
+#pragma unroll
+    for (int jj = 0; jj < 16; jj += 4)
+        *reinterpret_cast<float4 *>(sm + A1_VT + sw_off(128, ci, 16 * cq + jj)) =
+            make_float4(cr.vreg[jj], cr.vreg[jj + 1], cr.vreg[jj + 2], cr.vreg[jj + 3]);
+    __syncthreads();
+    return true;
+}
+
+// Tb = (I + A)^-1 Diag(beta) into R_G as a TF32 tile: forward substitution on
+// the four 16 x 16 diagonal blocks, then the off-diagonal blocks one block
+// diagonal at a time.  Ends with Tb fenced for the tensor core.
+__device__ __forceinline__ void solve_tb(char *sm) {
+    const int tid = threadIdx.x;
+    const float *sA = f32p(sm, A1_A32), *sBeta = f32p(sm, M_BETA);
+    float *sZ = f32p(sm, A1_Z), *sXs = f32p(sm, R_G);
+    if (tid < 64) {
+        const int Rb = tid >> 4, jc = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = r == jc ? 1.f : 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-sA[(16 * Rb + r) * LDA + 16 * Rb + s2], x[s2], acc);
+            x[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sXs[(16 * Rb + r) * 64 + 16 * Rb + jc] = x[r];
+    }
+    __syncthreads();
+    // Z_Rm = X_RR A_Rm for the six block pairs m < R (pair index R(R-1)/2 + m)
+    for (int idx = tid; idx < 6 * 256; idx += NT) {
+        const int pi = idx >> 8, rho = (idx >> 4) & 15, c = idx & 15;
+        const int Rb = pi == 0 ? 1 : (pi < 3 ? 2 : 3), mb = pi - Rb * (Rb - 1) / 2;
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            a4[u & 3] = fmaf(sXs[(16 * Rb + rho) * 64 + 16 * Rb + u], sA[(16 * Rb + u) * LDA + 16 * mb + c], a4[u & 3]);
+        sZ[idx] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+    }
+    __syncthreads();
+    // X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS, one block diagonal at a time
+#pragma unroll 1
+    for (int d = 1; d < 4; ++d) {
+        const int nblk = 4 - d;
+        for (int idx = tid; idx < nblk * 256; idx += NT) {
+            const int blk = idx >> 8, Rb = d + blk, Sb = Rb - d, rho = (idx >> 4) & 15, c = idx & 15;
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int mm = Sb; mm < Rb; ++mm) {
+                const float *z = sZ + (Rb * (Rb - 1) / 2 + mm) * 256 + rho * 16;
+                const float *xs = sXs + (16 * mm) * 64 + 16 * Sb + c;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) a4[u & 3] = fmaf(z[u], xs[u * 64], a4[u & 3]);
+            }
+            sXs[(16 * Rb + rho) * 64 + 16 * Sb + c] = -((a4[0] + a4[1]) + (a4[2] + a4[3]));
+        }
+        __syncthreads();
+    }
+    {
+        // thread t converts elements [4t, 4t+4) and [2048 + 4t, 2048 + 4t + 4): 16-byte reads, no conflicts
+        float4 tv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
+            const float4 x = *reinterpret_cast<const float4 *>(sXs + idx);
+            tv[e] = make_float4(s2 <= r ? x.x * sBeta[s2] : 0.f, s2 + 1 <= r ? x.y * sBeta[s2 + 1] : 0.f,
+                                s2 + 2 <= r ? x.z * sBeta[s2 + 2] : 0.f, s2 + 3 <= r ? x.w * sBeta[s2 + 3] : 0.f);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
+            st_tile4(sm, R_G, 64, r, s2, tv[e].x, tv[e].y, tv[e].z, tv[e].w);
+        }
+    }
+    fence_smem_to_async();
+    fence_before_sync();
+    __syncthreads();
+}
+
+// Columns [16 wc, 16 wc + 16) of O^T (chunk at t0, L valid tokens) from TMEM to o.
+__device__ __forceinline__ void store_o(const Tc05Params &p, int64_t obase, uint32_t taddr, int t0, int L) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3, wc = warp >> 2;
+    const int trow = 32 * wq + lane;
+    float v[16];
+    tmem_ld16(taddr + ((uint32_t)(32 * wq) << 16) + 16 * wc, v);
+    const int64_t off0 = obase + (int64_t)(t0 + 16 * wc) * p.o_st + trow;
+    const int nv = min(16, L - 16 * wc);
+    if (p.o_f32) {
+        float *op = static_cast<float *>(p.o) + off0;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            if (c < nv) op[c * p.o_st] = v[c];
+    } else {
+        __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            if (c < nv) op[c * p.o_st] = __float2bfloat16_rn(v[c]);
+    }
+}
+
+}  // namespace tc05c
+}  // namespace cgdr

@@ -137,15 +137,50 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
  * state carry, with a ragged last chunk handled by the same code.
  * T == 0 is a no-op.  The result equals T applications of the token
  * recurrence up to rounding, for every chunk length.
- * Paths: bf16 inputs with dk = dv = 128 and chunk 64 run the tensor-core
- * kernel (tcgen05, TF32 operands, fp32 accumulation and state; one CTA per
- * (batch, v-head)); every other case runs an fp32 CUDA-core kernel.
+ * Paths: bf16 inputs with dk = dv = 128 and chunk 64 run one of the two
+ * tensor-core kernels (tcgen05, TF32 operands, fp32 accumulation and state),
+ * chosen as cgdr_set_prefill_path describes; every other case runs an fp32
+ * CUDA-core kernel.
  * Workspace: the tensor-core path needs cgdr_prefill_workspace_size() bytes
  * (16-byte aligned); its first int32 is set to CGDR_ERR_TIMEOUT if a bounded
  * device wait gave up (see cgdr_workspace_status).  `workspace` may be NULL
  * when the size is 0.  Returns CGDR_ERR_WORKSPACE if it is too small.
  */
 cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The kernels behind cgdr_prefill.  The two tensor-core kernels cover bf16
+ * inputs with dk = dv = 128 and chunk 64 and agree up to rounding order; the
+ * CUDA-core kernel covers every supported shape.  The split of the chunk's
+ * work into a state-free part and the state carry follows the chunkwise form
+ * of "Add parallel chunked prefill for channelwise gated delta rule"
+ * (Summary); running them on different SMs has no counterpart there.
+ */
+typedef enum cgdr_prefill_path {
+    CGDR_PREFILL_AUTO = 0,      /* per call: CLUSTER when every (batch, v-head) cluster is
+                                   resident on the GPU at once, else PER_HEAD */
+    CGDR_PREFILL_PER_HEAD = 1,  /* tensor cores, one CTA per (batch, v-head) */
+    CGDR_PREFILL_CLUSTER = 2,   /* tensor cores, a cluster of four CTAs per (batch, v-head):
+                                   one carries the state, three prepare chunks for it */
+    CGDR_PREFILL_SIMT = 3       /* fp32 CUDA cores */
+} cgdr_prefill_path;
+
+/*
+ * Process-wide kernel choice for later cgdr_prefill and cgdr_prefill_noalloc
+ * calls (default CGDR_PREFILL_AUTO).  A tensor-core choice for a shape those
+ * kernels do not cover runs the CUDA-core kernel.  Returns
+ * CGDR_ERR_INVALID_ARG (and keeps the current choice) for any other value.
+ */
+cgdr_status cgdr_set_prefill_path(int path);
+
+/*
+ * The kernel cgdr_prefill would run for `args` on the current device under
+ * the current choice: CGDR_PREFILL_PER_HEAD, CGDR_PREFILL_CLUSTER or
+ * CGDR_PREFILL_SIMT; CGDR_PREFILL_AUTO (0) if `args` is invalid or there is
+ * nothing to do (B == 0 or T == 0).  Queries the device once per device for
+ * the cluster capacity.
+ */
+int cgdr_prefill_path_for(const cgdr_args *args);
 
 /*
  * Waits for `stream`, then reports the device-side status a cgdr_prefill

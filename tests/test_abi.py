@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     assert declared_functions() == sorted([
         "cgdr_abi_version", "cgdr_status_string", "cgdr_validate", "cgdr_decode",
-        "cgdr_prefill_workspace_size", "cgdr_prefill", "cgdr_workspace_status", "cgdr_prefill_noalloc"])
+        "cgdr_prefill_workspace_size", "cgdr_prefill", "cgdr_workspace_status", "cgdr_prefill_noalloc",
+        "cgdr_set_prefill_path", "cgdr_prefill_path_for"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -149,3 +150,29 @@ def test_output_dtype_strides(lib):
 
 def test_token_strides_ignored_by_decode(lib):
     assert cg.validate(_args(q_st=3, v_st=5, o_st=1, g_st=7), False) == cg.OK
+
+
+def test_prefill_path_choice(lib):
+    """Kernel selection is host logic: a forced tensor-core kernel applies only to the shapes it
+    covers (bf16, dk = dv = 128, chunk 64); unknown choices are rejected and change nothing."""
+    A = _args(T=100)
+    try:
+        assert lib.cgdr_set_prefill_path(4) == cg.ERR_INVALID_ARG
+        assert lib.cgdr_set_prefill_path(-1) == cg.ERR_INVALID_ARG
+        for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
+            assert lib.cgdr_set_prefill_path(path) == cg.OK
+            assert lib.cgdr_prefill_path_for(ctypes.byref(A)) == path
+            assert lib.cgdr_set_prefill_path(9) == cg.ERR_INVALID_ARG
+            assert lib.cgdr_prefill_path_for(ctypes.byref(A)) == path
+            for other in (_args(T=100, chunk=32), _args(T=100, dv=64),
+                          _args(T=100, dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128)):
+                assert lib.cgdr_prefill_path_for(ctypes.byref(other)) == cg.PREFILL_SIMT
+        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=0))) == cg.PREFILL_AUTO
+        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, dk=96))) == cg.PREFILL_AUTO
+        assert lib.cgdr_prefill_path_for(None) == cg.PREFILL_AUTO
+        # the cluster kernel needs the workspace too
+        assert lib.cgdr_set_prefill_path(cg.PREFILL_CLUSTER) == cg.OK
+        assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
+    finally:
+        lib.cgdr_set_prefill_path(cg.PREFILL_AUTO)
+    assert lib.cgdr_prefill_path_for(ctypes.byref(A)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)

@@ -23,6 +23,22 @@ def _built():
     cg.lib()
 
 
+TC_PATHS = [pytest.param(cg.PREFILL_PER_HEAD, id="per_head"), pytest.param(cg.PREFILL_CLUSTER, id="cluster")]
+
+
+@pytest.fixture(params=TC_PATHS)
+def tc_path(request):
+    """Runs the test once per tensor-core prefill kernel (restores automatic choice after)."""
+    cg.set_prefill_path(request.param)
+    yield request.param
+    cg.set_prefill_path(cg.PREFILL_AUTO)
+
+
+def _expect_path(inp, path):
+    o = torch.empty(inp["v"].shape, device=inp["v"].device)
+    assert cg.prefill_path_for(inp["q"], inp["k"], inp["v"], inp["S0"], o, chunk=64, **gate_kwargs(inp)) == path
+
+
 def _prefill(inp, chunk, state=None, **kw):
     state = inp["S0"].clone() if state is None else state
     o = cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=chunk, **gate_kwargs(inp), **kw)
@@ -64,9 +80,12 @@ def test_fp32_chunk_sizes_and_tails(chunk, T, dk, dv):
 @pytest.mark.parametrize("T", [1, 2, 31, 63, 64, 65, 127, 200])
 @pytest.mark.parametrize("dv", [32, 64, 128])
 @pytest.mark.parametrize("gate", ["channel", "gdn"])
-def test_tensor_core_path_tails(T, dv, gate):
+def test_tensor_core_path_tails(T, dv, gate, tc_path):
+    if dv != 128 and tc_path == cg.PREFILL_CLUSTER:
+        pytest.skip("dv < 128 runs the CUDA-core kernel whatever the choice")
     w = Workload("tc", B=2, Hk=1, Hv=2, dk=128, dv=dv, T=T, dtype="bf16", gate=gate, seed=T * 3 + dv)
     inp = make_inputs(w, device="cuda")
+    _expect_path(inp, tc_path if dv == 128 else cg.PREFILL_SIMT)
     o, s = _prefill(inp, 64)
     _check(w, inp, o, s)
 
@@ -82,7 +101,7 @@ def test_bf16_cuda_core_chunks_agree(chunk):
     _check(w, inp, o2, s2)
 
 
-def test_strong_decay_anchoring():
+def test_strong_decay_anchoring(tc_path):
     """Log-decay near -3 per token (-190 per chunk): e^-gamma would overflow fp32 without anchoring."""
     w = Workload("strong", B=1, Hk=2, Hv=2, dk=128, dv=128, T=300, dtype="bf16", gate="channel",
                  g_mu=3.0, g_scale=1.0, seed=77)
@@ -91,22 +110,23 @@ def test_strong_decay_anchoring():
     _check(w, inp, o, s)
 
 
-def test_head_repeat_prefill():
+def test_head_repeat_prefill(tc_path):
     w = Workload("rep", B=2, Hk=2, Hv=8, dk=128, dv=128, T=90, dtype="bf16", gate="channel", seed=3)
     inp = make_inputs(w, device="cuda")
     o, s = _prefill(inp, 64)
     _check(w, inp, o, s)
 
 
-def test_prefill_t4000_full():
+def test_prefill_t4000_full(tc_path):
     """B=1, H=32, dk=dv=128, T=4000, chunk 64 (ragged 32), zero initial state: every unit checked."""
     w = WORKLOADS["prefill_t4000"]
     inp = make_inputs(w, device="cuda")
+    _expect_path(inp, tc_path)
     o, s = _prefill(inp, 64)
     _check(w, inp, o, s)
 
 
-def test_prefill_long_then_decode_sampled():
+def test_prefill_long_then_decode_sampled(tc_path):
     """B=4, H=32, T=16411 (ragged 27), strong decay; then 64 decode steps from the final state.
     Eight sampled (b, h) units are checked against the oracle over all T + 64 tokens."""
     w = WORKLOADS["prefill_long"]
@@ -142,7 +162,7 @@ def test_prefill_T1_matches_decode():
     assert rel_err(s_p, s_d.double().cpu().numpy()) <= 1e-2
 
 
-def test_prefill_continuation():
+def test_prefill_continuation(tc_path):
     """prefill(T1) then prefill(T2) from the carried state equals the oracle over T1 + T2."""
     w = Workload("cont", B=2, Hk=2, Hv=2, dk=128, dv=128, T=230, dtype="bf16", gate="channel", seed=21)
     inp = make_inputs(w, device="cuda")
@@ -162,7 +182,7 @@ def test_zero_length_is_noop():
 
 
 @pytest.mark.parametrize("dtype,chunk", [("bf16", 64), ("bf16", 32), ("f32", 16)])
-def test_bf16_output_is_the_rounded_fp32_output(dtype, chunk):
+def test_bf16_output_is_the_rounded_fp32_output(dtype, chunk, tc_path):
     w = Workload("obf", B=1, Hk=2, Hv=2, dk=128, dv=128, T=77, dtype=dtype, gate="channel", seed=23)
     inp = make_inputs(w, device="cuda")
     o32, s1 = _prefill(inp, chunk)
@@ -174,7 +194,7 @@ def test_bf16_output_is_the_rounded_fp32_output(dtype, chunk):
     assert torch.equal(o16, o32.to(torch.bfloat16))
 
 
-def test_tensor_core_path_reports_ok_status():
+def test_tensor_core_path_reports_ok_status(tc_path):
     """The tensor-core prefill leaves CGDR_OK in its workspace status word."""
     w = Workload("st", B=1, Hk=1, Hv=1, dk=128, dv=128, T=70, dtype="bf16", gate="channel", seed=4)
     inp = make_inputs(w, device="cuda")
@@ -187,7 +207,7 @@ def test_tensor_core_path_reports_ok_status():
     assert cg.workspace_status(ws) == cg.OK
 
 
-def test_mixed_wide_and_narrow_chunks():
+def test_mixed_wide_and_narrow_chunks(tc_path):
     """Decay that switches between mild and extreme across chunks (both A/P paths in one call)."""
     w = Workload("mix", B=1, Hk=2, Hv=2, dk=128, dv=128, T=260, dtype="bf16", gate="channel", seed=31)
     inp = make_inputs(w, device="cuda")
@@ -196,3 +216,19 @@ def test_mixed_wide_and_narrow_chunks():
     inp["g"] = g
     o, s = _prefill(inp, 64)
     _check(w, inp, o, s)
+
+
+def test_both_tensor_core_kernels_agree():
+    """The per-head and the cluster kernel run the same arithmetic per chunk; their results agree
+    far inside the oracle tolerance (only the order of the fp32 state carry is shared)."""
+    w = Workload("agree", B=1, Hk=2, Hv=4, dk=128, dv=128, T=700, dtype="bf16", gate="channel", seed=55)
+    inp = make_inputs(w, device="cuda")
+    outs = []
+    try:
+        for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER):
+            cg.set_prefill_path(path)
+            outs.append(_prefill(inp, 64))
+    finally:
+        cg.set_prefill_path(cg.PREFILL_AUTO)
+    (o1, s1), (o2, s2) = outs
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
