@@ -62,6 +62,37 @@ cgdr_status check(const cgdr_args *a, bool prefill) {
 
 }  // namespace
 
+namespace cgdr {
+
+int prefill_path(const cgdr_args &a, bool allow_cluster) {
+    const int choice = g_prefill_path.load();
+    if (choice == CGDR_PREFILL_SIMT || !prefill_tc05_supported(a)) return CGDR_PREFILL_SIMT;
+    int path = choice;
+    if (path == CGDR_PREFILL_AUTO) {
+        const int64_t units = (int64_t)a.B * a.Hv;
+        const int cap = prefill_cluster_capacity();
+        path = (cap > 0 && units <= cap) ? CGDR_PREFILL_CLUSTER : CGDR_PREFILL_PER_HEAD;
+    }
+    if (path == CGDR_PREFILL_CLUSTER && !allow_cluster) path = CGDR_PREFILL_PER_HEAD;
+    return path;
+}
+
+size_t prefill_workspace_for(const cgdr_args &a, int path) {
+    if (path == CGDR_PREFILL_CLUSTER) return prefill_cluster_workspace(a);
+    if (path == CGDR_PREFILL_PER_HEAD) return prefill_tc05_workspace(a);
+    return 0;
+}
+
+cgdr_status prefill_dispatch(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s, bool allow_cluster) {
+    const int path = prefill_path(a, allow_cluster);
+    if (path == CGDR_PREFILL_SIMT) return launch_prefill_simt(a, s);
+    const size_t need = prefill_workspace_for(a, path);
+    if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
+    return path == CGDR_PREFILL_CLUSTER ? launch_prefill_cluster(a, ws, s) : launch_prefill_tc05(a, ws, s);
+}
+
+}  // namespace cgdr
+
 extern "C" {
 
 int cgdr_abi_version(void) { return CGDR_ABI_VERSION; }
@@ -89,8 +120,7 @@ cgdr_status cgdr_decode(const cgdr_args *a, void *stream) {
 
 size_t cgdr_prefill_workspace_size(const cgdr_args *a) {
     if (check(a, true) != CGDR_OK || a->B == 0 || a->T == 0) return 0;
-    if (cgdr::prefill_tc05_supported(*a)) return cgdr::prefill_tc05_workspace(*a);
-    return 0;
+    return cgdr::prefill_workspace_for(*a, cgdr::prefill_path(*a, true));
 }
 
 cgdr_status cgdr_set_prefill_path(int path) {
@@ -101,25 +131,13 @@ cgdr_status cgdr_set_prefill_path(int path) {
 
 int cgdr_prefill_path_for(const cgdr_args *a) {
     if (check(a, true) != CGDR_OK || a->B == 0 || a->T == 0) return CGDR_PREFILL_AUTO;
-    const int choice = g_prefill_path.load();
-    if (choice == CGDR_PREFILL_SIMT || !cgdr::prefill_tc05_supported(*a)) return CGDR_PREFILL_SIMT;
-    if (choice != CGDR_PREFILL_AUTO) return choice;
-    const int64_t units = (int64_t)a->B * a->Hv;
-    const int cap = cgdr::prefill_cluster_capacity();
-    return (cap > 0 && units <= cap) ? CGDR_PREFILL_CLUSTER : CGDR_PREFILL_PER_HEAD;
+    return cgdr::prefill_path(*a, true);
 }
 
 cgdr_status cgdr_prefill(const cgdr_args *a, void *ws, size_t ws_bytes, void *stream) {
     cgdr_status st = check(a, true);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (g_prefill_path.load() == CGDR_PREFILL_SIMT || !cgdr::prefill_tc05_supported(*a))
-        return cgdr::launch_prefill_simt(*a, s);
-    const size_t need = cgdr::prefill_tc05_workspace(*a);
-    if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
-    const int path = cgdr_prefill_path_for(a);
-    if (path == CGDR_PREFILL_SIMT) return cgdr::launch_prefill_simt(*a, s);
-    return path == CGDR_PREFILL_CLUSTER ? cgdr::launch_prefill_cluster(*a, ws, s) : cgdr::launch_prefill_tc05(*a, ws, s);
+    return cgdr::prefill_dispatch(*a, ws, ws_bytes, static_cast<cudaStream_t>(stream), true);
 }
 
 cgdr_status cgdr_workspace_status(const void *ws, void *stream) {

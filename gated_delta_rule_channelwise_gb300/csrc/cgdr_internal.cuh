@@ -16,6 +16,12 @@ bool prefill_tc05_supported(const cgdr_args &a);
 size_t prefill_tc05_workspace(const cgdr_args &a);
 cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s);
 int prefill_cluster_capacity();
+size_t prefill_cluster_workspace(const cgdr_args &a);
+// The prefill kernel for `a` under the process-wide choice (CGDR_PREFILL_PER_HEAD,
+// _CLUSTER or _SIMT); allow_cluster = false maps the cluster kernel to the per-head one.
+int prefill_path(const cgdr_args &a, bool allow_cluster);
+size_t prefill_workspace_for(const cgdr_args &a, int path);
+cgdr_status prefill_dispatch(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s, bool allow_cluster);
 cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s);
 
 inline float eps_of(const cgdr_args &a) { return a.eps < 0.f ? 1e-6f : a.eps; }

@@ -7,20 +7,21 @@
 // output O = Qg S + P U) and work that does not (decay prefix, operand tiles,
 // causal terms, the triangular transform, W and U~).  Only the first is
 // serial along T.  So:
-//   rank 0 (the chain)   keeps S^T in tensor memory and, per chunk, runs the
-//                        four state-dependent contractions and writes o;
+//   rank 0 (the chain)     keeps S^T in tensor memory and, per chunk, runs
+//                          the four state-dependent contractions and writes o;
 //   ranks 1..3 (preparers) take chunks round robin (chunk c on rank
-//                        1 + c % 3), run the state-free phases and push
-//                        -W, Qg, U~^T, e^gC (inbox A) and P, Kend^T (inbox B)
-//                        into rank 0's shared memory with bulk copies over
-//                        the cluster (distributed shared memory).
-// Handshake per chunk c: rank 0's full_A / full_B barriers count the bytes
-// of c's pushes (armed with expect_tx before the preparer may push); once
-// rank 0's contractions have read inbox A (B) of chunk c it arrives on
-// free_A (free_B) of the preparer of chunk c + 1.  Every wait is bounded;
-// a wait that gives up records CGDR_ERR_TIMEOUT and every CTA leaves its
-// loop, drains its copies, frees tensor memory and meets the others at the
-// final cluster barrier.
+//                          1 + c % 3) and run the state-free phases.
+// Hand-off through L2: a preparer writes -W, Qg, U~^T, e^gC (inbox A image)
+// and P, Kend^T (inbox B image) into one of its two slots of a ring in the
+// workspace, already in rank 0's shared-memory tile layout, and arrives on
+// rank 0's ready barrier for that slot; rank 0 pulls each image into its
+// inbox with one bulk copy as soon as the inbox is free, and arrives on the
+// preparer's slot-free barrier once both copies have landed.  (A bulk copy
+// from L2 fills shared memory about five times faster than a copy between
+// the CTAs' shared memories.)  One barrier per slot on each side keeps every
+// barrier at most one phase ahead of its waiter.  Every wait is bounded; a
+// wait that gives up records CGDR_ERR_TIMEOUT and every CTA leaves its loop,
+// frees tensor memory and meets the others at the final cluster barrier.
 #include <atomic>
 #include <mutex>
 
@@ -31,28 +32,37 @@ namespace {
 
 using namespace tc05c;
 
-constexpr int CLUSTER = 4, NPREP = CLUSTER - 1;
+constexpr int CLUSTER = 4, NPREP = CLUSTER - 1, NSLOT = 2 * NPREP;
+
+// one hand-off slot (bytes): the inbox A image, then the inbox B image
+constexpr int SL_W = 0;                          // -W    [64 x 128] tile
+constexpr int SL_QG = 32768;                     // Qg    [64 x 128] tile
+constexpr int SL_UT = 65536;                     // U~^T  [128 x 64] fp32 in tile order (not rounded)
+constexpr int SL_DEC = 98304;                    // e^gC  [128] fp32
+constexpr uint32_t A_BYTES = 98304 + 512;
+constexpr int SL_P = (int)A_BYTES;               // P      [64 x 64] tile
+constexpr int SL_KE = SL_P + 16384;              // Kend^T [128 x 64] tile
+constexpr uint32_t B_BYTES = 16384 + 32768;
+constexpr size_t SLOT_BYTES = A_BYTES + B_BYTES;
+constexpr size_t WS_HEADER = 256;                // status word, then the slots
+static_assert(SLOT_BYTES % 16 == 0 && SL_P % 16 == 0 && SL_KE % 16 == 0, "bulk copies need 16-byte alignment");
 
 // rank 0 shared memory map (bytes from the 1024-aligned base)
-constexpr int CH_IN_A = 0;
-constexpr int CH_W = CH_IN_A;                    // -W    [64 x 128] tile
-constexpr int CH_QG = CH_IN_A + 32768;           // Qg    [64 x 128] tile
-constexpr int CH_UT = CH_IN_A + 65536;           // U~^T  [128 x 64] fp32 in tile order (not rounded)
-constexpr int CH_DEC = CH_IN_A + 98304;          // e^gC  [128] fp32
-constexpr uint32_t A_BYTES = 98304 + 512;
+constexpr int CH_IN_A = 0;                       // inbox A: the slot's first A_BYTES
+constexpr int CH_W = CH_IN_A + SL_W, CH_QG = CH_IN_A + SL_QG, CH_UT = CH_IN_A + SL_UT, CH_DEC = CH_IN_A + SL_DEC;
 constexpr int CH_SC = 99328;                     // S^T copy [128 x 128] tile, then U^T [128 x 64]
-constexpr int CH_IN_B = CH_SC + 65536;
-constexpr int CH_P = CH_IN_B;                    // P      [64 x 64] tile
-constexpr int CH_KE = CH_IN_B + 16384;           // Kend^T [128 x 64] tile
-constexpr uint32_t B_BYTES = 16384 + 32768;
+constexpr int CH_IN_B = CH_SC + 65536;           // inbox B: the slot's last B_BYTES
+constexpr int CH_P = CH_IN_B, CH_KE = CH_IN_B + 16384;
 constexpr int CH_MISC = CH_IN_B + 49152;
 constexpr int CH_MBAR = CH_MISC, CH_FULL_A = CH_MISC + 8, CH_FULL_B = CH_MISC + 16, CH_TMEM = CH_MISC + 24;
-constexpr int CH_END = CH_MISC + 32;
+constexpr int CH_READY = CH_MISC + 32;           // NSLOT barriers, slot (rank - 1) * 2 + (own chunk & 1)
+constexpr int CH_END = CH_READY + 8 * NSLOT;
+static_assert(CH_IN_A + (int)A_BYTES <= CH_SC, "inbox A overlaps");
 static_assert(CH_SC % 1024 == 0 && CH_IN_B % 1024 == 0 && CH_KE % 1024 == 0, "tiles must be 1024-aligned");
 constexpr int CL_SMEM_BYTES = (CH_END > M_END ? CH_END : M_END) + 1024;
 static_assert(CL_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 
-// ---------------------------------------------------------------- cluster primitives
+// ---------------------------------------------------------------- cluster and bulk-copy primitives
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -66,6 +76,15 @@ __device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
 }
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Non-blocking test, with cluster-scope acquire, of the phase with the given parity.
+__device__ __forceinline__ bool cl_test(uint32_t mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+    return done != 0;
 }
 // Bounded wait, with cluster-scope acquire, for the phase of a local barrier with the given parity.
 __device__ __forceinline__ bool cl_wait(uint32_t mbar, uint32_t parity) {
@@ -85,22 +104,26 @@ __device__ __forceinline__ void arrive_expect_tx(uint32_t mbar, uint32_t bytes) 
 __device__ __forceinline__ void remote_arrive(uint32_t mbar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar_cluster) : "memory");
 }
-// Bulk copy of `bytes` from this CTA's shared memory into another CTA's, completion
-// counted in bytes on the destination CTA's barrier.
-__device__ __forceinline__ void push(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t mbar_cluster) {
+// Order this thread's generic-proxy global accesses with later bulk copies (async proxy).
+__device__ __forceinline__ void fence_global_to_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Bulk copy of `bytes` from global memory into this CTA's shared memory, completion on `mbar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(mbar_cluster) : "memory");
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
-__device__ __forceinline__ void push_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void push_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void push_wait_done() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t owner_of(int c) { return 1u + (uint32_t)(c % NPREP); }
+// Slot of chunk c among the head's NSLOT: two per preparer, alternating over its chunks.
+__device__ __forceinline__ int slot_of(int c) { return 2 * (c % NPREP) + ((c / NPREP) & 1); }
+// Parity of the phase, on a per-slot barrier, that belongs to chunk c.
+__device__ __forceinline__ uint32_t slot_parity(int c) { return (uint32_t)(((c / NPREP) >> 1) & 1); }
 
 // ---------------------------------------------------------------- rank 0: the state carry
+// ia, ib count the bulk loads issued on full_A, full_B (thread 0), so that a
+// failure can wait for the one that may still be landing.
 __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
-                                          int n) {
+                                          int n, const unsigned char *hslots, int &ia, int &ib) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;
     const uint32_t sbase = smem_u32(sm);
@@ -109,6 +132,17 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     float *state = p.state + ((size_t)hd.b * p.Hv + hd.h) * DK * DV;
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
     const float *dec = f32p(sm, CH_DEC);
+    auto load_a = [&](int c) {
+        ++ia;
+        arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
+        bulk_load(sbase + CH_IN_A, hslots + slot_of(c) * SLOT_BYTES + SL_W, A_BYTES, sbase + CH_FULL_A);
+    };
+    auto load_b = [&](int c) {
+        ++ib;
+        arrive_expect_tx(sbase + CH_FULL_B, B_BYTES);
+        bulk_load(sbase + CH_IN_B, hslots + slot_of(c) * SLOT_BYTES + SL_P, B_BYTES, sbase + CH_FULL_B);
+    };
+    auto ready = [&](int c) { return sbase + CH_READY + 8 * slot_of(c); };
 
     // state -> D0 = S^T: row j = trow, columns i in [32 wc, 32 wc + 32)
     {
@@ -117,6 +151,18 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(32 * wc + c) * DV + trow];
         tmem_st32(tmem + lane_off + T_D0 + 32 * wc, v);
     }
+    {
+        int okw = 1;
+        if (tid == 0 && n > 0) {
+            okw = cl_wait(ready(0), slot_parity(0));
+            if (okw) {
+                fence_global_to_async();
+                load_a(0);
+                load_b(0);
+            }
+        }
+        if (__syncthreads_or(!okw)) return false;
+    }
     for (int c = 0; c < n; ++c) {
         const uint32_t d4 = (c & 1) ? T_D4B : T_D4;
         // ---------------------------------------------------------- inbox A: -W, Qg, U~^T, e^gC
@@ -124,7 +170,6 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             const bool done = cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1));
             if (__syncthreads_or(!done)) return false;
         }
-        if (tid == 0 && c + 1 < n) arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
         {
             float u[16];
 #pragma unroll
@@ -153,7 +198,13 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         }
         if (c > 0) store_o(p, obase, tmem + ((c & 1) ? T_D4 : T_D4B), (c - 1) * C, C);   // previous chunk's o
         if (!mma_wait(mb)) return false;
-        if (tid == 0 && c + 1 < n) remote_arrive(mapa_rank(sbase + M_FREE_A, owner_of(c + 1)));
+        // inbox A is free: pull the next chunk's A image now if it is already there
+        bool next_a = false;
+        if (tid == 0 && c + 1 < n && cl_test(ready(c + 1), slot_parity(c + 1))) {
+            fence_global_to_async();
+            load_a(c + 1);
+            next_a = true;
+        }
         {
             float v[16];
             tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, v);
@@ -169,14 +220,26 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             if (__syncthreads_or(!done)) return false;
         }
         if (tid == 0) {
-            if (c + 1 < n) arrive_expect_tx(sbase + CH_FULL_B, B_BYTES);
+            // both images of chunk c have landed: its slot may be rewritten
+            remote_arrive(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) & 1), owner_of(c)));
             fence_after_sync();
             gemm<64, 64>(tmem + d4, sbase + CH_SC, sbase + CH_P, true);       // O^T += U^T P^T
             gemm<128, 64>(tmem + T_D0, sbase + CH_SC, sbase + CH_KE, true);   // S^T += U^T Kend
             commit(mb.mbar);
         }
         if (!mma_wait(mb)) return false;
-        if (tid == 0 && c + 1 < n) remote_arrive(mapa_rank(sbase + M_FREE_B, owner_of(c + 1)));
+        int okw = 1;
+        if (tid == 0 && c + 1 < n) {
+            if (!next_a) {
+                okw = cl_wait(ready(c + 1), slot_parity(c + 1));
+                if (okw) {
+                    fence_global_to_async();
+                    load_a(c + 1);
+                }
+            }
+            if (okw) load_b(c + 1);
+        }
+        if (__syncthreads_or(!okw)) return false;
     }
     if (n > 0) store_o(p, obase, tmem + (((n - 1) & 1) ? T_D4B : T_D4), (n - 1) * C, p.T - (n - 1) * C);
     float v[32];
@@ -188,26 +251,34 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
 
 // ---------------------------------------------------------------- ranks 1..3: state-free phases
 __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
-                                         int n, int rank) {
+                                         int n, int rank, unsigned char *hslots) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;
     const int ci = tid & 127, cq = tid >> 7;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const int trow = 32 * wq + lane;
+    const float *sDec = f32p(sm, M_DEC);
     const int c_first = rank - 1;
     if (c_first < n) {
         stage_rows<STG_V | STG_K>(p, hd, sbase, c_first * C);
         stage_rows<STG_Q | STG_G>(p, hd, sbase, c_first * C);
     }
-    int nfree = 0;
     ChunkRegs cr;
-    for (int c = c_first; c < n; c += NPREP) {
+    int k = 0;                                                           // own chunk index
+    for (int c = c_first; c < n; c += NPREP, ++k) {
         const int t0 = c * C, L = min(C, p.T - t0), tn = t0 + NPREP * C;
+        char *slot = reinterpret_cast<char *>(hslots + slot_of(c) * SLOT_BYTES);
         cp_async_wait_all();
-        __syncthreads();
-        prep_chunk(p, hd, sm, t0, L, tn, cr);
-        if (!causal_terms(sm, tmem, mb, cr)) return false;
+        {
+            // the slot's previous chunk (own chunk k - 2) has been pulled by rank 0
+            int okw = 1;
+            if (tid == 0 && k >= 2) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k & 1), (uint32_t)(((k - 2) >> 1) & 1));
+            if (__syncthreads_or(!okw)) return false;
+        }
+        prep_chunk(p, hd, sm, t0, L, tn, slot + SL_QG, cr);
+        if (tn < p.T) stage_rows<STG_Q | STG_V>(p, hd, sbase, tn);         // F and B are free
+        if (!causal_terms(sm, tmem, mb, cr, slot + SL_P)) return false;
         solve_tb(sm);
         if (tid == 0) {
             fence_after_sync();
@@ -221,47 +292,29 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             float w16[16];
             tmem_ld16(tmem + lane_off + T_D2 + 16 * wc, w16);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) st_tile(sm, R_C, 64, 16 * wc + k, trow, -w16[k]);   // -W [r][i]
+            for (int j = 0; j < 16; ++j) st_tile(slot, SL_W, 64, 16 * wc + j, trow, -w16[j]);   // -W [r][i]
             float u16[16];
             tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, u16);
 #pragma unroll
-            for (int k = 0; k < 16; k += 4)                                   // U~^T [j][s], full fp32
-                *reinterpret_cast<float4 *>(sm + A1_VT + sw_off(128, trow, 16 * wc + k)) =
-                    make_float4(u16[k], u16[k + 1], u16[k + 2], u16[k + 3]);
+            for (int j = 0; j < 16; j += 4)                                   // U~^T [j][s], full fp32
+                *reinterpret_cast<float4 *>(slot + SL_UT + sw_off(128, trow, 16 * wc + j)) =
+                    make_float4(u16[j], u16[j + 1], u16[j + 2], u16[j + 3]);
             const float sc = cr.wide ? 1.f : __expf(cr.gcv - cr.gm);
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {                              // Kend^T [i][s]
                 const int s0 = 16 * cq + jj;
-                st_tile4(sm, R_A1, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
+                st_tile4(slot, SL_KE, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
                          ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc,
                          ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc);
             }
+            if (tid < DK) reinterpret_cast<float *>(slot + SL_DEC)[tid] = sDec[tid];
         }
-        fence_smem_to_async();
+        // every write of the slot is visible, to bulk copies too, before rank 0 hears of it
+        fence_global_to_async();
+        __threadfence();
         __syncthreads();
         if (tn < p.T) stage_rows<STG_G>(p, hd, sbase, tn);                 // A2 is free
-        int pushed = 1;
-        if (tid == 0) {
-            const uint32_t fullA = mapa_rank(sbase + CH_FULL_A, 0), fullB = mapa_rank(sbase + CH_FULL_B, 0);
-            bool okw = c == 0 || cl_wait(sbase + M_FREE_A, (uint32_t)(nfree & 1));
-            if (okw) {
-                push(mapa_rank(sbase + CH_W, 0), sbase + R_C, 32768, fullA);
-                push(mapa_rank(sbase + CH_QG, 0), sbase + R_B, 32768, fullA);
-                push(mapa_rank(sbase + CH_UT, 0), sbase + A1_VT, 32768, fullA);
-                push(mapa_rank(sbase + CH_DEC, 0), sbase + M_DEC, 512, fullA);
-            }
-            okw = okw && (c == 0 || cl_wait(sbase + M_FREE_B, (uint32_t)(nfree & 1)));
-            if (okw) {
-                push(mapa_rank(sbase + CH_P, 0), sbase + R_F, 16384, fullB);
-                push(mapa_rank(sbase + CH_KE, 0), sbase + R_A1, 32768, fullB);
-            }
-            push_commit();
-            push_wait_read();
-            pushed = okw ? 1 : 0;
-        }
-        if (c > 0) ++nfree;
-        if (__syncthreads_or(!pushed)) return false;
-        if (tn < p.T) stage_rows<STG_Q | STG_V>(p, hd, sbase, tn);         // F and B are free
+        if (tid == 0) remote_arrive(mapa_rank(sbase + CH_READY + 8 * slot_of(c), 0));
     }
     return true;
 }
@@ -273,6 +326,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill
     const int rank = (int)cluster_ctarank();
     const bool chain = rank == 0;
     const Head hd = head_of(p, blockIdx.y, blockIdx.x / CLUSTER);
+    unsigned char *hslots = p.slots + ((size_t)hd.b * p.Hv + hd.h) * NSLOT * SLOT_BYTES;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int n = (p.T + C - 1) / C;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + (chain ? CH_TMEM : M_TMEM));
@@ -282,15 +336,12 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill
         if (chain) {
             mbar_init(sbase + CH_FULL_A, 1);
             mbar_init(sbase + CH_FULL_B, 1);
+            for (int i = 0; i < NSLOT; ++i) mbar_init(sbase + CH_READY + 8 * i, 1);
         } else {
-            mbar_init(sbase + M_FREE_A, 1);
-            mbar_init(sbase + M_FREE_B, 1);
+            mbar_init(sbase + M_SLOTFREE, 1);
+            mbar_init(sbase + M_SLOTFREE + 8, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (chain && n > 0) {
-            arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
-            arrive_expect_tx(sbase + CH_FULL_B, B_BYTES);
-        }
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), T_COLS);
     fence_before_sync();
@@ -299,13 +350,18 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill
     const uint32_t tmem = *tslot;
     cluster_barrier();                         // every CTA's barriers exist before any remote use
 
-    const bool ok = chain ? run_chain(p, hd, sm, tmem, mb, n) : run_prep(p, hd, sm, tmem, mb, n, rank);
+    int ia = 0, ib = 0;
+    const bool ok = chain ? run_chain(p, hd, sm, tmem, mb, n, hslots, ia, ib)
+                          : run_prep(p, hd, sm, tmem, mb, n, rank, hslots);
     if (!ok && tid == 0) {
-        // a wait gave up: record it and give the tensor core a bounded chance to finish
+        // a wait gave up: record it, give the tensor core and the last bulk load on
+        // each inbox (at most one can be outstanding) a bounded chance to finish
         atomicExch(p.err, (int)CGDR_ERR_TIMEOUT);
         mbar_wait(mb.mbar, mb.phase ^ 1u, kSpin);
+        if (ia > 0) cl_wait(sbase + CH_FULL_A, (uint32_t)((ia - 1) & 1));
+        if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1));
     }
-    if (!chain && tid == 0) push_wait_done();  // every copy into rank 0 has landed
+    cp_async_wait_all();
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, T_COLS);
@@ -338,8 +394,13 @@ int prefill_cluster_capacity() {
     return g_cluster_fit[dev] - 1;
 }
 
+size_t prefill_cluster_workspace(const cgdr_args &a) {
+    return WS_HEADER + (size_t)a.B * a.Hv * NSLOT * SLOT_BYTES;
+}
+
 cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s) {
-    const Tc05Params p = make_params(a, ws);
+    Tc05Params p = make_params(a, ws);
+    p.slots = static_cast<unsigned char *>(ws) + WS_HEADER;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CGDR_ERR_CUDA;
     if (cudaFuncSetAttribute(prefill_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CL_SMEM_BYTES) !=
         cudaSuccess)

@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         const int L = min(C, p.T - t0);
         cp_async_wait_all();
         __syncthreads();
-        prep_chunk(p, hd, sm, t0, L, t0 + C, cr);
-        if (!(ok = causal_terms(sm, tmem, mb, cr))) break;
+        prep_chunk(p, hd, sm, t0, L, t0 + C, sm + R_B, cr);
+        if (!(ok = causal_terms(sm, tmem, mb, cr, sm + R_F))) break;
         solve_tb(sm);
         // ------------------------------------------------------------ W^T, U~^T
         if (tid == 0) {
@@ -185,6 +185,7 @@ Tc05Params make_params(const cgdr_args &a, void *ws) {
     p.state = a.state; p.o = a.o;
     p.o_sb = a.o_sb; p.o_st = a.o_st; p.o_sh = a.o_sh;
     p.err = static_cast<int *>(ws);
+    p.slots = nullptr;
     return p;
 }
 }  // namespace tc05c
@@ -233,13 +234,16 @@ cgdr_status noalloc_scratch(int dev, void **out) {
 extern "C" cgdr_status cgdr_prefill_noalloc(const cgdr_args *a, void *stream) {
     const cgdr_status st = cgdr_validate(a, 1);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
-    const size_t need = cgdr_prefill_workspace_size(a);
+    // the cluster kernel's hand-off ring does not fit the static scratch: per-head kernel instead
+    const int path = cgdr::prefill_path(*a, false);
+    const size_t need = cgdr::prefill_workspace_for(*a, path);
     if (need > CGDR_NOALLOC_SCRATCH_BYTES) return CGDR_ERR_WORKSPACE;
-    if (need == 0) return cgdr_prefill(a, nullptr, 0, stream);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (need == 0) return cgdr::prefill_dispatch(*a, nullptr, 0, s, false);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return CGDR_ERR_CUDA;
     void *scratch = nullptr;
     const cgdr_status s2 = cgdr::noalloc_scratch(dev, &scratch);
     if (s2 != CGDR_OK) return s2;
-    return cgdr_prefill(a, scratch, CGDR_NOALLOC_SCRATCH_BYTES, stream);
+    return cgdr::prefill_dispatch(*a, scratch, CGDR_NOALLOC_SCRATCH_BYTES, s, false);
 }

@@ -47,8 +47,8 @@ constexpr int R_MISC = 196608;
 // misc (fp32 unless noted)
 constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BETA + 256;
 constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = M_GC + 512;
-constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_FREE_A = M_TMEM + 8, M_FREE_B = M_FREE_A + 8;
-constexpr int M_END = M_FREE_B + 8;
+constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_SLOTFREE = M_TMEM + 8;   // 2 barriers
+constexpr int M_END = M_SLOTFREE + 16;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
 constexpr int LDA = 65;                  // fp32 A rows (padded)
 constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_VT = R_A1 + 32768;
@@ -76,6 +76,7 @@ struct Tc05Params {
     void *o;
     int64_t o_sb, o_st, o_sh;
     int *err;                            // device word set to CGDR_ERR_TIMEOUT if a wait gives up
+    unsigned char *slots;                // cluster kernel: hand-off ring in the workspace (unused per head)
 };
 
 Tc05Params make_params(const cgdr_args &a, void *ws);
@@ -171,9 +172,10 @@ struct ChunkRegs {
 
 // Row norms, beta, the log-decay prefix and the decay-scaled operand tiles of
 // the chunk at t0 (L valid rows) from its staged raw rows; also prefetches the
-// rows at t_pf into L2.  Ends with the operand tiles fenced for the tensor core.
+// rows at t_pf into L2.  The Qg tile goes to qg (shared or global memory, same
+// tile image).  Ends with the operand tiles fenced for the tensor core.
 __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L, int t_pf,
-                                           ChunkRegs &cr) {
+                                           char *qg, ChunkRegs &cr) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ci = tid & 127, cq = tid >> 7;
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
@@ -294,7 +296,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             float eg, e1 = 0.f;
             if (!wide) e1 = __expf(cr.lam[jj] - gm);
             eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
-            st_tile(sm, R_B, 64, r, ci, qt * eg);             // Qg [r][i]
+            st_tile(qg, 0, 64, r, ci, qt * eg);               // Qg [r][i]
             kg4[jj & 3] = kt * eg;
             if ((jj & 3) == 3) st_tile4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);   // Kg^T [i][s]
             if (!wide) {
@@ -316,9 +318,9 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
 }
 
 // The causal terms: A (fp32, strictly lower, beta-folded) into A1_A32, P (tile,
-// lower with diagonal) into R_F, the Kend source into R_A2 for a wide chunk,
-// and V^T into A1_VT.  False if a tensor-core wait gave up.
-__device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, const ChunkRegs &cr) {
+// lower with diagonal) into pt (shared or global memory), the Kend source into
+// R_A2 for a wide chunk, and V^T into A1_VT.  False if a tensor-core wait gave up.
+__device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, const ChunkRegs &cr, char *pt) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;
     const int ci = tid & 127, cq = tid >> 7;
@@ -346,7 +348,7 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
 #pragma unroll
             for (int c = 0; c < 16; c += 4) {
                 const int s = 16 * wc + c;
-                st_tile4(sm, R_F, 64, r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
+                st_tile4(pt, 0, 64, r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
                          s + 2 <= r ? v[c + 2] : 0.f, s + 3 <= r ? v[c + 3] : 0.f);
             }
         }
@@ -384,7 +386,7 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
         for (int e = 0; e < 8; ++e) {
             const int idx = tid + NT * e, r = idx >> 6, s = idx & 63;
             sA[r * LDA + s] = ra[e];
-            st_tile(sm, R_F, 64, r, s, rp[e]);
+            st_tile(pt, 0, 64, r, s, rp[e]);
         }
     }
     // V^T [j][s] (exact: bf16 values are TF32 values)

@@ -122,10 +122,14 @@ cgdr_status cgdr_validate(const cgdr_args *args, int for_prefill);
 cgdr_status cgdr_decode(const cgdr_args *args, void *stream);
 
 /*
- * Bytes of device workspace cgdr_prefill needs for `args` (may be 0).
- * The workspace plays the part of the single scratch arena of "Add parallel
- * chunked prefill for channelwise gated delta rule" (Summary), sliced per
- * (batch, head) unit.  Returns 0 for invalid arguments as well.
+ * Bytes of device workspace cgdr_prefill needs for `args` (may be 0): 0 for
+ * the CUDA-core kernel, 256 for the per-head tensor-core kernel (a status
+ * word), and 256 + B * Hv * 887808 for the cluster kernel (the status word,
+ * then six 147968-byte hand-off slots per (batch, v-head)).  Depends on the
+ * kernel cgdr_prefill_path_for reports.  The workspace plays the part of the
+ * single scratch arena of "Add parallel chunked prefill for channelwise gated
+ * delta rule" (Summary), sliced per (batch, head) unit.  Returns 0 for
+ * invalid arguments as well.
  */
 size_t cgdr_prefill_workspace_size(const cgdr_args *args);
 
@@ -217,8 +221,10 @@ cgdr_status cgdr_workspace_status(const void *workspace, void *stream);
  * wait that gives up is recorded only in the static area, so use cgdr_prefill
  * with a workspace when that status must be read back.
  *
- * Arguments and results are those of cgdr_prefill.  Returns
- * CGDR_ERR_WORKSPACE if the problem needs more scratch than
+ * Arguments and results are those of cgdr_prefill, except that a choice of
+ * the cluster kernel (automatic or forced) runs the per-head tensor-core
+ * kernel: the cluster kernel's hand-off ring does not fit the static area.
+ * Returns CGDR_ERR_WORKSPACE if the problem needs more scratch than
  * CGDR_NOALLOC_SCRATCH_BYTES, and CGDR_ERR_CUDA if the set-up lookup fails.
  */
 cgdr_status cgdr_prefill_noalloc(const cgdr_args *args, void *stream);

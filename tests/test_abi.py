@@ -170,9 +170,16 @@ def test_prefill_path_choice(lib):
         assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=0))) == cg.PREFILL_AUTO
         assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, dk=96))) == cg.PREFILL_AUTO
         assert lib.cgdr_prefill_path_for(None) == cg.PREFILL_AUTO
-        # the cluster kernel needs the workspace too
+        # workspace by kernel: status word; status word + six hand-off slots per (batch, v-head)
+        assert lib.cgdr_set_prefill_path(cg.PREFILL_PER_HEAD) == cg.OK
+        assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 256
         assert lib.cgdr_set_prefill_path(cg.PREFILL_CLUSTER) == cg.OK
+        need = 256 + A.B * A.Hv * 6 * 147968
+        assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == need
         assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
+        assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(1 << 30), need - 16, None) == cg.ERR_WORKSPACE
+        assert lib.cgdr_set_prefill_path(cg.PREFILL_SIMT) == cg.OK
+        assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 0
     finally:
         lib.cgdr_set_prefill_path(cg.PREFILL_AUTO)
     assert lib.cgdr_prefill_path_for(ctypes.byref(A)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
