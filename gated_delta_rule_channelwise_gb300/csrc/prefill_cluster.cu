@@ -35,32 +35,34 @@ using namespace tc05c;
 constexpr int CLUSTER = 4, NPREP = CLUSTER - 1, NSLOT = 2 * NPREP;
 
 // one hand-off slot (bytes): the inbox A image, then the inbox B image
-constexpr int SL_W = 0;                          // -W    [64 x 128] tile
-constexpr int SL_QG = 32768;                     // Qg    [64 x 128] tile
+constexpr int SL_QW = 0;                         // [Qg ; -W]    [128 x 128] tile (rows 0..63 Qg, 64..127 -W)
 constexpr int SL_UT = 65536;                     // U~^T  [128 x 64] fp32 in tile order (not rounded)
 constexpr int SL_DEC = 98304;                    // e^gC  [128] fp32
 constexpr uint32_t A_BYTES = 98304 + 512;
-constexpr int SL_P = (int)A_BYTES;               // P      [64 x 64] tile
-constexpr int SL_KE = SL_P + 16384;              // Kend^T [128 x 64] tile
-constexpr uint32_t B_BYTES = 16384 + 32768;
+constexpr int SL_KP = (int)A_BYTES;              // [Kend^T ; P] [192 x 64] tile (rows 0..127 Kend^T, 128..191 P)
+constexpr uint32_t B_BYTES = 49152;
 constexpr size_t SLOT_BYTES = A_BYTES + B_BYTES;
 constexpr size_t WS_HEADER = 256;                // status word, then the slots
-static_assert(SLOT_BYTES % 16 == 0 && SL_P % 16 == 0 && SL_KE % 16 == 0, "bulk copies need 16-byte alignment");
+static_assert(SLOT_BYTES % 16 == 0 && SL_KP % 16 == 0, "bulk copies need 16-byte alignment");
 
 // rank 0 shared memory map (bytes from the 1024-aligned base)
 constexpr int CH_IN_A = 0;                       // inbox A: the slot's first A_BYTES
-constexpr int CH_W = CH_IN_A + SL_W, CH_QG = CH_IN_A + SL_QG, CH_UT = CH_IN_A + SL_UT, CH_DEC = CH_IN_A + SL_DEC;
-constexpr int CH_SC = 99328;                     // S^T copy [128 x 128] tile, then U^T [128 x 64]
-constexpr int CH_IN_B = CH_SC + 65536;           // inbox B: the slot's last B_BYTES
-constexpr int CH_P = CH_IN_B, CH_KE = CH_IN_B + 16384;
+constexpr int CH_QW = CH_IN_A + SL_QW, CH_UT = CH_IN_A + SL_UT, CH_DEC = CH_IN_A + SL_DEC;
+constexpr int CH_UR = 99328;                     // U^T [128 x 64] tile (TF32-rounded copy)
+constexpr int CH_IN_B = CH_UR + 32768;           // inbox B: the slot's last B_BYTES
+constexpr int CH_KP = CH_IN_B;
 constexpr int CH_MISC = CH_IN_B + 49152;
 constexpr int CH_MBAR = CH_MISC, CH_FULL_A = CH_MISC + 8, CH_FULL_B = CH_MISC + 16, CH_TMEM = CH_MISC + 24;
 constexpr int CH_READY = CH_MISC + 32;           // NSLOT barriers, slot (rank - 1) * 2 + (own chunk & 1)
-constexpr int CH_END = CH_READY + 8 * NSLOT;
-static_assert(CH_IN_A + (int)A_BYTES <= CH_SC, "inbox A overlaps");
-static_assert(CH_SC % 1024 == 0 && CH_IN_B % 1024 == 0 && CH_KE % 1024 == 0, "tiles must be 1024-aligned");
+constexpr int CH_DECC = CH_MISC + 128;           // e^gC copied out of inbox A (the next A image may land early)
+constexpr int CH_END = CH_DECC + 512;
+static_assert(CH_IN_A + (int)A_BYTES <= CH_UR, "inbox A overlaps");
+static_assert(CH_UR % 1024 == 0 && CH_IN_B % 1024 == 0, "tiles must be 1024-aligned");
 constexpr int CL_SMEM_BYTES = (CH_END > M_END ? CH_END : M_END) + 1024;
 static_assert(CL_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
+// rank 0 tensor memory columns: S^T, then O^T, then U^T, so that [O^T | U^T] and
+// [S^T | O^T] are each one accumulator of a single MMA
+constexpr uint32_t T_S = 0, T_O = 128, T_U = 192;
 
 // ---------------------------------------------------------------- cluster and bulk-copy primitives
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -131,25 +133,25 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     const int trow = 32 * wq + lane;
     float *state = p.state + ((size_t)hd.b * p.Hv + hd.h) * DK * DV;
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
-    const float *dec = f32p(sm, CH_DEC);
+    float *dec = f32p(sm, CH_DECC);
     auto load_a = [&](int c) {
         ++ia;
         arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
-        bulk_load(sbase + CH_IN_A, hslots + slot_of(c) * SLOT_BYTES + SL_W, A_BYTES, sbase + CH_FULL_A);
+        bulk_load(sbase + CH_IN_A, hslots + slot_of(c) * SLOT_BYTES + SL_QW, A_BYTES, sbase + CH_FULL_A);
     };
     auto load_b = [&](int c) {
         ++ib;
         arrive_expect_tx(sbase + CH_FULL_B, B_BYTES);
-        bulk_load(sbase + CH_IN_B, hslots + slot_of(c) * SLOT_BYTES + SL_P, B_BYTES, sbase + CH_FULL_B);
+        bulk_load(sbase + CH_IN_B, hslots + slot_of(c) * SLOT_BYTES + SL_KP, B_BYTES, sbase + CH_FULL_B);
     };
     auto ready = [&](int c) { return sbase + CH_READY + 8 * slot_of(c); };
 
-    // state -> D0 = S^T: row j = trow, columns i in [32 wc, 32 wc + 32)
+    // state -> T_S = S^T: row j = trow, columns i in [32 wc, 32 wc + 32)
     {
         float v[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(32 * wc + c) * DV + trow];
-        tmem_st32(tmem + lane_off + T_D0 + 32 * wc, v);
+        tmem_st32(tmem + lane_off + T_S + 32 * wc, v);
     }
     {
         int okw = 1;
@@ -163,9 +165,9 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         }
         if (__syncthreads_or(!okw)) return false;
     }
+    float oprev[16];                       // O^T columns 16 wc .. + 15 of the previous chunk, lane trow
     for (int c = 0; c < n; ++c) {
-        const uint32_t d4 = (c & 1) ? T_D4B : T_D4;
-        // ---------------------------------------------------------- inbox A: -W, Qg, U~^T, e^gC
+        // ---------------------------------------------------------- inbox A: [Qg; -W], U~^T, e^gC
         {
             const bool done = cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1));
             if (__syncthreads_or(!done)) return false;
@@ -177,26 +179,32 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
                 const float4 x = *reinterpret_cast<const float4 *>(sm + CH_UT + sw_off(128, trow, 16 * wc + 4 * m));
                 u[4 * m] = x.x; u[4 * m + 1] = x.y; u[4 * m + 2] = x.z; u[4 * m + 3] = x.w;
             }
-            tmem_st16(tmem + lane_off + T_D3 + 16 * wc, u);                  // D3 = U~^T
-            float v[32];
-            const int i0 = 32 * wc;
-            tmem_ld32(tmem + lane_off + T_D0 + i0, v);                       // S^T copy, then D0 <- D0 Diag(e^gC)
+            tmem_st16(tmem + lane_off + T_U + 16 * wc, u);                   // U^T starts at U~^T
 #pragma unroll
-            for (int k = 0; k < 32; k += 4) st_tile4(sm, CH_SC, 128, trow, i0 + k, v[k], v[k + 1], v[k + 2], v[k + 3]);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] *= dec[i0 + k];
-            tmem_st32(tmem + lane_off + T_D0 + i0, v);
+            for (int m = 0; m < 16; ++m) u[m] = 0.f;
+            tmem_st16(tmem + lane_off + T_O + 16 * wc, u);                   // O^T starts at 0
+            if (tid < DK) dec[tid] = f32p(sm, CH_DEC)[tid];
         }
-        fence_smem_to_async();
         fence_before_sync();
         __syncthreads();
         if (tid == 0) {
+            // [O^T | U^T] += S^T [Qg; -W]^T, S^T read from tensor memory
             fence_after_sync();
-            gemm<64, 128>(tmem + T_D3, sbase + CH_SC, sbase + CH_W, true);    // U^T = U~^T + S^T (-W)^T
-            gemm<64, 128>(tmem + d4, sbase + CH_SC, sbase + CH_QG, false);    // O^T = S^T Qg^T
+            gemm_ts<128, 128>(tmem + T_O, tmem + T_S, sbase + CH_QW, true);
             commit(mb.mbar);
         }
-        if (c > 0) store_o(p, obase, tmem + ((c & 1) ? T_D4 : T_D4B), (c - 1) * C, C);   // previous chunk's o
+        if (c > 0) {                                                         // previous chunk's o
+            const int64_t off0 = obase + (int64_t)((c - 1) * C + 16 * wc) * p.o_st + trow;
+            if (p.o_f32) {
+                float *op = static_cast<float *>(p.o) + off0;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) op[k * p.o_st] = oprev[k];
+            } else {
+                __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
+            }
+        }
         if (!mma_wait(mb)) return false;
         // inbox A is free: pull the next chunk's A image now if it is already there
         bool next_a = false;
@@ -206,15 +214,21 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             next_a = true;
         }
         {
-            float v[16];
-            tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, v);
+            float v[32];
+            const int i0 = 32 * wc;
+            tmem_ld32(tmem + lane_off + T_S + i0, v);                        // S^T <- S^T Diag(e^gC)
 #pragma unroll
-            for (int k = 0; k < 16; k += 4)                                   // U^T [j][s]
-                st_tile4(sm, CH_SC, 128, trow, 16 * wc + k, v[k], v[k + 1], v[k + 2], v[k + 3]);
+            for (int k = 0; k < 32; ++k) v[k] *= dec[i0 + k];
+            tmem_st32(tmem + lane_off + T_S + i0, v);
+            float u[16];
+            tmem_ld16(tmem + lane_off + T_U + 16 * wc, u);
+#pragma unroll
+            for (int k = 0; k < 16; k += 4)                                   // U^T [j][s], rounded
+                st_tile4(sm, CH_UR, 128, trow, 16 * wc + k, u[k], u[k + 1], u[k + 2], u[k + 3]);
         }
         fence_smem_to_async();
         fence_before_sync();
-        // ---------------------------------------------------------- inbox B: P, Kend^T
+        // ---------------------------------------------------------- inbox B: [Kend^T; P]
         {
             const bool done = cl_wait(sbase + CH_FULL_B, (uint32_t)(c & 1));
             if (__syncthreads_or(!done)) return false;
@@ -222,12 +236,13 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         if (tid == 0) {
             // both images of chunk c have landed: its slot may be rewritten
             remote_arrive(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) & 1), owner_of(c)));
+            // [S^T | O^T] += U^T [Kend^T; P]^T
             fence_after_sync();
-            gemm<64, 64>(tmem + d4, sbase + CH_SC, sbase + CH_P, true);       // O^T += U^T P^T
-            gemm<128, 64>(tmem + T_D0, sbase + CH_SC, sbase + CH_KE, true);   // S^T += U^T Kend
+            gemm<192, 64>(tmem + T_S, sbase + CH_UR, sbase + CH_KP, true);
             commit(mb.mbar);
         }
         if (!mma_wait(mb)) return false;
+        tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);
         int okw = 1;
         if (tid == 0 && c + 1 < n) {
             if (!next_a) {
@@ -241,9 +256,23 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         }
         if (__syncthreads_or(!okw)) return false;
     }
-    if (n > 0) store_o(p, obase, tmem + (((n - 1) & 1) ? T_D4B : T_D4), (n - 1) * C, p.T - (n - 1) * C);
+    if (n > 0) {                                                             // last chunk's o
+        const int t0 = (n - 1) * C, nv = min(16, p.T - t0 - 16 * wc);
+        const int64_t off0 = obase + (int64_t)(t0 + 16 * wc) * p.o_st + trow;
+        if (p.o_f32) {
+            float *op = static_cast<float *>(p.o) + off0;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (k < nv) op[k * p.o_st] = oprev[k];
+        } else {
+            __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (k < nv) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
+        }
+    }
     float v[32];
-    tmem_ld32(tmem + lane_off + T_D0 + 32 * wc, v);
+    tmem_ld32(tmem + lane_off + T_S + 32 * wc, v);
 #pragma unroll
     for (int c = 0; c < 32; ++c) state[(size_t)(32 * wc + c) * DV + trow] = v[c];
     return true;
@@ -276,9 +305,9 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             if (tid == 0 && k >= 2) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k & 1), (uint32_t)(((k - 2) >> 1) & 1));
             if (__syncthreads_or(!okw)) return false;
         }
-        prep_chunk(p, hd, sm, t0, L, tn, slot + SL_QG, cr);
+        prep_chunk(p, hd, sm, t0, L, tn, slot + SL_QW, 128, cr);
         if (tn < p.T) stage_rows<STG_Q | STG_V>(p, hd, sbase, tn);         // F and B are free
-        if (!causal_terms(sm, tmem, mb, cr, slot + SL_P)) return false;
+        if (!causal_terms(sm, tmem, mb, cr, slot + SL_KP, 192, 128)) return false;
         solve_tb(sm);
         if (tid == 0) {
             fence_after_sync();
@@ -292,7 +321,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             float w16[16];
             tmem_ld16(tmem + lane_off + T_D2 + 16 * wc, w16);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) st_tile(slot, SL_W, 64, 16 * wc + j, trow, -w16[j]);   // -W [r][i]
+            for (int j = 0; j < 16; ++j) st_tile(slot, SL_QW, 128, 64 + 16 * wc + j, trow, -w16[j]);   // -W [r][i]
             float u16[16];
             tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, u16);
 #pragma unroll
@@ -303,7 +332,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {                              // Kend^T [i][s]
                 const int s0 = 16 * cq + jj;
-                st_tile4(slot, SL_KE, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
+                st_tile4(slot, SL_KP, 192, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
                          ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc,
                          ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc);
             }

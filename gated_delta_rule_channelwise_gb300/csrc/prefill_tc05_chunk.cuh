@@ -50,9 +50,10 @@ constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = 
 constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_SLOTFREE = M_TMEM + 8;   // 2 barriers
 constexpr int M_END = M_SLOTFREE + 16;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
-constexpr int LDA = 65;                  // fp32 A rows (padded)
+constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned)
+constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
 constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_VT = R_A1 + 32768;
-static_assert(A1_Z + 6 * 256 * 4 <= A1_VT, "A1 overflow");
+static_assert(A1_Z + 6 * 16 * LDZ * 4 <= A1_VT, "A1 overflow");
 // Staged raw inputs of a chunk (cp.async, issued while an earlier chunk is finishing):
 // q rows -> F, k rows -> G (bf16 [64][128]); g rows -> A2 (fp32 [64][128]);
 // v rows -> B (bf16 [64][128]); beta -> B + 16 KB (fp32 [64]).
@@ -172,10 +173,11 @@ struct ChunkRegs {
 
 // Row norms, beta, the log-decay prefix and the decay-scaled operand tiles of
 // the chunk at t0 (L valid rows) from its staged raw rows; also prefetches the
-// rows at t_pf into L2.  The Qg tile goes to qg (shared or global memory, same
-// tile image).  Ends with the operand tiles fenced for the tensor core.
+// rows at t_pf into L2.  The Qg tile goes to rows 0..63 of the qg_rows-row tile
+// at qg (shared or global memory, same tile image).  Ends with the operand
+// tiles fenced for the tensor core.
 __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L, int t_pf,
-                                           char *qg, ChunkRegs &cr) {
+                                           char *qg, int qg_rows, ChunkRegs &cr) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ci = tid & 127, cq = tid >> 7;
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
@@ -296,7 +298,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             float eg, e1 = 0.f;
             if (!wide) e1 = __expf(cr.lam[jj] - gm);
             eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
-            st_tile(qg, 0, 64, r, ci, qt * eg);               // Qg [r][i]
+            st_tile(qg, 0, qg_rows, r, ci, qt * eg);          // Qg [r][i]
             kg4[jj & 3] = kt * eg;
             if ((jj & 3) == 3) st_tile4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);   // Kg^T [i][s]
             if (!wide) {
@@ -317,10 +319,12 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
     __syncthreads();
 }
 
-// The causal terms: A (fp32, strictly lower, beta-folded) into A1_A32, P (tile,
-// lower with diagonal) into pt (shared or global memory), the Kend source into
-// R_A2 for a wide chunk, and V^T into A1_VT.  False if a tensor-core wait gave up.
-__device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, const ChunkRegs &cr, char *pt) {
+// The causal terms: A (fp32, strictly lower, beta-folded) into A1_A32, P (lower
+// with diagonal) into rows pt_row0 .. pt_row0 + 63 of the pt_rows-row tile at pt
+// (shared or global memory), the Kend source into R_A2 for a wide chunk, and
+// V^T into A1_VT.  False if a tensor-core wait gave up.
+__device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, const ChunkRegs &cr, char *pt,
+                                             int pt_rows, int pt_row0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;
     const int ci = tid & 127, cq = tid >> 7;
@@ -348,7 +352,7 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
 #pragma unroll
             for (int c = 0; c < 16; c += 4) {
                 const int s = 16 * wc + c;
-                st_tile4(pt, 0, 64, r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
+                st_tile4(pt, 0, pt_rows, pt_row0 + r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
                          s + 2 <= r ? v[c + 2] : 0.f, s + 3 <= r ? v[c + 3] : 0.f);
             }
         }
@@ -386,7 +390,7 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
         for (int e = 0; e < 8; ++e) {
             const int idx = tid + NT * e, r = idx >> 6, s = idx & 63;
             sA[r * LDA + s] = ra[e];
-            st_tile(pt, 0, 64, r, s, rp[e]);
+            st_tile(pt, 0, pt_rows, pt_row0 + r, s, rp[e]);
         }
     }
     // V^T [j][s] (exact: bf16 values are TF32 values)
@@ -398,9 +402,17 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
     return true;
 }
 
-// Tb = (I + A)^-1 Diag(beta) into R_G as a TF32 tile: forward substitution on
-// the four 16 x 16 diagonal blocks, then the off-diagonal blocks one block
-// diagonal at a time.  Ends with Tb fenced for the tensor core.
+// Element (r, c) of the 64 x 64 fp32 X = (I + A)^-1 held in R_G: rows of 64
+// floats with the 16-byte chunks XOR-swizzled by r % 8, so that a float4 of
+// eight different rows hits eight different bank groups.
+__device__ __forceinline__ int xs_off(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
+
+// Tb = (I + A)^-1 Diag(beta) into R_G as a TF32 tile, by 16 x 16 blocks:
+// X_RR = (I + A_RR)^-1 by forward substitution (four blocks at once), then
+// Z_Rm = X_RR A_Rm for the six pairs m < R, then X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS
+// one block diagonal at a time.  Each thread of the product steps owns four
+// consecutive columns of one row (float4 loads).  Ends with Tb fenced for the
+// tensor core.
 __device__ __forceinline__ void solve_tb(char *sm) {
     const int tid = threadIdx.x;
     const float *sA = f32p(sm, A1_A32), *sBeta = f32p(sm, M_BETA);
@@ -416,44 +428,66 @@ __device__ __forceinline__ void solve_tb(char *sm) {
             x[r] = acc;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sXs[(16 * Rb + r) * 64 + 16 * Rb + jc] = x[r];
+        for (int r = 0; r < 16; ++r) sXs[xs_off(16 * Rb + r, 16 * Rb + jc)] = x[r];
     }
     __syncthreads();
-    // Z_Rm = X_RR A_Rm for the six block pairs m < R (pair index R(R-1)/2 + m)
-    for (int idx = tid; idx < 6 * 256; idx += NT) {
-        const int pi = idx >> 8, rho = (idx >> 4) & 15, c = idx & 15;
+    // Z_Rm = X_RR A_Rm: 6 pairs x 16 rows x 4 column quads (pair index R(R-1)/2 + m)
+    if (tid < 384) {
+        const int pi = tid >> 6, rho = (tid >> 2) & 15, c4 = 4 * (tid & 3);
         const int Rb = pi == 0 ? 1 : (pi < 3 ? 2 : 3), mb = pi - Rb * (Rb - 1) / 2;
-        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+        const int xr = 16 * Rb + rho;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-            a4[u & 3] = fmaf(sXs[(16 * Rb + rho) * 64 + 16 * Rb + u], sA[(16 * Rb + u) * LDA + 16 * mb + c], a4[u & 3]);
-        sZ[idx] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+        for (int u4 = 0; u4 < 16; u4 += 4) {
+            const float4 xv = *reinterpret_cast<const float4 *>(sXs + xs_off(xr, 16 * Rb + u4));
+            const float xs4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                const float4 av = *reinterpret_cast<const float4 *>(sA + (16 * Rb + u4 + uu) * LDA + 16 * mb + c4);
+                a[0] = fmaf(xs4[uu], av.x, a[0]);
+                a[1] = fmaf(xs4[uu], av.y, a[1]);
+                a[2] = fmaf(xs4[uu], av.z, a[2]);
+                a[3] = fmaf(xs4[uu], av.w, a[3]);
+            }
+        }
+        *reinterpret_cast<float4 *>(sZ + (pi * 16 + rho) * LDZ + c4) = make_float4(a[0], a[1], a[2], a[3]);
     }
     __syncthreads();
-    // X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS, one block diagonal at a time
-#pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int idx = tid; idx < nblk * 256; idx += NT) {
-            const int blk = idx >> 8, Rb = d + blk, Sb = Rb - d, rho = (idx >> 4) & 15, c = idx & 15;
-            float a4[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int mm = Sb; mm < Rb; ++mm) {
-                const float *z = sZ + (Rb * (Rb - 1) / 2 + mm) * 256 + rho * 16;
-                const float *xs = sXs + (16 * mm) * 64 + 16 * Sb + c;
+    // X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS, one block diagonal d = R - S at a time
 #pragma unroll
-                for (int u = 0; u < 16; ++u) a4[u & 3] = fmaf(z[u], xs[u * 64], a4[u & 3]);
+    for (int d = 1; d < 4; ++d) {
+        if (tid < (4 - d) * 64) {
+            const int blk = tid >> 6, Rb = d + blk, Sb = Rb - d, rho = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < d; ++j) {
+                const int mm = Sb + j;
+                const float *z = sZ + ((Rb * (Rb - 1) / 2 + mm) * 16 + rho) * LDZ;
+#pragma unroll
+                for (int u4 = 0; u4 < 16; u4 += 4) {
+                    const float4 zv = *reinterpret_cast<const float4 *>(z + u4);
+                    const float zs4[4] = {zv.x, zv.y, zv.z, zv.w};
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        const float4 xv = *reinterpret_cast<const float4 *>(sXs + xs_off(16 * mm + u4 + uu, 16 * Sb + c4));
+                        a[0] = fmaf(zs4[uu], xv.x, a[0]);
+                        a[1] = fmaf(zs4[uu], xv.y, a[1]);
+                        a[2] = fmaf(zs4[uu], xv.z, a[2]);
+                        a[3] = fmaf(zs4[uu], xv.w, a[3]);
+                    }
+                }
             }
-            sXs[(16 * Rb + rho) * 64 + 16 * Sb + c] = -((a4[0] + a4[1]) + (a4[2] + a4[3]));
+            *reinterpret_cast<float4 *>(sXs + xs_off(16 * Rb + rho, 16 * Sb + c4)) = make_float4(-a[0], -a[1], -a[2], -a[3]);
         }
         __syncthreads();
     }
     {
-        // thread t converts elements [4t, 4t+4) and [2048 + 4t, 2048 + 4t + 4): 16-byte reads, no conflicts
+        // thread t converts elements [4t, 4t+4) and [2048 + 4t, 2048 + 4t + 4) of X: Tb = X Diag(beta), lower part
         float4 tv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
-            const float4 x = *reinterpret_cast<const float4 *>(sXs + idx);
+            const float4 x = *reinterpret_cast<const float4 *>(sXs + xs_off(r, s2));
             tv[e] = make_float4(s2 <= r ? x.x * sBeta[s2] : 0.f, s2 + 1 <= r ? x.y * sBeta[s2 + 1] : 0.f,
                                 s2 + 2 <= r ? x.z * sBeta[s2 + 2] : 0.f, s2 + 3 <= r ? x.w * sBeta[s2 + 3] : 0.f);
         }

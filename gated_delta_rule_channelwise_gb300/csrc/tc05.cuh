@@ -62,6 +62,25 @@ __device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_smem, uint32_t 
     }
 }
 
+// The same with A read from tensor memory: A[m][k] = TMEM[lane m][column a_tmem + k],
+// fp32 values taken as TF32 (the low 13 mantissa bits are ignored).
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+template <int N, int K>
+__device__ __forceinline__ void gemm_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
+    constexpr uint32_t idesc = idesc_tf32(N);
+#pragma unroll
+    for (int ks = 0; ks < K / 8; ++ks) {
+        const uint32_t boff = (uint32_t)((ks >> 2) * N * 128 + (ks & 3) * 32);
+        mma_tf32_ts(d_tmem, a_tmem + 8 * ks, smem_desc(b_smem + boff), idesc, (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
 __device__ __forceinline__ void commit(uint32_t mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar));
 }

@@ -219,8 +219,9 @@ def test_mixed_wide_and_narrow_chunks(tc_path):
 
 
 def test_both_tensor_core_kernels_agree():
-    """The per-head and the cluster kernel run the same arithmetic per chunk; their results agree
-    far inside the oracle tolerance (only the order of the fp32 state carry is shared)."""
+    """The per-head and the cluster kernel run the same chunk algorithm; they differ only in the
+    rounding of the state operand (rounded to TF32 in shared memory, or read from tensor memory
+    and truncated) and in accumulation order, so they agree far inside the oracle tolerance."""
     w = Workload("agree", B=1, Hk=2, Hv=4, dk=128, dv=128, T=700, dtype="bf16", gate="channel", seed=55)
     inp = make_inputs(w, device="cuda")
     outs = []
@@ -231,4 +232,6 @@ def test_both_tensor_core_kernels_agree():
     finally:
         cg.set_prefill_path(cg.PREFILL_AUTO)
     (o1, s1), (o2, s2) = outs
-    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    eo, es = rel_err(o2, o1.double().cpu().numpy()), rel_err(s2, s1.double().cpu().numpy())
+    print("[kernels] o %.3e S %.3e" % (eo, es))
+    assert eo <= 5e-3 and es <= 5e-3
