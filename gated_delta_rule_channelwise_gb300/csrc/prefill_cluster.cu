@@ -5,23 +5,26 @@
 // gated delta rule" (executorch PR #21061, Summary) splits into work that
 // needs the state (the carry S <- e^gC S + Kend^T U with U = U~ - W S, and the
 // output O = Qg S + P U) and work that does not (decay prefix, operand tiles,
-// causal terms, the triangular transform, W and U~).  Only the first is
-// serial along T.  So:
-//   rank 0 (the chain)     keeps S^T in tensor memory and, per chunk, runs
-//                          the four state-dependent contractions and writes o;
+// causal terms, the triangular transform Tb).  Only the first is serial along
+// T.  So:
+//   rank 0 (the chain)     keeps S^T in tensor memory and, per chunk, forms
+//                          W = Tb Kg and U~ = Tb V, then the state-dependent
+//                          contractions, and writes o;
 //   ranks 1..3 (preparers) take chunks round robin (chunk c on rank
 //                          1 + c % 3) and run the state-free phases.
-// Hand-off through L2: a preparer writes -W, Qg, U~^T, e^gC (inbox A image)
-// and P, Kend^T (inbox B image) into one of its two slots of a ring in the
-// workspace, already in rank 0's shared-memory tile layout, and arrives on
-// rank 0's ready barrier for that slot; rank 0 pulls each image into its
-// inbox with one bulk copy as soon as the inbox is free, and arrives on the
-// preparer's slot-free barrier once both copies have landed.  (A bulk copy
-// from L2 fills shared memory about five times faster than a copy between
-// the CTAs' shared memories.)  One barrier per slot on each side keeps every
-// barrier at most one phase ahead of its waiter.  Every wait is bounded; a
-// wait that gives up records CGDR_ERR_TIMEOUT and every CTA leaves its loop,
-// frees tensor memory and meets the others at the final cluster barrier.
+// Hand-off through L2: a preparer sends the tiles it has built in shared
+// memory -- Qg, Kg^T, V^T, Tb, e^gC (inbox A image) and Kend^T, P (inbox B
+// image) -- with bulk stores into one of its three slots of a ring in the
+// workspace, each piece at its place in rank 0's shared-memory tile layout,
+// and arrives on rank 0's ready barrier for that slot; rank 0 pulls each
+// image into its inbox with one bulk load as soon as the inbox is free, and
+// arrives on the preparer's slot-free barrier once both loads have landed.
+// (Bulk copies through L2 move data about five times faster than copies
+// between the CTAs' shared memories, and run beside the threads' work.)  One
+// barrier per slot on each side keeps every barrier at most one phase ahead
+// of its waiter.  Every wait is bounded; a wait that gives up records
+// CGDR_ERR_TIMEOUT and every CTA leaves its loop, frees tensor memory and
+// meets the others at the final cluster barrier.
 #include <atomic>
 #include <mutex>
 
@@ -32,13 +35,15 @@ namespace {
 
 using namespace tc05c;
 
-constexpr int CLUSTER = 4, NPREP = CLUSTER - 1, NSLOT = 2 * NPREP;
+constexpr int CLUSTER = 4, NPREP = CLUSTER - 1, NSLOTP = 3, NSLOT = NSLOTP * NPREP;   // NSLOTP slots per preparer
 
 // one hand-off slot (bytes): the inbox A image, then the inbox B image
-constexpr int SL_QW = 0;                         // [Qg ; -W]    [128 x 128] tile (rows 0..63 Qg, 64..127 -W)
-constexpr int SL_UT = 65536;                     // U~^T  [128 x 64] fp32 in tile order (not rounded)
-constexpr int SL_DEC = 98304;                    // e^gC  [128] fp32
-constexpr uint32_t A_BYTES = 98304 + 512;
+constexpr int SL_QW = 0;                         // [Qg ; -W] [128 x 128] tile: rows 0..63 Qg (rows 64..127: rank 0)
+constexpr int SL_KG = 65536;                     // Kg^T [128 x 64] tile
+constexpr int SL_VT = 98304;                     // V^T  [128 x 64] tile
+constexpr int SL_TB = 131072;                    // Tb   [64 x 64] tile
+constexpr int SL_DEC = 147456;                   // e^gC [128] fp32
+constexpr uint32_t A_BYTES = 147456 + 512;
 constexpr int SL_KP = (int)A_BYTES;              // [Kend^T ; P] [192 x 64] tile (rows 0..127 Kend^T, 128..191 P)
 constexpr uint32_t B_BYTES = 49152;
 constexpr size_t SLOT_BYTES = A_BYTES + B_BYTES;
@@ -47,22 +52,25 @@ static_assert(SLOT_BYTES % 16 == 0 && SL_KP % 16 == 0, "bulk copies need 16-byte
 
 // rank 0 shared memory map (bytes from the 1024-aligned base)
 constexpr int CH_IN_A = 0;                       // inbox A: the slot's first A_BYTES
-constexpr int CH_QW = CH_IN_A + SL_QW, CH_UT = CH_IN_A + SL_UT, CH_DEC = CH_IN_A + SL_DEC;
-constexpr int CH_UR = 99328;                     // U^T [128 x 64] tile (TF32-rounded copy)
+constexpr int CH_QW = CH_IN_A + SL_QW, CH_KG = CH_IN_A + SL_KG, CH_VT = CH_IN_A + SL_VT, CH_TB = CH_IN_A + SL_TB;
+constexpr int CH_DEC = CH_IN_A + SL_DEC;
+constexpr int CH_UR = 148480;                    // U^T [128 x 64] tile (TF32-rounded copy)
 constexpr int CH_IN_B = CH_UR + 32768;           // inbox B: the slot's last B_BYTES
 constexpr int CH_KP = CH_IN_B;
 constexpr int CH_MISC = CH_IN_B + 49152;
 constexpr int CH_MBAR = CH_MISC, CH_FULL_A = CH_MISC + 8, CH_FULL_B = CH_MISC + 16, CH_TMEM = CH_MISC + 24;
-constexpr int CH_READY = CH_MISC + 32;           // NSLOT barriers, slot (rank - 1) * 2 + (own chunk & 1)
+constexpr int CH_READY = CH_MISC + 32;           // NSLOT barriers, one per slot
 constexpr int CH_DECC = CH_MISC + 128;           // e^gC copied out of inbox A (the next A image may land early)
 constexpr int CH_END = CH_DECC + 512;
+static_assert(CH_READY + 8 * NSLOT <= CH_DECC, "barriers overlap");
 static_assert(CH_IN_A + (int)A_BYTES <= CH_UR, "inbox A overlaps");
-static_assert(CH_UR % 1024 == 0 && CH_IN_B % 1024 == 0, "tiles must be 1024-aligned");
+static_assert(CH_UR % 1024 == 0 && CH_IN_B % 1024 == 0 && CH_KG % 1024 == 0 && CH_VT % 1024 == 0 &&
+              CH_TB % 1024 == 0, "tiles must be 1024-aligned");
 constexpr int CL_SMEM_BYTES = (CH_END > M_END ? CH_END : M_END) + 1024;
 static_assert(CL_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 // rank 0 tensor memory columns: S^T, then O^T, then U^T, so that [O^T | U^T] and
-// [S^T | O^T] are each one accumulator of a single MMA
-constexpr uint32_t T_S = 0, T_O = 128, T_U = 192;
+// [S^T | O^T] are each one accumulator of a single MMA; W^T after them
+constexpr uint32_t T_S = 0, T_O = 128, T_U = 192, T_W = 256;
 
 // ---------------------------------------------------------------- cluster and bulk-copy primitives
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -108,6 +116,16 @@ __device__ __forceinline__ void remote_arrive(uint32_t mbar_cluster) {
 }
 // Order this thread's generic-proxy global accesses with later bulk copies (async proxy).
 __device__ __forceinline__ void fence_global_to_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Bulk copy of `bytes` from this CTA's shared memory to global memory; bulk_commit closes
+// a group of them.  wait_read<N>: at most N most recent groups still reading shared memory;
+// bulk_store_wait: every group's writes complete.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bulk_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Bulk copy of `bytes` from global memory into this CTA's shared memory, completion on `mbar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
     asm volatile(
@@ -116,10 +134,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 }
 
 __device__ __forceinline__ uint32_t owner_of(int c) { return 1u + (uint32_t)(c % NPREP); }
-// Slot of chunk c among the head's NSLOT: two per preparer, alternating over its chunks.
-__device__ __forceinline__ int slot_of(int c) { return 2 * (c % NPREP) + ((c / NPREP) & 1); }
+// Slot of chunk c among the head's NSLOT: NSLOTP per preparer, in turn over its chunks.
+__device__ __forceinline__ int slot_of(int c) { return NSLOTP * (c % NPREP) + (c / NPREP) % NSLOTP; }
 // Parity of the phase, on a per-slot barrier, that belongs to chunk c.
-__device__ __forceinline__ uint32_t slot_parity(int c) { return (uint32_t)(((c / NPREP) >> 1) & 1); }
+__device__ __forceinline__ uint32_t slot_parity(int c) { return (uint32_t)((c / NPREP / NSLOTP) & 1); }
 
 // ---------------------------------------------------------------- rank 0: the state carry
 // ia, ib count the bulk loads issued on full_A, full_B (thread 0), so that a
@@ -167,30 +185,24 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     }
     float oprev[16];                       // O^T columns 16 wc .. + 15 of the previous chunk, lane trow
     for (int c = 0; c < n; ++c) {
-        // ---------------------------------------------------------- inbox A: [Qg; -W], U~^T, e^gC
+        // ---------------------------------------------------------- inbox A: Qg, Kg^T, V^T, Tb, e^gC
         {
             const bool done = cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1));
             if (__syncthreads_or(!done)) return false;
         }
         {
-            float u[16];
+            float z[16];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float4 x = *reinterpret_cast<const float4 *>(sm + CH_UT + sw_off(128, trow, 16 * wc + 4 * m));
-                u[4 * m] = x.x; u[4 * m + 1] = x.y; u[4 * m + 2] = x.z; u[4 * m + 3] = x.w;
-            }
-            tmem_st16(tmem + lane_off + T_U + 16 * wc, u);                   // U^T starts at U~^T
-#pragma unroll
-            for (int m = 0; m < 16; ++m) u[m] = 0.f;
-            tmem_st16(tmem + lane_off + T_O + 16 * wc, u);                   // O^T starts at 0
+            for (int m = 0; m < 16; ++m) z[m] = 0.f;
+            tmem_st16(tmem + lane_off + T_O + 16 * wc, z);                   // O^T starts at 0
             if (tid < DK) dec[tid] = f32p(sm, CH_DEC)[tid];
         }
         fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            // [O^T | U^T] += S^T [Qg; -W]^T, S^T read from tensor memory
             fence_after_sync();
-            gemm_ts<128, 128>(tmem + T_O, tmem + T_S, sbase + CH_QW, true);
+            gemm<64, 64>(tmem + T_W, sbase + CH_KG, sbase + CH_TB, false);   // W^T  = Kg^T Tb^T
+            gemm<64, 64>(tmem + T_U, sbase + CH_VT, sbase + CH_TB, false);   // U~^T = V^T Tb^T
             commit(mb.mbar);
         }
         if (c > 0) {                                                         // previous chunk's o
@@ -204,6 +216,22 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
 #pragma unroll
                 for (int k = 0; k < 16; ++k) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
             }
+        }
+        if (!mma_wait(mb)) return false;
+        {
+            float w16[16];
+            tmem_ld16(tmem + lane_off + T_W + 16 * wc, w16);                 // -W [r][i] into rows 64.. of [Qg; -W]
+#pragma unroll
+            for (int j = 0; j < 16; ++j) st_tile(sm, CH_QW, 128, 64 + 16 * wc + j, trow, -w16[j]);
+        }
+        fence_smem_to_async();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            // [O^T | U^T] += S^T [Qg; -W]^T, S^T read from tensor memory
+            fence_after_sync();
+            gemm_ts<128, 128>(tmem + T_O, tmem + T_S, sbase + CH_QW, true);
+            commit(mb.mbar);
         }
         if (!mma_wait(mb)) return false;
         // inbox A is free: pull the next chunk's A image now if it is already there
@@ -235,7 +263,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         }
         if (tid == 0) {
             // both images of chunk c have landed: its slot may be rewritten
-            remote_arrive(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) & 1), owner_of(c)));
+            remote_arrive(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) % NSLOTP), owner_of(c)));
             // [S^T | O^T] += U^T [Kend^T; P]^T
             fence_after_sync();
             gemm<192, 64>(tmem + T_S, sbase + CH_UR, sbase + CH_KP, true);
@@ -279,72 +307,94 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
 }
 
 // ---------------------------------------------------------------- ranks 1..3: state-free phases
+// Own chunk k (chunk c = rank - 1 + 3 k) goes to slot k % NSLOTP of this preparer.  Every
+// output leaves by bulk store from the shared-memory tile it was built in, as soon as the
+// tile is complete; the staging of the next own chunk's rows follows as the tiles' reads
+// finish.  Chunk k is announced to rank 0 at the top of own chunk k + 1 (or after the
+// loop), once its stores have completed.
 __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
                                          int n, int rank, unsigned char *hslots) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wq = warp & 3, wc = warp >> 2;
+    const int tid = threadIdx.x;
     const int ci = tid & 127, cq = tid >> 7;
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
-    const int trow = 32 * wq + lane;
-    const float *sDec = f32p(sm, M_DEC);
     const int c_first = rank - 1;
     if (c_first < n) {
         stage_rows<STG_V | STG_K>(p, hd, sbase, c_first * C);
         stage_rows<STG_Q | STG_G>(p, hd, sbase, c_first * C);
     }
+    auto slot_ptr = [&](int cc) { return reinterpret_cast<char *>(hslots + slot_of(cc) * SLOT_BYTES); };
+    // chunk cc's stores have completed, to bulk loads too: tell rank 0
+    auto announce = [&](int cc) {
+        if (tid == 0) {
+            bulk_store_wait();
+            remote_arrive(mapa_rank(sbase + CH_READY + 8 * slot_of(cc), 0));
+        }
+    };
     ChunkRegs cr;
     int k = 0;                                                           // own chunk index
     for (int c = c_first; c < n; c += NPREP, ++k) {
         const int t0 = c * C, L = min(C, p.T - t0), tn = t0 + NPREP * C;
-        char *slot = reinterpret_cast<char *>(hslots + slot_of(c) * SLOT_BYTES);
+        char *slot = slot_ptr(c);
         cp_async_wait_all();
+        if (k > 0) announce(c - NPREP);
         {
-            // the slot's previous chunk (own chunk k - 2) has been pulled by rank 0
+            // the slot's previous chunk (own chunk k - NSLOTP) has been pulled by rank 0
             int okw = 1;
-            if (tid == 0 && k >= 2) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k & 1), (uint32_t)(((k - 2) >> 1) & 1));
+            if (tid == 0 && k >= NSLOTP)
+                okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1));
             if (__syncthreads_or(!okw)) return false;
         }
-        prep_chunk(p, hd, sm, t0, L, tn, slot + SL_QW, 128, cr);
-        if (tn < p.T) stage_rows<STG_Q | STG_V>(p, hd, sbase, tn);         // F and B are free
-        if (!causal_terms(sm, tmem, mb, cr, slot + SL_KP, 192, 128)) return false;
+        // operand tiles; prefetch the next own chunk's rows into L2 (they are staged late)
+        prep_chunk(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
+        if (tid == 0) {
+            // Qg (64-row tile: 8 KB per K block) into rows 0..63 of [Qg; -W]; Kg^T; e^gC
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) bulk_store(slot + SL_QW + kb * 16384, sbase + R_B + kb * 8192, 8192);
+            bulk_store(slot + SL_KG, sbase + R_C, 32768);
+            bulk_store(slot + SL_DEC, sbase + M_DEC, 512);
+            bulk_commit();
+        }
+        if (!causal_terms<true>(sm, tmem, mb, cr, sm + R_F, 64, 0)) return false;
+        if (tid == 0) {
+            // P (64-row tile) into rows 128..191 of [Kend^T; P]; V^T
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576 + 16384, sbase + R_F + kb * 8192, 8192);
+            bulk_store(slot + SL_VT, sbase + A1_VT, 32768);
+            bulk_commit();
+        }
         solve_tb(sm);
         if (tid == 0) {
-            fence_after_sync();
-            gemm<64, 64>(tmem + T_D2, sbase + R_C, sbase + R_G, false);    // W^T  = Kg^T Tb^T
-            gemm<64, 64>(tmem + T_D3, sbase + A1_VT, sbase + R_G, false);  // U~^T = V^T Tb^T
-            commit(mb.mbar);
+            bulk_store(slot + SL_TB, sbase + R_G, 16384);
+            bulk_commit();
+            bulk_wait_read<0>();                                           // R_B, R_C, R_F, A1_VT, R_G read
         }
-        if (!mma_wait(mb)) return false;
-        if (tn < p.T) stage_rows<STG_K>(p, hd, sbase, tn);                 // G is free
+        __syncthreads();
+        if (tn < p.T) {
+            stage_rows<STG_Q | STG_V>(p, hd, sbase, tn);
+            stage_rows<STG_K>(p, hd, sbase, tn);
+        }
         {
-            float w16[16];
-            tmem_ld16(tmem + lane_off + T_D2 + 16 * wc, w16);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) st_tile(slot, SL_QW, 128, 64 + 16 * wc + j, trow, -w16[j]);   // -W [r][i]
-            float u16[16];
-            tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, u16);
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)                                   // U~^T [j][s], full fp32
-                *reinterpret_cast<float4 *>(slot + SL_UT + sw_off(128, trow, 16 * wc + j)) =
-                    make_float4(u16[j], u16[j + 1], u16[j + 2], u16[j + 3]);
+            // Kend^T [i][s] = X2 [s][i] e^(gC - gm) (wide chunk: the Kend source as is) into R_C
             const float sc = cr.wide ? 1.f : __expf(cr.gcv - cr.gm);
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 4) {                              // Kend^T [i][s]
+            for (int jj = 0; jj < 16; jj += 4) {
                 const int s0 = 16 * cq + jj;
-                st_tile4(slot, SL_KP, 192, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
+                st_tile4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
                          ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc,
                          ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc);
             }
-            if (tid < DK) reinterpret_cast<float *>(slot + SL_DEC)[tid] = sDec[tid];
         }
-        // every write of the slot is visible, to bulk copies too, before rank 0 hears of it
-        fence_global_to_async();
-        __threadfence();
+        fence_smem_to_async();
         __syncthreads();
+        if (tid == 0) {
+            // Kend^T (128-row tile: 16 KB per K block) into rows 0..127 of [Kend^T; P]
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576, sbase + R_C + kb * 16384, 16384);
+            bulk_commit();
+        }
         if (tn < p.T) stage_rows<STG_G>(p, hd, sbase, tn);                 // A2 is free
-        if (tid == 0) remote_arrive(mapa_rank(sbase + CH_READY + 8 * slot_of(c), 0));
     }
+    if (k > 0) announce(c_first + NPREP * (k - 1));                      // the last own chunk
     return true;
 }
 
@@ -367,8 +417,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill
             mbar_init(sbase + CH_FULL_B, 1);
             for (int i = 0; i < NSLOT; ++i) mbar_init(sbase + CH_READY + 8 * i, 1);
         } else {
-            mbar_init(sbase + M_SLOTFREE, 1);
-            mbar_init(sbase + M_SLOTFREE + 8, 1);
+            for (int i = 0; i < NSLOTP; ++i) mbar_init(sbase + M_SLOTFREE + 8 * i, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }

@@ -47,8 +47,8 @@ constexpr int R_MISC = 196608;
 // misc (fp32 unless noted)
 constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BETA + 256;
 constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = M_GC + 512;
-constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_SLOTFREE = M_TMEM + 8;   // 2 barriers
-constexpr int M_END = M_SLOTFREE + 16;
+constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_SLOTFREE = M_TMEM + 8;   // 4 barriers
+constexpr int M_END = M_SLOTFREE + 32;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
 constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned)
 constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
@@ -323,6 +323,8 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
 // with diagonal) into rows pt_row0 .. pt_row0 + 63 of the pt_rows-row tile at pt
 // (shared or global memory), the Kend source into R_A2 for a wide chunk, and
 // V^T into A1_VT.  False if a tensor-core wait gave up.
+// kBulkOut: P and V^T leave by bulk copy, so fence them for the async proxy.
+template <bool kBulkOut>
 __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, const ChunkRegs &cr, char *pt,
                                              int pt_rows, int pt_row0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -398,6 +400,7 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
     for (int jj = 0; jj < 16; jj += 4)
         *reinterpret_cast<float4 *>(sm + A1_VT + sw_off(128, ci, 16 * cq + jj)) =
             make_float4(cr.vreg[jj], cr.vreg[jj + 1], cr.vreg[jj + 2], cr.vreg[jj + 3]);
+    if (kBulkOut) fence_smem_to_async();
     __syncthreads();
     return true;
 }

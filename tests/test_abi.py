@@ -174,7 +174,7 @@ def test_prefill_path_choice(lib):
         assert lib.cgdr_set_prefill_path(cg.PREFILL_PER_HEAD) == cg.OK
         assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 256
         assert lib.cgdr_set_prefill_path(cg.PREFILL_CLUSTER) == cg.OK
-        need = 256 + A.B * A.Hv * 6 * 147968
+        need = 256 + A.B * A.Hv * 9 * 197120
         assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == need
         assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
         assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(1 << 30), need - 16, None) == cg.ERR_WORKSPACE
