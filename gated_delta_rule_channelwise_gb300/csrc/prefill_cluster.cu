@@ -114,6 +114,11 @@ __device__ __forceinline__ void arrive_expect_tx(uint32_t mbar, uint32_t bytes) 
 __device__ __forceinline__ void remote_arrive(uint32_t mbar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar_cluster) : "memory");
 }
+// Arrive without release: for a signal that orders nothing of this thread's own memory
+// operations (a release would first wait for its outstanding global stores).
+__device__ __forceinline__ void remote_arrive_relaxed(uint32_t mbar_cluster) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar_cluster) : "memory");
+}
 // Order this thread's generic-proxy global accesses with later bulk copies (async proxy).
 __device__ __forceinline__ void fence_global_to_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 // Bulk copy of `bytes` from this CTA's shared memory to global memory; bulk_commit closes
@@ -262,12 +267,13 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             if (__syncthreads_or(!done)) return false;
         }
         if (tid == 0) {
-            // both images of chunk c have landed: its slot may be rewritten
-            remote_arrive(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) % NSLOTP), owner_of(c)));
             // [S^T | O^T] += U^T [Kend^T; P]^T
             fence_after_sync();
             gemm<192, 64>(tmem + T_S, sbase + CH_UR, sbase + CH_KP, true);
             commit(mb.mbar);
+            // both images of chunk c have landed (their bulk loads completed, which this
+            // thread observed): its slot may be rewritten.  Nothing else to order, so no release.
+            remote_arrive_relaxed(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) % NSLOTP), owner_of(c)));
         }
         if (!mma_wait(mb)) return false;
         tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);
