@@ -350,8 +350,8 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
                 okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1));
             if (__syncthreads_or(!okw)) return false;
         }
-        // operand tiles; prefetch the next own chunk's rows into L2 (they are staged late)
-        prep_chunk(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
+        // operand tiles; prefetch the next own chunk's g rows into L2 (they are staged last)
+        prep_chunk<false>(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
         if (tid == 0) {
             // Qg (64-row tile: 8 KB per K block) into rows 0..63 of [Qg; -W]; Kg^T; e^gC
 #pragma unroll

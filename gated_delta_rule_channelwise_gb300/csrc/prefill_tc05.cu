@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         const int L = min(C, p.T - t0);
         cp_async_wait_all();
         __syncthreads();
-        prep_chunk(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
+        prep_chunk<true>(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
         if (!(ok = causal_terms<false>(sm, tmem, mb, cr, sm + R_F, 64, 0))) break;
         solve_tb(sm);
         // ------------------------------------------------------------ W^T, U~^T

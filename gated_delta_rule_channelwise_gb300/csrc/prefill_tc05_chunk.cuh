@@ -176,17 +176,20 @@ struct ChunkRegs {
 // rows at t_pf into L2.  The Qg tile goes to rows 0..63 of the qg_rows-row tile
 // at qg (shared or global memory, same tile image).  Ends with the operand
 // tiles fenced for the tensor core.
+// kPrefetchQKV = false prefetches only the g rows (for callers that stage q, k, v early).
+template <bool kPrefetchQKV>
 __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L, int t_pf,
                                            char *qg, int qg_rows, ChunkRegs &cr) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ci = tid & 127, cq = tid >> 7;
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
     float *sQt = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
-    if (t_pf < p.T) {
+    if (t_pf < p.T && (kPrefetchQKV || p.gate == CGDR_GATE_CHANNEL)) {
+        // 128-byte L2 prefetches of the rows at t_pf: q, k, v (two each) and g (four)
         for (int idx = tid; idx < C * 16; idx += NT) {
             const int r = idx >> 4, part = idx & 15;
             const int64_t t = t_pf + r;
-            if (t >= p.T || part >= 10) continue;
+            if (t >= p.T || part >= 10 || (!kPrefetchQKV && part < 6)) continue;
             const void *ptr;
             if (part < 2) ptr = hd.qb + t * p.q_st + 64 * part;
             else if (part < 4) ptr = hd.kb + t * p.k_st + 64 * (part - 2);
