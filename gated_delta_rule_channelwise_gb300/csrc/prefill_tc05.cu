@@ -79,34 +79,34 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             commit(mb.mbar);
         }
         if (!(ok = mma_wait(mb))) break;
-        // -W [r][i] from D2; S^T copy [j][i] from D0, then D0 <- D0 Diag(e^gC)
+        // -W [r][i] from D2
         {
             float w16[16];
             tmem_ld16(tmem + lane_off + T_D2 + 16 * wc, w16);
 #pragma unroll
             for (int c = 0; c < 16; ++c) st_tile(sm, R_C, 64, 16 * wc + c, trow, -w16[c]);
-            float v[32];
-            const int i0 = 32 * wc;
-            tmem_ld32(tmem + lane_off + T_D0 + i0, v);
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) st_tile4(sm, R_A1, 128, trow, i0 + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] *= sDec[i0 + c];
-            tmem_st32(tmem + lane_off + T_D0 + i0, v);
         }
         fence_smem_to_async();
         fence_before_sync();
         __syncthreads();
         // ------------------------------------------------------------ U^T, O^T (state part)
         if (tid == 0) {
+            // S^T is read straight from tensor memory (taken as TF32)
             fence_after_sync();
-            gemm<64, 128>(tmem + T_D3, sbase + R_A1, sbase + R_C, true);   // U^T += S^T (-W)^T
-            gemm<64, 128>(tmem + T_D4, sbase + R_A1, sbase + R_B, false);  // O^T  = S^T Qg^T
+            gemm_ts<64, 128>(tmem + T_D3, tmem + T_D0, sbase + R_C, true);    // U^T += S^T (-W)^T
+            gemm_ts<64, 128>(tmem + T_D4, tmem + T_D0, sbase + R_B, false);   // O^T  = S^T Qg^T
             commit(mb.mbar);
         }
         if (!(ok = mma_wait(mb))) break;
         if (t0 + C < p.T) stage_rows<STG_V | STG_K>(p, hd, sbase, t0 + C);   // B and G are free
         {
+            // D0 <- D0 Diag(e^gC), now that the products above have read it
+            float sv[32];
+            const int i0 = 32 * wc;
+            tmem_ld32(tmem + lane_off + T_D0 + i0, sv);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[c] *= sDec[i0 + c];
+            tmem_st32(tmem + lane_off + T_D0 + i0, sv);
             float v[16];
             tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, v);
 #pragma unroll

@@ -37,7 +37,7 @@ constexpr float kRange = 80.f;           // max |gamma_r - gamma_mid| for the te
 constexpr uint32_t kSpin = 1u << 20;     // bounded mbarrier wait (iterations)
 
 // shared memory map of a CTA that prepares chunks (bytes from a 1024-aligned base)
-constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, V^T | S^T copy | U^T ; wide: q~, k~
+constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, V^T | U^T ; wide: q~, k~
 constexpr int R_A2 = 65536;              // 32 KB: X2 (kn e^(gm-g)), the source of Kend ; wide: gamma
 constexpr int R_B = 98304;               // 32 KB: Qg = qn e^g            [64 x 128]
 constexpr int R_C = 131072;              // 32 KB: Kg^T [128 x 64] | -W [64 x 128] | Kend^T [128 x 64]
