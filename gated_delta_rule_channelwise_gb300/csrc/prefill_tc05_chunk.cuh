@@ -248,32 +248,42 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
         sBeta[r] = be;
         sGs[r] = gs;
     }
-    __syncthreads();
-    // per-channel log-decay prefix: thread (channel ci, rows 16 cq .. +15)
-    {
+    // per-channel log-decay prefix: thread (channel ci, rows 16 cq .. +15), first within its
+    // quarter; a per-channel gate needs only the staged g rows, so that runs before the barrier
+    auto quarter_prefix = [&](bool scalar_gate) {
         float run = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int r = 16 * cq + jj;
             float gv = 0.f;
-            if (r < L) gv = p.gate == CGDR_GATE_CHANNEL ? f32p(sm, ST_G)[r * DK + ci] : sGs[r];
+            if (r < L) gv = scalar_gate ? sGs[r] : f32p(sm, ST_G)[r * DK + ci];
             run += gv;
             cr.lam[jj] = run;
         }
         sQt[cq * DK + ci] = run;
-    }
+    };
+    if (p.gate == CGDR_GATE_CHANNEL) quarter_prefix(false);
     __syncthreads();
+    if (p.gate != CGDR_GATE_CHANNEL) {
+        quarter_prefix(true);
+        __syncthreads();
+    }
     {
-        float off = 0.f;
-        for (int qq = 0; qq < cq; ++qq) off += sQt[qq * DK + ci];
+        // every thread forms its quarter's offset, the anchor (row 32) and the chunk total
+        // from the four quarter totals of its channel
+        const float q0 = sQt[ci], q1 = sQt[DK + ci], q2 = sQt[2 * DK + ci], q3 = sQt[3 * DK + ci];
+        const float q01 = q0 + q1, q012 = q01 + q2;
+        const float off = cq == 0 ? 0.f : (cq == 1 ? q0 : (cq == 2 ? q01 : q012));
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) cr.lam[jj] += off;
-        if (cq == 2) sGm[ci] = cr.lam[0];    // gamma at row 32 (the anchor)
-        if (cq == 3) sGc[ci] = cr.lam[15];   // gamma at the end of the chunk
+        const float g32 = 32 < L ? (p.gate == CGDR_GATE_CHANNEL ? f32p(sm, ST_G)[32 * DK + ci] : sGs[32]) : 0.f;
+        cr.gm = g32 + q01;                   // gamma at row 32 (the anchor)
+        cr.gcv = q3 + q012;                  // gamma at the end of the chunk
+        if (cq == 0) {
+            sGm[ci] = cr.gm;
+            sGc[ci] = cr.gcv;
+        }
     }
-    __syncthreads();
-    cr.gm = sGm[ci];
-    cr.gcv = sGc[ci];
     const float gm = cr.gm;
     // v column ci for this thread's 16 rows (staged), read before B is reused for Qg
     {
@@ -292,12 +302,20 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
         const float emv = gm > -80.f ? __expf(gm) : 0.f;
         const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_Q);
         const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_K);
-        float kg4[4];
+        float kg4[4], rk4[4], rq4[4], be4[4];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int r = 16 * cq + jj;
-            const float kt = __bfloat162float(ks[r * DK + ci]) * sRk[r];
-            const float qt = __bfloat162float(qs[r * DK + ci]) * sRq[r];
+            if ((jj & 3) == 0) {                 // per-row factors of the next four rows: one 16-byte load each
+                const float4 a = *reinterpret_cast<const float4 *>(sRk + r);
+                const float4 b2 = *reinterpret_cast<const float4 *>(sRq + r);
+                const float4 c2 = *reinterpret_cast<const float4 *>(sBeta + r);
+                rk4[0] = a.x; rk4[1] = a.y; rk4[2] = a.z; rk4[3] = a.w;
+                rq4[0] = b2.x; rq4[1] = b2.y; rq4[2] = b2.z; rq4[3] = b2.w;
+                be4[0] = c2.x; be4[1] = c2.y; be4[2] = c2.z; be4[3] = c2.w;
+            }
+            const float kt = __bfloat162float(ks[r * DK + ci]) * rk4[jj & 3];
+            const float qt = __bfloat162float(qs[r * DK + ci]) * rq4[jj & 3];
             float eg, e1 = 0.f;
             if (!wide) e1 = __expf(cr.lam[jj] - gm);
             eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
@@ -306,7 +324,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             if ((jj & 3) == 3) st_tile4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);   // Kg^T [i][s]
             if (!wide) {
                 const float e2 = __expf(gm - cr.lam[jj]);
-                st_tile(sm, R_A1, 128, r, ci, sBeta[r] * kt * e1);   // X1 rows 0..63
+                st_tile(sm, R_A1, 128, r, ci, be4[jj & 3] * kt * e1);   // X1 rows 0..63
                 st_tile(sm, R_A1, 128, 64 + r, ci, qt * e1);         // X1 rows 64..127
                 st_tile(sm, R_A2, 64, r, ci, kt * e2);               // X2
             } else {
