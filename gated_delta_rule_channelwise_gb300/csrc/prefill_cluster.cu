@@ -124,18 +124,22 @@ __device__ __forceinline__ void fence_global_to_async() { asm volatile("fence.pr
 // Bulk copy of `bytes` from this CTA's shared memory to global memory; bulk_commit closes
 // a group of them.  wait_read<N>: at most N most recent groups still reading shared memory;
 // bulk_store_wait: every group's writes complete.
+// The ring is read back within microseconds: keep its lines (evict last) against the
+// streamed inputs.
 __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 ::"l"(dst), "r"(src), "r"(bytes), "l"(l2_evict_last()) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Bulk copy of `bytes` from global memory into this CTA's shared memory, completion on `mbar`.
+// (A ring slot is read once: its lines may go first.)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar), "l"(l2_evict_first()) : "memory");
 }
 
 __device__ __forceinline__ uint32_t owner_of(int c) { return 1u + (uint32_t)(c % NPREP); }
@@ -325,8 +329,8 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
     const uint32_t sbase = smem_u32(sm);
     const int c_first = rank - 1;
     if (c_first < n) {
-        stage_rows<STG_V | STG_K>(p, hd, sbase, c_first * C);
-        stage_rows<STG_Q | STG_G>(p, hd, sbase, c_first * C);
+        stage_rows<STG_V | STG_K | STG_ONCE>(p, hd, sbase, c_first * C);
+        stage_rows<STG_Q | STG_G | STG_ONCE>(p, hd, sbase, c_first * C);
     }
     auto slot_ptr = [&](int cc) { return reinterpret_cast<char *>(hslots + slot_of(cc) * SLOT_BYTES); };
     // chunk cc's stores have completed, to bulk loads too: tell rank 0
@@ -376,8 +380,8 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         }
         __syncthreads();
         if (tn < p.T) {
-            stage_rows<STG_Q | STG_V>(p, hd, sbase, tn);
-            stage_rows<STG_K>(p, hd, sbase, tn);
+            stage_rows<STG_Q | STG_V | STG_ONCE>(p, hd, sbase, tn);
+            stage_rows<STG_K | STG_ONCE>(p, hd, sbase, tn);
         }
         {
             // Kend^T [i][s] = X2 [s][i] e^(gC - gm) (wide chunk: the Kend source as is) into R_C
@@ -398,7 +402,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576, sbase + R_C + kb * 16384, 16384);
             bulk_commit();
         }
-        if (tn < p.T) stage_rows<STG_G>(p, hd, sbase, tn);                 // A2 is free
+        if (tn < p.T) stage_rows<STG_G | STG_ONCE>(p, hd, sbase, tn);                 // A2 is free
     }
     if (k > 0) announce(c_first + NPREP * (k - 1));                      // the last own chunk
     return true;

@@ -91,6 +91,16 @@ __device__ __forceinline__ void st_tile4(char *base, int region, int R, int r, i
                                          float d) {
     *reinterpret_cast<float4 *>(base + region + sw_off(R, r, k0)) = make_float4(tf32r(a), tf32r(b), tf32r(c), tf32r(d));
 }
+// Unrounded stores: the tensor core then reads the value as TF32 by dropping the low
+// mantissa bits.  Used only for the Qg and Kg^T operands, whose truncation leaves the
+// result unchanged to the printed digits in emulation (the other operands need rounding).
+__device__ __forceinline__ void st_raw(char *base, int region, int R, int r, int k, float x) {
+    *reinterpret_cast<float *>(base + region + sw_off(R, r, k)) = x;
+}
+__device__ __forceinline__ void st_raw4(char *base, int region, int R, int r, int k0, float a, float b, float c,
+                                        float d) {
+    *reinterpret_cast<float4 *>(base + region + sw_off(R, r, k0)) = make_float4(a, b, c, d);
+}
 __device__ __forceinline__ float ld_tile(const char *base, int region, int R, int r, int k) {
     return *reinterpret_cast<const float *>(base + region + sw_off(R, r, k));
 }
@@ -114,21 +124,30 @@ __device__ __forceinline__ Head head_of(const Tc05Params &p, int b, int h) {
     return hd;
 }
 
+template <int PARTS>
+__device__ __forceinline__ void stage16(uint32_t dst, const void *src, bool valid, uint64_t pol) {
+    if (PARTS & 16) cp_async16_hint(dst, src, valid, pol);
+    else cp_async16(dst, src, valid);
+}
+
 // cp.async staging of the raw rows of the chunk starting at token tn; rows past
 // the end are zero-filled.  One commit group per call.
-enum : int { STG_Q = 1, STG_K = 2, STG_V = 4, STG_G = 8 };
+// STG_ONCE: mark the rows evict-first in L2 (each is read once; for a kernel that keeps
+// other data resident in L2 beside the streamed inputs).
+enum : int { STG_Q = 1, STG_K = 2, STG_V = 4, STG_G = 8, STG_ONCE = 16 };
 template <int PARTS>
 __device__ __forceinline__ void stage_rows(const Tc05Params &p, const Head &hd, uint32_t sbase, int tn) {
     const int tid = threadIdx.x;
     const int Ln = min(C, p.T - tn);
+    const uint64_t once = (PARTS & STG_ONCE) ? l2_evict_first() : 0;
     if (PARTS & (STG_V | STG_K | STG_Q)) {
         for (int idx = tid; idx < C * 16; idx += NT) {
             const int r = idx >> 4, c16 = idx & 15;
             const bool ok_row = r < Ln;
             const int64_t t = tn + (ok_row ? r : 0);
-            if (PARTS & STG_V) cp_async16(sbase + ST_V + r * 256 + c16 * 16, hd.vb + t * p.v_st + 8 * c16, ok_row);
-            if (PARTS & STG_K) cp_async16(sbase + ST_K + r * 256 + c16 * 16, hd.kb + t * p.k_st + 8 * c16, ok_row);
-            if (PARTS & STG_Q) cp_async16(sbase + ST_Q + r * 256 + c16 * 16, hd.qb + t * p.q_st + 8 * c16, ok_row);
+            if (PARTS & STG_V) stage16<PARTS>(sbase + ST_V + r * 256 + c16 * 16, hd.vb + t * p.v_st + 8 * c16, ok_row, once);
+            if (PARTS & STG_K) stage16<PARTS>(sbase + ST_K + r * 256 + c16 * 16, hd.kb + t * p.k_st + 8 * c16, ok_row, once);
+            if (PARTS & STG_Q) stage16<PARTS>(sbase + ST_Q + r * 256 + c16 * 16, hd.qb + t * p.q_st + 8 * c16, ok_row, once);
         }
     }
     if ((PARTS & STG_V) && p.gate == CGDR_GATE_CHANNEL && tid < C) {
@@ -141,7 +160,7 @@ __device__ __forceinline__ void stage_rows(const Tc05Params &p, const Head &hd, 
             const int r = idx >> 5, c16 = idx & 31;
             const bool ok_row = r < Ln;
             const int64_t t = tn + (ok_row ? r : 0);
-            cp_async16(sbase + ST_G + r * 512 + c16 * 16, hd.gbase + t * p.g_st + 4 * c16, ok_row);
+            stage16<PARTS>(sbase + ST_G + r * 512 + c16 * 16, hd.gbase + t * p.g_st + 4 * c16, ok_row, once);
         }
     }
     cp_async_commit();
@@ -319,9 +338,9 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             float eg, e1 = 0.f;
             if (!wide) e1 = __expf(cr.lam[jj] - gm);
             eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
-            st_tile(qg, 0, qg_rows, r, ci, qt * eg);          // Qg [r][i]
+            st_raw(qg, 0, qg_rows, r, ci, qt * eg);           // Qg [r][i] (taken as TF32 by truncation)
             kg4[jj & 3] = kt * eg;
-            if ((jj & 3) == 3) st_tile4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);   // Kg^T [i][s]
+            if ((jj & 3) == 3) st_raw4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);    // Kg^T [i][s]
             if (!wide) {
                 const float e2 = __expf(gm - cr.lam[jj]);
                 st_tile(sm, R_A1, 128, r, ci, be4[jj & 3] * kt * e1);   // X1 rows 0..63
