@@ -88,7 +88,9 @@ cgdr_status prefill_dispatch(const cgdr_args &a, void *ws, size_t ws_bytes, cuda
     if (path == CGDR_PREFILL_SIMT) return launch_prefill_simt(a, s);
     const size_t need = prefill_workspace_for(a, path);
     if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
-    return path == CGDR_PREFILL_CLUSTER ? launch_prefill_cluster(a, ws, s) : launch_prefill_tc05(a, ws, s);
+    const cgdr_status st = path == CGDR_PREFILL_CLUSTER ? launch_prefill_cluster(a, ws, s) : launch_prefill_tc05(a, ws, s);
+    // the driver's tensor-map encoder refused a tensor that the host check accepted: CUDA-core kernel
+    return st == CGDR_ERR_ALIGNMENT ? launch_prefill_simt(a, s) : st;
 }
 
 }  // namespace cgdr

@@ -323,14 +323,14 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
 // finish.  Chunk k is announced to rank 0 at the top of own chunk k + 1 (or after the
 // loop), once its stores have completed.
 __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
-                                         int n, int rank, unsigned char *hslots) {
+                                         int n, int rank, unsigned char *hslots, StageTrack &st) {
     const int tid = threadIdx.x;
     const int ci = tid & 127, cq = tid >> 7;
     const uint32_t sbase = smem_u32(sm);
     const int c_first = rank - 1;
     if (c_first < n) {
-        stage_rows<STG_V | STG_K | STG_ONCE>(p, hd, sbase, c_first * C);
-        stage_rows<STG_Q | STG_G | STG_ONCE>(p, hd, sbase, c_first * C);
+        st.stage<STG_V | STG_K | STG_ONCE>(p, hd, sbase, c_first * C);
+        st.stage<STG_Q | STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, c_first * C);
     }
     auto slot_ptr = [&](int cc) { return reinterpret_cast<char *>(hslots + slot_of(cc) * SLOT_BYTES); };
     // chunk cc's stores have completed, to bulk loads too: tell rank 0
@@ -345,7 +345,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
     for (int c = c_first; c < n; c += NPREP, ++k) {
         const int t0 = c * C, L = min(C, p.T - t0), tn = t0 + NPREP * C;
         char *slot = slot_ptr(c);
-        cp_async_wait_all();
+        if (!st.wait(sbase)) return false;
         if (k > 0) announce(c - NPREP);
         {
             // the slot's previous chunk (own chunk k - NSLOTP) has been pulled by rank 0
@@ -380,8 +380,8 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         }
         __syncthreads();
         if (tn < p.T) {
-            stage_rows<STG_Q | STG_V | STG_ONCE>(p, hd, sbase, tn);
-            stage_rows<STG_K | STG_ONCE>(p, hd, sbase, tn);
+            st.stage<STG_Q | STG_V | STG_ONCE>(p, hd, sbase, tn);
+            st.stage<STG_K | STG_ONCE>(p, hd, sbase, tn);
         }
         {
             // Kend^T [i][s] = X2 [s][i] e^(gC - gm) (wide chunk: the Kend source as is) into R_C
@@ -402,13 +402,14 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576, sbase + R_C + kb * 16384, 16384);
             bulk_commit();
         }
-        if (tn < p.T) stage_rows<STG_G | STG_ONCE>(p, hd, sbase, tn);                 // A2 is free
+        if (tn < p.T) st.stage<STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, tn);        // A2 is free
     }
     if (k > 0) announce(c_first + NPREP * (k - 1));                      // the last own chunk
     return true;
 }
 
-__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill_cluster_kernel(const Tc05Params p) {
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
+    prefill_cluster_kernel(const __grid_constant__ Tc05Params p) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sbase = smem_u32(sm);
@@ -428,6 +429,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill
             for (int i = 0; i < NSLOT; ++i) mbar_init(sbase + CH_READY + 8 * i, 1);
         } else {
             for (int i = 0; i < NSLOTP; ++i) mbar_init(sbase + M_SLOTFREE + 8 * i, 1);
+            mbar_init(sbase + M_STAGE, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -439,8 +441,9 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill
     cluster_barrier();                         // every CTA's barriers exist before any remote use
 
     int ia = 0, ib = 0;
+    StageTrack st;
     const bool ok = chain ? run_chain(p, hd, sm, tmem, mb, n, hslots, ia, ib)
-                          : run_prep(p, hd, sm, tmem, mb, n, rank, hslots);
+                          : run_prep(p, hd, sm, tmem, mb, n, rank, hslots, st);
     if (!ok && tid == 0) {
         // a wait gave up: record it, give the tensor core and the last bulk load on
         // each inbox (at most one can be outstanding) a bounded chance to finish
@@ -448,6 +451,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1) prefill
         mbar_wait(mb.mbar, mb.phase ^ 1u, kSpin);
         if (ia > 0) cl_wait(sbase + CH_FULL_A, (uint32_t)((ia - 1) & 1));
         if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1));
+        if (!chain) st.drain(sbase);
     }
     cp_async_wait_all();
     fence_before_sync();
@@ -487,7 +491,8 @@ size_t prefill_cluster_workspace(const cgdr_args &a) {
 }
 
 cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s) {
-    Tc05Params p = make_params(a, ws);
+    Tc05Params p;
+    if (!make_params(a, ws, p)) return CGDR_ERR_ALIGNMENT;
     p.slots = static_cast<unsigned char *>(ws) + WS_HEADER;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CGDR_ERR_CUDA;
     if (cudaFuncSetAttribute(prefill_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CL_SMEM_BYTES) !=

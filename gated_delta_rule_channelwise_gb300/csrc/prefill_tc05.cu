@@ -10,6 +10,8 @@
 // cluster kernel.  TF32 operands (rounded to nearest) with fp32 accumulation
 // keep the error near 1e-2 of the output RMS or below; the state is carried
 // in fp32.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "prefill_tc05_chunk.cuh"
@@ -21,7 +23,7 @@ using namespace tc05c;
 
 static_assert(PREP_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 
-__global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p) {
+__global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_constant__ Tc05Params p) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sbase = smem_u32(sm);
@@ -38,6 +40,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
     MmaBar mb{sbase + M_MBAR, 0u};
     if (tid == 0) {
         mbar_init(mb.mbar, 1);
+        mbar_init(sbase + M_STAGE, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), T_COLS);
@@ -55,9 +58,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(32 * wc + c) * DV + trow];
         tmem_st32(tmem + lane_off + T_D0 + 32 * wc, v);
     }
+    StageTrack st;
     if (p.T > 0) {
-        stage_rows<STG_V | STG_K>(p, hd, sbase, 0);
-        stage_rows<STG_Q | STG_G>(p, hd, sbase, 0);
+        st.stage<STG_V | STG_K>(p, hd, sbase, 0);
+        st.stage<STG_Q | STG_G | STG_LAST>(p, hd, sbase, 0);
     }
     fence_before_sync();
     __syncthreads();
@@ -66,8 +70,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
     ChunkRegs cr;
     for (int t0 = 0; t0 < p.T && ok; t0 += C) {
         const int L = min(C, p.T - t0);
-        cp_async_wait_all();
-        __syncthreads();
+        if (!(ok = st.wait(sbase))) break;
         prep_chunk<true>(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
         if (!(ok = causal_terms<false>(sm, tmem, mb, cr, sm + R_F, 64, 0))) break;
         solve_tb(sm);
@@ -98,7 +101,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             commit(mb.mbar);
         }
         if (!(ok = mma_wait(mb))) break;
-        if (t0 + C < p.T) stage_rows<STG_V | STG_K>(p, hd, sbase, t0 + C);   // B and G are free
+        if (t0 + C < p.T) st.stage<STG_V | STG_K>(p, hd, sbase, t0 + C);   // B and G are free
         {
             // D0 <- D0 Diag(e^gC), now that the products above have read it
             float sv[32];
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
             commit(mb.mbar);
         }
         if (!(ok = mma_wait(mb))) break;
-        if (t0 + C < p.T) stage_rows<STG_Q | STG_G>(p, hd, sbase, t0 + C);   // F and A2 are free
+        if (t0 + C < p.T) st.stage<STG_Q | STG_G | STG_LAST>(p, hd, sbase, t0 + C);   // F and A2 are free
         store_o(p, obase, tmem + T_D4, t0, L);
         fence_before_sync();
         __syncthreads();
@@ -147,8 +150,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
         if (tid == 0) {
             atomicExch(p.err, (int)CGDR_ERR_TIMEOUT);
             mbar_wait(mb.mbar, mb.phase ^ 1u, kSpin);
+            st.drain(sbase);
         }
     }
+    cp_async_wait_all();
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, T_COLS);
@@ -157,14 +162,82 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const Tc05Params p)
 }  // namespace
 
 bool prefill_tc05_supported(const cgdr_args &a) {
-    return a.dtype == CGDR_BF16 && a.dk == 128 && a.dv == 128 && chunk_of(a) == 64;
+    return a.dtype == CGDR_BF16 && a.dk == 128 && a.dv == 128 && chunk_of(a) == 64 && tc05c::maps_describable(a);
 }
 
 size_t prefill_tc05_workspace(const cgdr_args &) { return 256; }
 
 namespace tc05c {
-Tc05Params make_params(const cgdr_args &a, void *ws) {
-    Tc05Params p;
+
+namespace {
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Byte strides of a 4-D map with dims (channel, token, head, batch) and element strides
+// (st, sh, sb); false if a tensor map cannot take them (each a positive multiple of 16 bytes
+// below 2^40).
+bool map_strides(size_t esz, const cuuint64_t dims[4], int64_t st, int64_t sh, int64_t sb, cuuint64_t strides[3]) {
+    const int64_t given[3] = {st, sh, sb};
+    for (int i = 0; i < 3; ++i) {
+        // a dimension of extent 1 is never stepped: give it the dense stride whatever the caller passed
+        const cuuint64_t dense = i == 0 ? dims[0] * esz : strides[i - 1] * dims[i];
+        if (dims[i + 1] == 1) {
+            strides[i] = dense;
+        } else {
+            if (given[i] <= 0) return false;
+            strides[i] = (cuuint64_t)given[i] * esz;
+        }
+        if (strides[i] % 16 != 0 || strides[i] >= (1ull << 40)) return false;
+    }
+    return true;
+}
+
+bool encode4(CUtensorMap &m, CUtensorMapDataType type, size_t esz, const void *base, int dch, int T, int H, int B,
+             int64_t st, int64_t sh, int64_t sb) {
+    const cuuint64_t dims[4] = {(cuuint64_t)dch, (cuuint64_t)T, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3];
+    if (!map_strides(esz, dims, st, sh, sb, strides)) return false;
+    const cuuint32_t box[4] = {(cuuint32_t)dch, (cuuint32_t)C, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return g_encode(&m, type, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool describable(size_t esz, int dch, const cgdr_args &a, int H, int64_t st, int64_t sh, int64_t sb) {
+    const cuuint64_t dims[4] = {(cuuint64_t)dch, (cuuint64_t)a.T, (cuuint64_t)H, (cuuint64_t)a.B};
+    cuuint64_t strides[3];
+    return map_strides(esz, dims, st, sh, sb, strides);
+}
+}  // namespace
+
+bool maps_describable(const cgdr_args &a) {
+    if (a.T <= 0 || a.B <= 0) return true;                  // nothing to launch
+    return describable(2, a.dk, a, a.Hk, a.q_st, a.q_sh, a.q_sb) && describable(2, a.dk, a, a.Hk, a.k_st, a.k_sh, a.k_sb) &&
+           describable(2, a.dv, a, a.Hv, a.v_st, a.v_sh, a.v_sb) &&
+           (a.gate != CGDR_GATE_CHANNEL || describable(4, a.dk, a, a.Hv, a.g_st, a.g_sh, a.g_sb));
+}
+
+bool make_maps(const cgdr_args &a, Tc05Maps &tm) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr || a.T <= 0 || a.B <= 0) return false;
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    bool ok = encode4(tm.q, bf, 2, a.q, a.dk, a.T, a.Hk, a.B, a.q_st, a.q_sh, a.q_sb) &&
+              encode4(tm.k, bf, 2, a.k, a.dk, a.T, a.Hk, a.B, a.k_st, a.k_sh, a.k_sb) &&
+              encode4(tm.v, bf, 2, a.v, a.dv, a.T, a.Hv, a.B, a.v_st, a.v_sh, a.v_sb);
+    if (ok && a.gate == CGDR_GATE_CHANNEL)
+        ok = encode4(tm.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.g, a.dk, a.T, a.Hv, a.B, a.g_st, a.g_sh, a.g_sb);
+    return ok;
+}
+
+bool make_params(const cgdr_args &a, void *ws, Tc05Params &p) {
+    if (!make_maps(a, p.tm)) return false;
     p.T = a.T; p.Hk = a.Hk; p.Hv = a.Hv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate;
     p.o_f32 = a.o_dtype == CGDR_F32;
     p.q_scale = qscale_of(a); p.eps = eps_of(a);
@@ -186,12 +259,13 @@ Tc05Params make_params(const cgdr_args &a, void *ws) {
     p.o_sb = a.o_sb; p.o_st = a.o_st; p.o_sh = a.o_sh;
     p.err = static_cast<int *>(ws);
     p.slots = nullptr;
-    return p;
+    return true;
 }
 }  // namespace tc05c
 
 cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s) {
-    const tc05c::Tc05Params p = tc05c::make_params(a, ws);
+    tc05c::Tc05Params p;
+    if (!tc05c::make_params(a, ws, p)) return CGDR_ERR_ALIGNMENT;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CGDR_ERR_CUDA;
     if (cudaFuncSetAttribute(prefill_tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tc05c::PREP_SMEM_BYTES) != cudaSuccess)

@@ -24,6 +24,8 @@
 // decay).
 #pragma once
 
+#include <cuda.h>
+
 #include "cgdr_internal.cuh"
 #include "tc05.cuh"
 
@@ -48,7 +50,8 @@ constexpr int R_MISC = 196608;
 constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BETA + 256;
 constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = M_GC + 512;
 constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_SLOTFREE = M_TMEM + 8;   // 4 barriers
-constexpr int M_END = M_SLOTFREE + 32;
+constexpr int M_STAGE = M_SLOTFREE + 32;  // staging barrier: the TMA tiles of the next chunk's rows
+constexpr int M_END = M_STAGE + 8;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
 constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned)
 constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
@@ -63,7 +66,14 @@ static_assert(PREP_SMEM_BYTES <= 232448, "shared memory over the per-block limit
 // tensor memory columns
 constexpr uint32_t T_D0 = 0, T_D1 = 128, T_D2 = 192, T_D3 = 256, T_D4 = 320, T_D4B = 384, T_COLS = 512;
 
+// TMA tensor maps of the inputs: 4-D (channel, token, head, batch) with the caller's
+// strides, box = 128 channels x 64 tokens; rows past T read as zeros.
+struct Tc05Maps {
+    CUtensorMap q, k, v, g;
+};
+
 struct Tc05Params {
+    Tc05Maps tm;                         // first: 64-byte aligned
     int T, Hk, Hv, l2norm, gate, o_f32;
     float q_scale, eps;
     const __nv_bfloat16 *q, *k, *v;
@@ -80,7 +90,12 @@ struct Tc05Params {
     unsigned char *slots;                // cluster kernel: hand-off ring in the workspace (unused per head)
 };
 
-Tc05Params make_params(const cgdr_args &a, void *ws);
+bool make_params(const cgdr_args &a, void *ws, Tc05Params &p);   // false if a tensor map cannot be encoded
+// Whether every input's strides can be described by a tensor map (host arithmetic only).
+bool maps_describable(const cgdr_args &a);
+// Fills the tensor maps of `a` through the driver's encoder; false if it cannot (then the
+// tensor-core kernels do not run).
+bool make_maps(const cgdr_args &a, Tc05Maps &tm);
 
 __device__ __forceinline__ float *f32p(char *base, int off) { return reinterpret_cast<float *>(base + off); }
 __device__ __forceinline__ void st_tile(char *base, int region, int R, int r, int k, float x) {
@@ -124,46 +139,97 @@ __device__ __forceinline__ Head head_of(const Tc05Params &p, int b, int h) {
     return hd;
 }
 
-template <int PARTS>
-__device__ __forceinline__ void stage16(uint32_t dst, const void *src, bool valid, uint64_t pol) {
-    if (PARTS & 16) cp_async16_hint(dst, src, valid, pol);
-    else cp_async16(dst, src, valid);
+// TMA load of one 128 x 64 tile (channels x tokens at token tn) of a 4-D tensor map into
+// shared memory, completion counted in bytes on mbar; L2 evict-first or default.
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *tm, int tn, int head, int b, uint32_t mbar,
+                                         bool once, uint64_t pol) {
+    if (once)
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+            "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+            ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(tn), "r"(head), "r"(b), "r"(mbar), "l"(pol)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%2, %3, %4, %5}], [%6];"
+            ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(tn), "r"(head), "r"(b), "r"(mbar)
+            : "memory");
+}
+// L2 prefetch of the same tile.
+__device__ __forceinline__ void tma_prefetch(const CUtensorMap *tm, int tn, int head, int b) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(tn), "r"(head), "r"(b) : "memory");
 }
 
-// cp.async staging of the raw rows of the chunk starting at token tn; rows past
-// the end are zero-filled.  One commit group per call.
-// STG_ONCE: mark the rows evict-first in L2 (each is read once; for a kernel that keeps
+// Staging of the raw rows of the chunk starting at token tn: q, k, v (bf16 [64][128]) and g
+// (fp32 [64][128]) by TMA tiles on the staging barrier M_STAGE (thread 0: expect the bytes,
+// issue the tiles, and with STG_LAST arrive, which closes the chunk's phase); beta by
+// cp.async (one commit group per call, empty unless STG_V).  Rows past T arrive as zeros.
+// STG_ONCE marks the rows evict-first in L2 (each is read once; for a kernel that keeps
 // other data resident in L2 beside the streamed inputs).
-enum : int { STG_Q = 1, STG_K = 2, STG_V = 4, STG_G = 8, STG_ONCE = 16 };
+enum : int { STG_Q = 1, STG_K = 2, STG_V = 4, STG_G = 8, STG_ONCE = 16, STG_LAST = 32 };
 template <int PARTS>
 __device__ __forceinline__ void stage_rows(const Tc05Params &p, const Head &hd, uint32_t sbase, int tn) {
     const int tid = threadIdx.x;
-    const int Ln = min(C, p.T - tn);
-    const uint64_t once = (PARTS & STG_ONCE) ? l2_evict_first() : 0;
-    if (PARTS & (STG_V | STG_K | STG_Q)) {
-        for (int idx = tid; idx < C * 16; idx += NT) {
-            const int r = idx >> 4, c16 = idx & 15;
-            const bool ok_row = r < Ln;
-            const int64_t t = tn + (ok_row ? r : 0);
-            if (PARTS & STG_V) stage16<PARTS>(sbase + ST_V + r * 256 + c16 * 16, hd.vb + t * p.v_st + 8 * c16, ok_row, once);
-            if (PARTS & STG_K) stage16<PARTS>(sbase + ST_K + r * 256 + c16 * 16, hd.kb + t * p.k_st + 8 * c16, ok_row, once);
-            if (PARTS & STG_Q) stage16<PARTS>(sbase + ST_Q + r * 256 + c16 * 16, hd.qb + t * p.q_st + 8 * c16, ok_row, once);
-        }
+    if (tid == 0) {
+        const bool once = (PARTS & STG_ONCE) != 0;
+        const uint64_t pol = once ? l2_evict_first() : 0;
+        const bool g_on = (PARTS & STG_G) && p.gate == CGDR_GATE_CHANNEL;
+        const uint32_t bytes = ((PARTS & STG_Q) ? 16384u : 0u) + ((PARTS & STG_K) ? 16384u : 0u) +
+                               ((PARTS & STG_V) ? 16384u : 0u) + (g_on ? 32768u : 0u);
+        const uint32_t mbar = sbase + M_STAGE;
+        if (bytes) asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+        const int hk = hd.h / (p.Hv / p.Hk);
+        if (PARTS & STG_V) tma_tile(sbase + ST_V, &p.tm.v, tn, hd.h, hd.b, mbar, once, pol);
+        if (PARTS & STG_K) tma_tile(sbase + ST_K, &p.tm.k, tn, hk, hd.b, mbar, once, pol);
+        if (PARTS & STG_Q) tma_tile(sbase + ST_Q, &p.tm.q, tn, hk, hd.b, mbar, once, pol);
+        if (g_on) tma_tile(sbase + ST_G, &p.tm.g, tn, hd.h, hd.b, mbar, once, pol);
+        if (PARTS & STG_LAST) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
     }
     if ((PARTS & STG_V) && p.gate == CGDR_GATE_CHANNEL && tid < C) {
+        const int Ln = min(C, p.T - tn);
         const bool ok_row = tid < Ln;
         const int64_t t = tn + (ok_row ? tid : 0);
         cp_async4(sbase + ST_BETA + 4 * tid, p.beta + hd.b * p.beta_sb + t * p.beta_st + hd.h * p.beta_sh, ok_row);
     }
-    if ((PARTS & STG_G) && p.gate == CGDR_GATE_CHANNEL) {
-        for (int idx = tid; idx < C * 32; idx += NT) {
-            const int r = idx >> 5, c16 = idx & 31;
-            const bool ok_row = r < Ln;
-            const int64_t t = tn + (ok_row ? r : 0);
-            stage16<PARTS>(sbase + ST_G + r * 512 + c16 * 16, hd.gbase + t * p.g_st + 4 * c16, ok_row, once);
-        }
-    }
     cp_async_commit();
+}
+
+// Phases of the staging barrier: closed by an STG_LAST call, waited for, and whether one
+// has been opened by a call without STG_LAST and not yet closed.  The values are the same
+// in every thread of the CTA.
+struct StageTrack {
+    uint32_t issued = 0, waited = 0;
+    bool half = false;
+
+    template <int PARTS>
+    __device__ __forceinline__ void stage(const Tc05Params &p, const Head &hd, uint32_t sbase, int tn);
+    // Waits for the staged rows of the next chunk (the oldest closed phase and this
+    // thread's beta copies); every thread calls it.  False if the wait gave up.
+    __device__ __forceinline__ bool wait(uint32_t sbase) {
+        const bool done = mbar_wait(sbase + M_STAGE, waited & 1u, kSpin);
+        cp_async_wait_all();
+        ++waited;
+        return __syncthreads_or(!done) == 0;
+    }
+    // After a failure (thread 0): closes an open phase and gives the tiles of a phase that
+    // was not waited for a bounded chance to land before the CTA leaves.
+    __device__ __forceinline__ void drain(uint32_t sbase) {
+        if (half) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sbase + M_STAGE) : "memory");
+        if (half || issued > waited) mbar_wait(sbase + M_STAGE, waited & 1u, kSpin);
+    }
+};
+
+template <int PARTS>
+__device__ __forceinline__ void StageTrack::stage(const Tc05Params &p, const Head &hd, uint32_t sbase, int tn) {
+    stage_rows<PARTS>(p, hd, sbase, tn);
+    if (PARTS & STG_LAST) {
+        ++issued;
+        half = false;
+    } else {
+        half = true;
+    }
 }
 
 // The CTA's tensor-core completion barrier and the parity it waits for next.
@@ -203,19 +269,15 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
     const int ci = tid & 127, cq = tid >> 7;
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
     float *sQt = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
-    if (t_pf < p.T && (kPrefetchQKV || p.gate == CGDR_GATE_CHANNEL)) {
-        // 128-byte L2 prefetches of the rows at t_pf: q, k, v (two each) and g (four)
-        for (int idx = tid; idx < C * 16; idx += NT) {
-            const int r = idx >> 4, part = idx & 15;
-            const int64_t t = t_pf + r;
-            if (t >= p.T || part >= 10 || (!kPrefetchQKV && part < 6)) continue;
-            const void *ptr;
-            if (part < 2) ptr = hd.qb + t * p.q_st + 64 * part;
-            else if (part < 4) ptr = hd.kb + t * p.k_st + 64 * (part - 2);
-            else if (part < 6) ptr = hd.vb + t * p.v_st + 64 * (part - 4);
-            else ptr = p.gate == CGDR_GATE_CHANNEL ? (const void *)(hd.gbase + t * p.g_st + 32 * (part - 6)) : nullptr;
-            if (ptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+    if (t_pf < p.T && tid == 0) {
+        // L2 prefetch of the rows at t_pf, one TMA prefetch per tile
+        const int hk = hd.h / (p.Hv / p.Hk);
+        if (kPrefetchQKV) {
+            tma_prefetch(&p.tm.q, t_pf, hk, hd.b);
+            tma_prefetch(&p.tm.k, t_pf, hk, hd.b);
+            tma_prefetch(&p.tm.v, t_pf, hd.h, hd.b);
         }
+        if (p.gate == CGDR_GATE_CHANNEL) tma_prefetch(&p.tm.g, t_pf, hd.h, hd.b);
     }
     // row norms (a warp per 4 rows) from the staged raw q/k rows
     {
