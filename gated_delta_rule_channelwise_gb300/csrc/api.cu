@@ -1,6 +1,7 @@
 // C ABI entry points of libcgdr: host-side argument checks and dispatch.
 // The operation and the argument conventions are documented in cgdr.h.
 #include <atomic>
+#include <mutex>
 
 #include "cgdr_internal.cuh"
 
@@ -63,6 +64,20 @@ cgdr_status check(const cgdr_args *a, bool prefill) {
 }  // namespace
 
 namespace cgdr {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
 
 int prefill_path(const cgdr_args &a, bool allow_cluster) {
     const int choice = g_prefill_path.load();

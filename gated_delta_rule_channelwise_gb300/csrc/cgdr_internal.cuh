@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -23,6 +24,10 @@ int prefill_path(const cgdr_args &a, bool allow_cluster);
 size_t prefill_workspace_for(const cgdr_args &a, int path);
 cgdr_status prefill_dispatch(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s, bool allow_cluster);
 cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s);
+
+// The driver's tiled tensor-map encoder, looked up once through the runtime (nullptr if
+// the driver does not provide it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 inline float eps_of(const cgdr_args &a) { return a.eps < 0.f ? 1e-6f : a.eps; }
 inline float qscale_of(const cgdr_args &a) {

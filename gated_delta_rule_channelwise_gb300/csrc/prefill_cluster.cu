@@ -320,25 +320,27 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
 // Own chunk k (chunk c = rank - 1 + 3 k) goes to slot k % NSLOTP of this preparer.  Every
 // output leaves by bulk store from the shared-memory tile it was built in, as soon as the
 // tile is complete; the staging of the next own chunk's rows follows as the tiles' reads
-// finish.  Chunk k is announced to rank 0 at the top of own chunk k + 1 (or after the
-// loop), once its stores have completed.
+// finish.  Thread 0 issues the tensor-core work and the TMA staging; thread kIO (a warp with
+// no part in the triangular solve's serial steps) issues the bulk stores, waits for their
+// reads, and announces chunk k to rank 0 after the operand phase of own chunk k + 1 (or
+// after the loop), when its stores have long completed.
+constexpr int kIO = 448;
 __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
                                          int n, int rank, unsigned char *hslots, StageTrack &st) {
     const int tid = threadIdx.x;
     const int ci = tid & 127, cq = tid >> 7;
     const uint32_t sbase = smem_u32(sm);
+    volatile int *slot_ok = reinterpret_cast<volatile int *>(sm + M_FLAG);
     const int c_first = rank - 1;
     if (c_first < n) {
         st.stage<STG_V | STG_K | STG_ONCE>(p, hd, sbase, c_first * C);
         st.stage<STG_Q | STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, c_first * C);
     }
     auto slot_ptr = [&](int cc) { return reinterpret_cast<char *>(hslots + slot_of(cc) * SLOT_BYTES); };
-    // chunk cc's stores have completed, to bulk loads too: tell rank 0
+    // (thread kIO) chunk cc's stores have completed, to bulk loads too: tell rank 0
     auto announce = [&](int cc) {
-        if (tid == 0) {
-            bulk_store_wait();
-            remote_arrive(mapa_rank(sbase + CH_READY + 8 * slot_of(cc), 0));
-        }
+        bulk_store_wait();
+        remote_arrive(mapa_rank(sbase + CH_READY + 8 * slot_of(cc), 0));
     };
     ChunkRegs cr;
     int k = 0;                                                           // own chunk index
@@ -346,26 +348,26 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         const int t0 = c * C, L = min(C, p.T - t0), tn = t0 + NPREP * C;
         char *slot = slot_ptr(c);
         if (!st.wait(sbase)) return false;
-        if (k > 0) announce(c - NPREP);
-        {
-            // the slot's previous chunk (own chunk k - NSLOTP) has been pulled by rank 0
-            int okw = 1;
-            if (tid == 0 && k >= NSLOTP)
-                okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1));
-            if (__syncthreads_or(!okw)) return false;
-        }
         // operand tiles; prefetch the next own chunk's g rows into L2 (they are staged last)
         prep_chunk<false>(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
-        if (tid == 0) {
-            // Qg (64-row tile: 8 KB per K block) into rows 0..63 of [Qg; -W]; Kg^T; e^gC
+        if (tid == kIO) {
+            if (k > 0) announce(c - NPREP);
+            // the slot's previous chunk (own chunk k - NSLOTP) has been pulled by rank 0
+            int okw = 1;
+            if (k >= NSLOTP) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1));
+            if (okw) {
+                // Qg (64-row tile: 8 KB per K block) into rows 0..63 of [Qg; -W]; Kg^T; e^gC
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb) bulk_store(slot + SL_QW + kb * 16384, sbase + R_B + kb * 8192, 8192);
-            bulk_store(slot + SL_KG, sbase + R_C, 32768);
-            bulk_store(slot + SL_DEC, sbase + M_DEC, 512);
-            bulk_commit();
+                for (int kb = 0; kb < 4; ++kb) bulk_store(slot + SL_QW + kb * 16384, sbase + R_B + kb * 8192, 8192);
+                bulk_store(slot + SL_KG, sbase + R_C, 32768);
+                bulk_store(slot + SL_DEC, sbase + M_DEC, 512);
+                bulk_commit();
+            }
+            *slot_ok = okw;                                              // read after the next barrier
         }
         if (!causal_terms<true>(sm, tmem, mb, cr, sm + R_F, 64, 0)) return false;
-        if (tid == 0) {
+        if (*slot_ok == 0) return false;
+        if (tid == kIO) {
             // P (64-row tile) into rows 128..191 of [Kend^T; P]; V^T
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576 + 16384, sbase + R_F + kb * 8192, 8192);
@@ -373,7 +375,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             bulk_commit();
         }
         solve_tb(sm);
-        if (tid == 0) {
+        if (tid == kIO) {
             bulk_store(slot + SL_TB, sbase + R_G, 16384);
             bulk_commit();
             bulk_wait_read<0>();                                           // R_B, R_C, R_F, A1_VT, R_G read
@@ -396,7 +398,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         }
         fence_smem_to_async();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == kIO) {
             // Kend^T (128-row tile: 16 KB per K block) into rows 0..127 of [Kend^T; P]
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576, sbase + R_C + kb * 16384, 16384);
@@ -404,7 +406,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         }
         if (tn < p.T) st.stage<STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, tn);        // A2 is free
     }
-    if (k > 0) announce(c_first + NPREP * (k - 1));                      // the last own chunk
+    if (k > 0 && tid == kIO) announce(c_first + NPREP * (k - 1));        // the last own chunk
     return true;
 }
 
@@ -453,6 +455,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
         if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1));
         if (!chain) st.drain(sbase);
     }
+    if (!chain && tid == kIO) bulk_store_wait();   // no bulk store may still read this CTA's shared memory
     cp_async_wait_all();
     fence_before_sync();
     __syncthreads();

@@ -10,8 +10,6 @@
 // cluster kernel.  TF32 operands (rounded to nearest) with fp32 accumulation
 // keep the error near 1e-2 of the output RMS or below; the state is carried
 // in fp32.
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "prefill_tc05_chunk.cuh"
@@ -170,8 +168,6 @@ size_t prefill_tc05_workspace(const cgdr_args &) { return 256; }
 namespace tc05c {
 
 namespace {
-std::once_flag g_encode_once;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Byte strides of a 4-D map with dims (channel, token, head, batch) and element strides
 // (st, sh, sb); false if a tensor map cannot take them (each a positive multiple of 16 bytes
@@ -199,7 +195,7 @@ bool encode4(CUtensorMap &m, CUtensorMapDataType type, size_t esz, const void *b
     if (!map_strides(esz, dims, st, sh, sb, strides)) return false;
     const cuuint32_t box[4] = {(cuuint32_t)dch, (cuuint32_t)C, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return g_encode(&m, type, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return tensor_map_encoder()(&m, type, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -218,15 +214,7 @@ bool maps_describable(const cgdr_args &a) {
 }
 
 bool make_maps(const cgdr_args &a, Tc05Maps &tm) {
-    std::call_once(g_encode_once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (g_encode == nullptr || a.T <= 0 || a.B <= 0) return false;
+    if (tensor_map_encoder() == nullptr || a.T <= 0 || a.B <= 0) return false;
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     bool ok = encode4(tm.q, bf, 2, a.q, a.dk, a.T, a.Hk, a.B, a.q_st, a.q_sh, a.q_sb) &&
               encode4(tm.k, bf, 2, a.k, a.dk, a.T, a.Hk, a.B, a.k_st, a.k_sh, a.k_sb) &&

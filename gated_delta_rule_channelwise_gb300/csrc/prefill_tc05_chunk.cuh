@@ -51,7 +51,8 @@ constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BE
 constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = M_GC + 512;
 constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_SLOTFREE = M_TMEM + 8;   // 4 barriers
 constexpr int M_STAGE = M_SLOTFREE + 32;  // staging barrier: the TMA tiles of the next chunk's rows
-constexpr int M_END = M_STAGE + 8;
+constexpr int M_FLAG = M_STAGE + 8;       // int flag passed between threads across a barrier
+constexpr int M_END = M_FLAG + 8;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
 constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned)
 constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
