@@ -53,6 +53,25 @@ PREFILL_KERNELS = {1: ("prefill_tc05_kernel", ["prefill_tc05.cu", "prefill_tc05_
 DECODE_KERNEL = ("decode_kernel", ["decode.cu", "cgdr_internal.cuh"])
 
 
+def max_over_ranks(values, world, device):
+    """The element-wise max over ranks of this rank's timing totals (one all_reduce)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_rates(dec_total_ms, pre_total_ms, world, steps):
+    """Whole-job rates from the slowest rank's totals: every rank runs the same
+    workload on its own GPU (replicas, weak scaling), so the job moves `world`
+    times one rank's state bytes and tokens in the slowest rank's time."""
+    dec_gbs = world * steps * DEC_STATE_BYTES / (dec_total_ms / 1e3) / 1e9
+    pre_tps = world * steps * PRE["B"] * PRE["T"] / (pre_total_ms / 1e3)
+    return dec_gbs, pre_tps
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -213,10 +232,8 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     dec_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     pre_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
-    tot = torch.tensor([sum(dec_ms), sum(pre_ms), sum(dec_ms) + sum(pre_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-    dec_total, pre_total, step_total = (float(x) for x in tot.tolist())
+    dec_total, pre_total, step_total = max_over_ranks([sum(dec_ms), sum(pre_ms), sum(dec_ms) + sum(pre_ms)], world,
+                                                      dev)
 
     # ---- end to end: host (pinned) buffers, copies inside the timed region
     e2e = run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world)
@@ -225,8 +242,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     hbm, tflops, peak_kind = _peaks()
-    dec_gbs = world * K * DEC_STATE_BYTES / (dec_total / 1e3) / 1e9
-    pre_tps = world * K * PRE["B"] * PRE["T"] / (pre_total / 1e3)
+    dec_gbs, pre_tps = job_rates(dec_total, pre_total, world, K)
     dec_launch_s = statistics.mean(dec_ms) / 1e3
     pre_launch_s = statistics.mean(pre_ms) / 1e3
     pre_ach = PRE_BYTES / pre_launch_s / 1e9
