@@ -284,7 +284,7 @@ def run_secondary(cg, dev, stream, flush_l2):
     """The other workloads, timed once each: the fused GatedDeltaNet decode at B=1
     (256 steps, eager and as one CUDA graph) and the long prefill (B=4, T=16411)."""
     import torch
-    from gated_delta_rule_channelwise_gb300.synth import WORKLOADS, gate_kwargs, make_inputs
+    from gated_delta_rule_channelwise_gb300.synth import WORKLOADS, Workload, gate_kwargs, make_inputs
     out = {}
     w = WORKLOADS["gdn_decode_b1"]
     inp = make_inputs(w, device=dev)
@@ -362,6 +362,25 @@ def run_secondary(cg, dev, stream, flush_l2):
     out["prefill_t4000_by_kernel"] = {"ms_per_launch_cluster_kernel": time_prefill(inp, st, o, cg.PREFILL_CLUSTER),
                                       "ms_per_launch_per_head_kernel": time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)}
     del inp, st, o
+    # prefill over a range of lengths (same shapes and distributions as the T = 4000 workload), by the
+    # kernel the library picks, and small T at B = 64 by the token recurrence against the chunked kernels
+    sweep = {}
+    for B, T in ((1, 8), (1, 16), (1, 128), (1, 512), (1, 4000), (64, 2), (64, 4), (64, 8)):
+        wl = Workload("sweep", B=B, Hk=32, Hv=32, dk=128, dv=128, T=T, dtype="bf16", gate="channel",
+                      s0_std=0.0, seed=5000 + T)
+        inp = make_inputs(wl, device=dev)
+        st = torch.empty_like(inp["S0"])
+        o = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
+        key = "B%d_T%d" % (B, T)
+        pth = cg.prefill_path_for(inp["q"], inp["k"], inp["v"], st, o, chunk=64, **gate_kwargs(inp))
+        t_auto = time_prefill(inp, st, o, cg.PREFILL_AUTO)
+        sweep[key] = {"kernel": {cg.PREFILL_PER_HEAD: "per_head", cg.PREFILL_CLUSTER: "cluster",
+                                 cg.PREFILL_SIMT: "simt", cg.PREFILL_RECURRENT: "recurrent"}.get(pth, str(pth)),
+                      "ms": t_auto, "tokens_per_s": round(B * T / (t_auto / 1e3), 1)}
+        if pth == cg.PREFILL_RECURRENT:
+            sweep[key]["ms_chunked_per_head"] = time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)
+        del inp, st, o
+    out["prefill_sweep"] = sweep
     torch.cuda.empty_cache()
     return out
 

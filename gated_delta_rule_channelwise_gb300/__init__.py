@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "libcgdr.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 F32, BF16 = 0, 1
 GATE_CHANNEL, GATE_GDN = 0, 1
-PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT = range(4)
+PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT, PREFILL_RECURRENT = range(5)
 
 
 class CgdrArgs(ctypes.Structure):
@@ -247,12 +247,13 @@ def prefill_noalloc(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None
 
 
 def set_prefill_path(path: int) -> None:
-    """Process-wide prefill kernel choice: PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER or PREFILL_SIMT."""
+    """Process-wide prefill kernel choice: PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT or
+    PREFILL_RECURRENT (the token recurrence for 1 <= T <= 8)."""
     _check(lib().cgdr_set_prefill_path(int(path)), "cgdr_set_prefill_path")
 
 
 def prefill_path_for(q, k, v, state, o, **kw) -> int:
-    """The kernel (PREFILL_PER_HEAD, PREFILL_CLUSTER or PREFILL_SIMT) a prefill with these arguments
+    """The kernel (PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT or PREFILL_RECURRENT) a prefill with these arguments
     runs under the current choice; PREFILL_AUTO if the arguments are invalid or there is no work."""
     A = make_args(q, k, v, state, o, T=q.shape[1], **kw)
     return int(lib().cgdr_prefill_path_for(ctypes.byref(A)))

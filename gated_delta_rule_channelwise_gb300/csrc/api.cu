@@ -81,8 +81,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 int prefill_path(const cgdr_args &a, bool allow_cluster) {
     const int choice = g_prefill_path.load();
+    const bool few = a.T >= 1 && a.T <= kRecurrentMaxT;
+    if (few && (choice == CGDR_PREFILL_AUTO || choice == CGDR_PREFILL_RECURRENT)) return CGDR_PREFILL_RECURRENT;
     if (choice == CGDR_PREFILL_SIMT || !prefill_tc05_supported(a)) return CGDR_PREFILL_SIMT;
-    int path = choice;
+    int path = choice == CGDR_PREFILL_RECURRENT ? CGDR_PREFILL_AUTO : choice;
     if (path == CGDR_PREFILL_AUTO) {
         const int64_t units = (int64_t)a.B * a.Hv;
         const int cap = prefill_cluster_capacity();
@@ -100,6 +102,7 @@ size_t prefill_workspace_for(const cgdr_args &a, int path) {
 
 cgdr_status prefill_dispatch(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s, bool allow_cluster) {
     const int path = prefill_path(a, allow_cluster);
+    if (path == CGDR_PREFILL_RECURRENT) return launch_recurrent(a, s);
     if (path == CGDR_PREFILL_SIMT) return launch_prefill_simt(a, s);
     const size_t need = prefill_workspace_for(a, path);
     if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
@@ -141,7 +144,7 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *a) {
 }
 
 cgdr_status cgdr_set_prefill_path(int path) {
-    if (path < CGDR_PREFILL_AUTO || path > CGDR_PREFILL_SIMT) return CGDR_ERR_INVALID_ARG;
+    if (path < CGDR_PREFILL_AUTO || path > CGDR_PREFILL_RECURRENT) return CGDR_ERR_INVALID_ARG;
     g_prefill_path.store(path);
     return CGDR_OK;
 }

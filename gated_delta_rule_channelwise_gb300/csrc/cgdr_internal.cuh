@@ -12,6 +12,9 @@ namespace cgdr {
 
 // ---------------------------------------------------------------- host side
 cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s);
+// Prefill with 1 <= T <= kRecurrentMaxT: the decode kernel stepping through the tokens.
+constexpr int kRecurrentMaxT = 8;
+cgdr_status launch_recurrent(const cgdr_args &a, cudaStream_t s);
 cgdr_status launch_prefill_simt(const cgdr_args &a, cudaStream_t s);
 bool prefill_tc05_supported(const cgdr_args &a);
 size_t prefill_tc05_workspace(const cgdr_args &a);

@@ -10,6 +10,11 @@
 // from HBM once and written once:
 //   sweep 1:  vh = S^T (alpha * kn)            (decay folded into the key)
 //   sweep 2:  S  = alpha * S + kn u^T,  u = beta (v - vh);  o += S^T qn
+// The same kernel steps through up to eight tokens per call (prefill with a
+// small T: the token recurrence itself, the route "T == 1 keeps the token
+// recurrence" of "Add parallel chunked prefill for channelwise gated delta
+// rule" (Summary) extended to a few tokens): the tile stays in registers from
+// token to token and is still read once and written once.
 // Layout: a warp instruction covers RW consecutive rows of the dk x dv tile
 // with 16-byte (float4) loads, so every access is a full 128-byte line.  The
 // reduction over dk runs in registers, then across the row-lanes of a warp
@@ -21,17 +26,18 @@ namespace {
 
 struct DecodeParams {
     int Hk, Hv, l2norm, gate, o_f32;
+    int ntok;                                         // tokens per call (1 for decode, up to kRecurrentMaxT)
     float q_scale, eps;
     const void *q, *k, *v;
-    int64_t q_sb, q_sh, k_sb, k_sh, v_sb, v_sh;
+    int64_t q_sb, q_sh, q_st, k_sb, k_sh, k_st, v_sb, v_sh, v_st;
     const float *g, *beta;
-    int64_t g_sb, g_sh, beta_sb, beta_sh;
+    int64_t g_sb, g_sh, g_st, beta_sb, beta_sh, beta_st;
     const void *ga, *gb;
-    int64_t a_sb, a_sh, b_sb, b_sh;
+    int64_t a_sb, a_sh, a_st, b_sb, b_sh, b_st;
     const float *A_log, *dt_bias;
     float *state;
     void *o;
-    int64_t o_sb, o_sh;
+    int64_t o_sb, o_sh, o_st;
 };
 
 template <int DK, int DV>
@@ -78,14 +84,15 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v
 // (cp.async.bulk, completion on an mbarrier), the small per-unit rows (q, k,
 // v, g) by cp.async, so the next tiles are already in flight while the
 // current one is updated and written back with 16-byte streaming stores.
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, int NTOK>
 struct PipeShape {
-    static constexpr int NS = 3;
+    static constexpr int NS = NTOK == 1 ? 3 : 2;
     static constexpr int TILE = DK * DV * 4;
     static constexpr int ROWQ = ((DK * (int)sizeof(T) + 15) / 16) * 16;
     static constexpr int ROWV = ((DV * (int)sizeof(T) + 15) / 16) * 16;
     static constexpr int ROWG = DK * 4;
-    static constexpr int SMALL = 2 * ROWQ + ROWV + ROWG;
+    static constexpr int SMALL1 = 2 * ROWQ + ROWV + ROWG;      // one token's q, k, v, g rows
+    static constexpr int SMALL = NTOK * SMALL1;
     static constexpr int STAGE = ((TILE + SMALL + 127) / 128) * 128;
     static constexpr int BYTES = NS * STAGE + 64 + 128;   // stages, mbarriers, alignment slack
 };
@@ -107,11 +114,13 @@ __device__ __forceinline__ bool mbar_wait_parity(uint32_t mbar, uint32_t parity,
 template <int N>
 __device__ __forceinline__ void cp_async_wait_groups() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, int NTOK>
 __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(const DecodeParams p, int units) {
     using Sh = DecodeShape<DK, DV>;
-    using Ps = PipeShape<DK, DV, T>;
+    using Ps = PipeShape<DK, DV, T, NTOK>;
     constexpr int CL = Sh::CL, RW = Sh::RW, NW = Sh::NW, RPT = Sh::RPT, NT = Sh::NT, NS = Ps::NS;
+    static_assert(NTOK <= NT, "one thread per token holds its scalars");
+    const int ntok = NTOK == 1 ? 1 : p.ntok;
     constexpr uint32_t kSpin = 1u << 20;
     extern __shared__ __align__(128) char dsm_raw[];
     char *dsm = dsm_raw + ((128 - (smem_u32(dsm_raw) & 127)) & 127);
@@ -137,31 +146,40 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
             const int b = u / p.Hv, h = u % p.Hv, hk = h / (p.Hv / p.Hk);
             const uint32_t base = sb + st * Ps::STAGE;
             if (tid == 0) bulk_g2s(base, p.state + (size_t)u * DK * DV, Ps::TILE, mbar0 + 8 * st);
-            const char *qsrc = reinterpret_cast<const char *>(static_cast<const T *>(p.q) + b * p.q_sb + hk * p.q_sh);
-            const char *ksrc = reinterpret_cast<const char *>(static_cast<const T *>(p.k) + b * p.k_sb + hk * p.k_sh);
-            const char *vsrc = reinterpret_cast<const char *>(static_cast<const T *>(p.v) + b * p.v_sb + h * p.v_sh);
-            const char *gsrc = reinterpret_cast<const char *>(p.g + b * p.g_sb + h * p.g_sh);
             constexpr int nq = Ps::ROWQ / 16, nv = Ps::ROWV / 16, ng = Ps::ROWG / 16;
-            const int total = 2 * nq + nv + (p.gate == CGDR_GATE_CHANNEL ? ng : 0);
-            const uint32_t sm0 = base + Ps::TILE;
-            for (int x = tid; x < total; x += NT) {
-                if (x < nq) cp_async16(sm0 + 16 * x, qsrc + 16 * x, true);
-                else if (x < 2 * nq) cp_async16(sm0 + Ps::ROWQ + 16 * (x - nq), ksrc + 16 * (x - nq), true);
-                else if (x < 2 * nq + nv) cp_async16(sm0 + 2 * Ps::ROWQ + 16 * (x - 2 * nq), vsrc + 16 * (x - 2 * nq), true);
-                else cp_async16(sm0 + 2 * Ps::ROWQ + Ps::ROWV + 16 * (x - 2 * nq - nv), gsrc + 16 * (x - 2 * nq - nv), true);
+            const int per = 2 * nq + nv + (p.gate == CGDR_GATE_CHANNEL ? ng : 0);   // 16-byte pieces per token
+            for (int x = tid; x < ntok * per; x += NT) {
+                const int t = x / per, y = x - t * per;
+                const uint32_t sm0 = base + Ps::TILE + t * Ps::SMALL1;
+                if (y < nq) {
+                    const T *src = static_cast<const T *>(p.q) + b * p.q_sb + t * p.q_st + hk * p.q_sh;
+                    cp_async16(sm0 + 16 * y, reinterpret_cast<const char *>(src) + 16 * y, true);
+                } else if (y < 2 * nq) {
+                    const T *src = static_cast<const T *>(p.k) + b * p.k_sb + t * p.k_st + hk * p.k_sh;
+                    cp_async16(sm0 + Ps::ROWQ + 16 * (y - nq), reinterpret_cast<const char *>(src) + 16 * (y - nq), true);
+                } else if (y < 2 * nq + nv) {
+                    const T *src = static_cast<const T *>(p.v) + b * p.v_sb + t * p.v_st + h * p.v_sh;
+                    cp_async16(sm0 + 2 * Ps::ROWQ + 16 * (y - 2 * nq), reinterpret_cast<const char *>(src) + 16 * (y - 2 * nq),
+                               true);
+                } else {
+                    const float *src = p.g + b * p.g_sb + t * p.g_st + h * p.g_sh;
+                    cp_async16(sm0 + 2 * Ps::ROWQ + Ps::ROWV + 16 * (y - 2 * nq - nv),
+                               reinterpret_cast<const char *>(src) + 16 * (y - 2 * nq - nv), true);
+                }
             }
         }
         cp_async_commit();
     };
-    // Per-unit scalars (beta, or a and b of the scalar gate), kept two units ahead in registers of thread 0.
+    // Per-unit scalars (beta, or a and b of the scalar gate), kept two units ahead in registers:
+    // thread t holds those of token t.
     auto scalars = [&](int u) -> float2 {
         float2 x = make_float2(0.f, 0.f);
-        if (tid == 0 && u < units) {
-            const int b = u / p.Hv, h = u % p.Hv;
-            if (p.gate == CGDR_GATE_CHANNEL) x.x = p.beta[b * p.beta_sb + h * p.beta_sh];
+        if (tid < ntok && u < units) {
+            const int b = u / p.Hv, h = u % p.Hv, t = tid;
+            if (p.gate == CGDR_GATE_CHANNEL) x.x = p.beta[b * p.beta_sb + t * p.beta_st + h * p.beta_sh];
             else {
-                x.x = Cvt<T>::to_f(static_cast<const T *>(p.ga)[b * p.a_sb + h * p.a_sh]);
-                x.y = Cvt<T>::to_f(static_cast<const T *>(p.gb)[b * p.b_sb + h * p.b_sh]);
+                x.x = Cvt<T>::to_f(static_cast<const T *>(p.ga)[b * p.a_sb + t * p.a_st + h * p.a_sh]);
+                x.y = Cvt<T>::to_f(static_cast<const T *>(p.gb)[b * p.b_sb + t * p.b_st + h * p.b_sh]);
             }
         }
         return x;
@@ -190,10 +208,6 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
         }
         const char *stage = dsm + st * Ps::STAGE;
         const float *S = reinterpret_cast<const float *>(stage);
-        const T *sq = reinterpret_cast<const T *>(stage + Ps::TILE);
-        const T *sk = reinterpret_cast<const T *>(stage + Ps::TILE + Ps::ROWQ);
-        const T *sv = reinterpret_cast<const T *>(stage + Ps::TILE + 2 * Ps::ROWQ);
-        const float *sg = reinterpret_cast<const float *>(stage + Ps::TILE + 2 * Ps::ROWQ + Ps::ROWV);
 
         float4 s[RPT];
 #pragma unroll
@@ -201,109 +215,118 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
             const int row = (warp * RPT + ii) * RW + r;
             s[ii] = *reinterpret_cast<const float4 *>(S + row * DV + 4 * c);
         }
-        // q/k L2 norm (a warp each), decay alpha, beta
-        for (int which = warp; which < 2; which += NW) {
-            const T *x = which == 0 ? sq : sk;
-            float vals[DK / 32];
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < DK / 32; ++j) {
-                vals[j] = Cvt<T>::to_f(x[lane + 32 * j]);
-                ss += vals[j] * vals[j];
-            }
-            ss = warp_sum(ss);
-            float scale = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
-            if (which == 0) scale *= p.q_scale;
-            float *dst = which == 0 ? s_qn : s_kn;
-#pragma unroll
-            for (int j = 0; j < DK / 32; ++j) dst[lane + 32 * j] = vals[j] * scale;
-        }
-        if (p.gate == CGDR_GATE_CHANNEL) {
-            for (int i = tid; i < DK; i += NT) s_alpha[i] = expf(sg[i]);
-            if (tid == 0) s_beta = sc.x;
-        } else {
-            if (tid == 0) {
-                s_alpha[0] = expf(gdn_gate(p.A_log[h], sc.x, p.dt_bias[h]));
-                s_beta = sigmoid_f(sc.y);
-            }
-            __syncthreads();
-            const float al = s_alpha[0];
-            __syncthreads();
-            for (int i = tid; i < DK; i += NT) s_alpha[i] = al;
-        }
-        __syncthreads();
-
-        // sweep 1: vh = S^T (alpha * kn)
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int ii = 0; ii < RPT; ++ii) {
-            const int row = (warp * RPT + ii) * RW + r;
-            const float ak = s_alpha[row] * s_kn[row];
-            acc.x = fmaf(ak, s[ii].x, acc.x);
-            acc.y = fmaf(ak, s[ii].y, acc.y);
-            acc.z = fmaf(ak, s[ii].z, acc.z);
-            acc.w = fmaf(ak, s[ii].w, acc.w);
-        }
-#pragma unroll
-        for (int off = CL; off < 32; off <<= 1) {
-            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
-        }
-        if (r == 0) s_red[warp][c] = acc;
-        __syncthreads();
-        float4 vh = s_red[0][c];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) {
-            const float4 t = s_red[w][c];
-            vh.x += t.x; vh.y += t.y; vh.z += t.z; vh.w += t.w;
-        }
-        const float4 vv = load4<T>(sv + 4 * c);
-        const float beta = s_beta;
-        const float4 uu = make_float4(beta * (vv.x - vh.x), beta * (vv.y - vh.y), beta * (vv.z - vh.z),
-                                      beta * (vv.w - vh.w));
-        __syncthreads();  // s_red is reused below
-
-        // sweep 2: decay + rank-one write, o accumulated, the tile stored once
         float *Sg = p.state + (size_t)u * DK * DV;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int t = 0; t < ntok; ++t) {
+            const char *rows = stage + Ps::TILE + t * Ps::SMALL1;
+            const T *sq = reinterpret_cast<const T *>(rows);
+            const T *sk = reinterpret_cast<const T *>(rows + Ps::ROWQ);
+            const T *sv = reinterpret_cast<const T *>(rows + 2 * Ps::ROWQ);
+            const float *sg = reinterpret_cast<const float *>(rows + 2 * Ps::ROWQ + Ps::ROWV);
+            const float4 vv = load4<T>(sv + 4 * c);
+            // q/k L2 norm (a warp each), decay alpha, beta
+            for (int which = warp; which < 2; which += NW) {
+                const T *x = which == 0 ? sq : sk;
+                float vals[DK / 32];
+                float ss = 0.f;
 #pragma unroll
-        for (int ii = 0; ii < RPT; ++ii) {
-            const int row = (warp * RPT + ii) * RW + r;
-            const float al = s_alpha[row], kn = s_kn[row], qn = s_qn[row];
-            float4 x = s[ii];
-            x.x = fmaf(al, x.x, kn * uu.x);
-            x.y = fmaf(al, x.y, kn * uu.y);
-            x.z = fmaf(al, x.z, kn * uu.z);
-            x.w = fmaf(al, x.w, kn * uu.w);
-            o.x = fmaf(qn, x.x, o.x);
-            o.y = fmaf(qn, x.y, o.y);
-            o.z = fmaf(qn, x.z, o.z);
-            o.w = fmaf(qn, x.w, o.w);
-            st_stream(Sg + (size_t)row * DV + 4 * c, x);
-        }
+                for (int j = 0; j < DK / 32; ++j) {
+                    vals[j] = Cvt<T>::to_f(x[lane + 32 * j]);
+                    ss += vals[j] * vals[j];
+                }
+                ss = warp_sum(ss);
+                float scale = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
+                if (which == 0) scale *= p.q_scale;
+                float *dst = which == 0 ? s_qn : s_kn;
 #pragma unroll
-        for (int off = CL; off < 32; off <<= 1) {
-            o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
-            o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
-            o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
-            o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
-        }
-        if (r == 0) s_red[warp][c] = o;
-        __syncthreads();
-        if (warp == 0 && r == 0) {
-            float4 t = s_red[0][c];
+                for (int j = 0; j < DK / 32; ++j) dst[lane + 32 * j] = vals[j] * scale;
+            }
+            if (p.gate == CGDR_GATE_CHANNEL) {
+                for (int i = tid; i < DK; i += NT) s_alpha[i] = expf(sg[i]);
+                if (tid == t) s_beta = sc.x;
+            } else {
+                if (tid == t) {
+                    s_alpha[0] = expf(gdn_gate(p.A_log[h], sc.x, p.dt_bias[h]));
+                    s_beta = sigmoid_f(sc.y);
+                }
+                __syncthreads();
+                const float al = s_alpha[0];
+                __syncthreads();
+                for (int i = tid; i < DK; i += NT) s_alpha[i] = al;
+            }
+            __syncthreads();
+
+            // sweep 1: vh = S^T (alpha * kn)
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int ii = 0; ii < RPT; ++ii) {
+                const int row = (warp * RPT + ii) * RW + r;
+                const float ak = s_alpha[row] * s_kn[row];
+                acc.x = fmaf(ak, s[ii].x, acc.x);
+                acc.y = fmaf(ak, s[ii].y, acc.y);
+                acc.z = fmaf(ak, s[ii].z, acc.z);
+                acc.w = fmaf(ak, s[ii].w, acc.w);
+            }
+#pragma unroll
+            for (int off = CL; off < 32; off <<= 1) {
+                acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+                acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+                acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+                acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+            }
+            if (r == 0) s_red[warp][c] = acc;
+            __syncthreads();
+            float4 vh = s_red[0][c];
 #pragma unroll
             for (int w = 1; w < NW; ++w) {
-                const float4 y = s_red[w][c];
-                t.x += y.x; t.y += y.y; t.z += y.z; t.w += y.w;
+                const float4 tt = s_red[w][c];
+                vh.x += tt.x; vh.y += tt.y; vh.z += tt.z; vh.w += tt.w;
             }
-            const int64_t off = b * p.o_sb + h * p.o_sh + 4 * c;
-            if (p.o_f32) store4<float>(static_cast<float *>(p.o) + off, t);
-            else store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(p.o) + off, t);
+            const float beta = s_beta;
+            const float4 uu = make_float4(beta * (vv.x - vh.x), beta * (vv.y - vh.y), beta * (vv.z - vh.z),
+                                          beta * (vv.w - vh.w));
+            __syncthreads();  // s_red is reused below
+
+            // sweep 2: decay + rank-one write, o accumulated; the tile is stored once, after the last token
+            const bool last = t == ntok - 1;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int ii = 0; ii < RPT; ++ii) {
+                const int row = (warp * RPT + ii) * RW + r;
+                const float al = s_alpha[row], kn = s_kn[row], qn = s_qn[row];
+                float4 x = s[ii];
+                x.x = fmaf(al, x.x, kn * uu.x);
+                x.y = fmaf(al, x.y, kn * uu.y);
+                x.z = fmaf(al, x.z, kn * uu.z);
+                x.w = fmaf(al, x.w, kn * uu.w);
+                o.x = fmaf(qn, x.x, o.x);
+                o.y = fmaf(qn, x.y, o.y);
+                o.z = fmaf(qn, x.z, o.z);
+                o.w = fmaf(qn, x.w, o.w);
+                s[ii] = x;
+                if (last) st_stream(Sg + (size_t)row * DV + 4 * c, x);
+            }
+#pragma unroll
+            for (int off = CL; off < 32; off <<= 1) {
+                o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+                o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+                o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+                o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+            }
+            if (r == 0) s_red[warp][c] = o;
+            __syncthreads();
+            if (warp == 0 && r == 0) {
+                float4 tt = s_red[0][c];
+#pragma unroll
+                for (int w = 1; w < NW; ++w) {
+                    const float4 y = s_red[w][c];
+                    tt.x += y.x; tt.y += y.y; tt.z += y.z; tt.w += y.w;
+                }
+                const int64_t off = b * p.o_sb + t * p.o_st + h * p.o_sh + 4 * c;
+                if (p.o_f32) store4<float>(static_cast<float *>(p.o) + off, tt);
+                else store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(p.o) + off, tt);
+            }
+            __syncthreads();  // the token's rows, the norms and s_red are free again
         }
-        __syncthreads();  // the stage and s_red are free again
     }
 
     if (failed) {
@@ -313,8 +336,8 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
             const int u = u0 + k * G;
             if (u >= units) break;
             const int b = u / p.Hv, h = u % p.Hv;
-            for (int j = tid; j < DV; j += NT) {
-                const int64_t off = b * p.o_sb + h * p.o_sh + j;
+            for (int j = tid; j < ntok * DV; j += NT) {
+                const int64_t off = b * p.o_sb + (j / DV) * p.o_st + h * p.o_sh + j % DV;
                 if (p.o_f32) static_cast<float *>(p.o)[off] = __int_as_float(0x7fc00000);
                 else static_cast<__nv_bfloat16 *>(p.o)[off] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
             }
@@ -324,26 +347,26 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, int NTOK>
 cgdr_status launch_t(const DecodeParams &p, int units, cudaStream_t s) {
     using Sh = DecodeShape<DK, DV>;
-    using Ps = PipeShape<DK, DV, T>;
+    using Ps = PipeShape<DK, DV, T, NTOK>;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // units per CTA as even as the SM count allows
     const int per = (units + sms - 1) / sms;
     const int grid = (units + per - 1) / per;
-    if (cudaFuncSetAttribute(decode_kernel<DK, DV, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ps::BYTES) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(decode_kernel<DK, DV, T, NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ps::BYTES) != cudaSuccess)
         return CGDR_ERR_CUDA;
-    decode_kernel<DK, DV, T><<<grid, Sh::NT, Ps::BYTES, s>>>(p, units);
+    decode_kernel<DK, DV, T, NTOK><<<grid, Sh::NT, Ps::BYTES, s>>>(p, units);
     return cudaGetLastError() == cudaSuccess ? CGDR_OK : CGDR_ERR_CUDA;
 }
 
-template <typename T>
+template <typename T, int NTOK>
 cgdr_status launch_dtype(const DecodeParams &p, int dk, int dv, int units, cudaStream_t s) {
 #define CGDR_DEC_CASE(K, V) \
-    if (dk == K && dv == V) return launch_t<K, V, T>(p, units, s);
+    if (dk == K && dv == V) return launch_t<K, V, T, NTOK>(p, units, s);
     CGDR_DEC_CASE(32, 32) CGDR_DEC_CASE(32, 64) CGDR_DEC_CASE(32, 128)
     CGDR_DEC_CASE(64, 32) CGDR_DEC_CASE(64, 64) CGDR_DEC_CASE(64, 128)
     CGDR_DEC_CASE(128, 32) CGDR_DEC_CASE(128, 64) CGDR_DEC_CASE(128, 128)
@@ -351,11 +374,10 @@ cgdr_status launch_dtype(const DecodeParams &p, int dk, int dv, int units, cudaS
     return CGDR_ERR_UNSUPPORTED;
 }
 
-}  // namespace
-
-cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s) {
+DecodeParams params_of(const cgdr_args &a, int ntok) {
     DecodeParams p;
     p.Hk = a.Hk; p.Hv = a.Hv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate; p.o_f32 = a.o_dtype == CGDR_F32;
+    p.ntok = ntok;
     p.q_scale = qscale_of(a); p.eps = eps_of(a);
     p.q = a.q; p.k = a.k; p.v = a.v;
     p.q_sb = a.q_sb; p.q_sh = a.q_sh; p.k_sb = a.k_sb; p.k_sh = a.k_sh; p.v_sb = a.v_sb; p.v_sh = a.v_sh;
@@ -365,9 +387,29 @@ cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s) {
     p.a_sb = a.a_sb; p.a_sh = a.a_sh; p.b_sb = a.b_sb; p.b_sh = a.b_sh;
     p.A_log = a.A_log; p.dt_bias = a.dt_bias;
     p.state = a.state; p.o = a.o; p.o_sb = a.o_sb; p.o_sh = a.o_sh;
+    // token strides: a single token never steps them (decode ignores them)
+    const bool one = ntok == 1;
+    p.q_st = one ? 0 : a.q_st; p.k_st = one ? 0 : a.k_st; p.v_st = one ? 0 : a.v_st; p.g_st = one ? 0 : a.g_st;
+    p.beta_st = one ? 0 : a.beta_st; p.a_st = one ? 0 : a.a_st; p.b_st = one ? 0 : a.b_st;
+    p.o_st = one ? 0 : a.o_st;
+    return p;
+}
+
+}  // namespace
+
+cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s) {
+    const DecodeParams p = params_of(a, 1);
     const int units = a.B * a.Hv;
-    if (a.dtype == CGDR_BF16) return launch_dtype<__nv_bfloat16>(p, a.dk, a.dv, units, s);
-    return launch_dtype<float>(p, a.dk, a.dv, units, s);
+    if (a.dtype == CGDR_BF16) return launch_dtype<__nv_bfloat16, 1>(p, a.dk, a.dv, units, s);
+    return launch_dtype<float, 1>(p, a.dk, a.dv, units, s);
+}
+
+cgdr_status launch_recurrent(const cgdr_args &a, cudaStream_t s) {
+    if (a.T < 1 || a.T > kRecurrentMaxT) return CGDR_ERR_UNSUPPORTED;
+    const DecodeParams p = params_of(a, a.T);
+    const int units = a.B * a.Hv;
+    if (a.dtype == CGDR_BF16) return launch_dtype<__nv_bfloat16, kRecurrentMaxT>(p, a.dk, a.dv, units, s);
+    return launch_dtype<float, kRecurrentMaxT>(p, a.dk, a.dv, units, s);
 }
 
 }  // namespace cgdr

@@ -141,10 +141,12 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
  * state carry, with a ragged last chunk handled by the same code.
  * T == 0 is a no-op.  The result equals T applications of the token
  * recurrence up to rounding, for every chunk length.
- * Paths: bf16 inputs with dk = dv = 128 and chunk 64 run one of the two
- * tensor-core kernels (tcgen05, TF32 operands, fp32 accumulation and state),
- * chosen as cgdr_set_prefill_path describes; every other case runs an fp32
- * CUDA-core kernel.
+ * Paths: 1 <= T <= 8 runs the token recurrence itself (the decode kernel
+ * stepping through the tokens, each state tile read once and written once;
+ * the chunk length plays no part); otherwise bf16 inputs with dk = dv = 128
+ * and chunk 64 run one of the two tensor-core kernels (tcgen05, TF32
+ * operands, fp32 accumulation and state), and every other case an fp32
+ * CUDA-core kernel; cgdr_set_prefill_path can force a kernel.
  * Workspace: the tensor-core path needs cgdr_prefill_workspace_size() bytes
  * (16-byte aligned); its first int32 is set to CGDR_ERR_TIMEOUT if a bounded
  * device wait gave up (see cgdr_workspace_status).  `workspace` may be NULL
@@ -161,12 +163,15 @@ cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspac
  * (Summary); running them on different SMs has no counterpart there.
  */
 typedef enum cgdr_prefill_path {
-    CGDR_PREFILL_AUTO = 0,      /* per call: CLUSTER when every (batch, v-head) cluster is
-                                   resident on the GPU at once, else PER_HEAD */
+    CGDR_PREFILL_AUTO = 0,      /* per call: RECURRENT when 1 <= T <= 8; else CLUSTER when every
+                                   (batch, v-head) cluster is resident on the GPU at once, else
+                                   PER_HEAD (SIMT for shapes the tensor-core kernels do not cover) */
     CGDR_PREFILL_PER_HEAD = 1,  /* tensor cores, one CTA per (batch, v-head) */
     CGDR_PREFILL_CLUSTER = 2,   /* tensor cores, a cluster of four CTAs per (batch, v-head):
                                    one carries the state, three prepare chunks for it */
-    CGDR_PREFILL_SIMT = 3       /* fp32 CUDA cores */
+    CGDR_PREFILL_SIMT = 3,      /* fp32 CUDA cores, chunked */
+    CGDR_PREFILL_RECURRENT = 4  /* 1 <= T <= 8: the token recurrence, fp32 CUDA cores, no
+                                   workspace; for a longer T it means AUTO */
 } cgdr_prefill_path;
 
 /*
@@ -179,8 +184,8 @@ cgdr_status cgdr_set_prefill_path(int path);
 
 /*
  * The kernel cgdr_prefill would run for `args` on the current device under
- * the current choice: CGDR_PREFILL_PER_HEAD, CGDR_PREFILL_CLUSTER or
- * CGDR_PREFILL_SIMT; CGDR_PREFILL_AUTO (0) if `args` is invalid or there is
+ * the current choice: CGDR_PREFILL_PER_HEAD, CGDR_PREFILL_CLUSTER,
+ * CGDR_PREFILL_SIMT or CGDR_PREFILL_RECURRENT; CGDR_PREFILL_AUTO (0) if `args` is invalid or there is
  * nothing to do (B == 0 or T == 0).  Queries the device once per device for
  * the cluster capacity.
  */

@@ -157,7 +157,7 @@ def test_prefill_path_choice(lib):
     covers (bf16, dk = dv = 128, chunk 64); unknown choices are rejected and change nothing."""
     A = _args(T=100)
     try:
-        assert lib.cgdr_set_prefill_path(4) == cg.ERR_INVALID_ARG
+        assert lib.cgdr_set_prefill_path(5) == cg.ERR_INVALID_ARG
         assert lib.cgdr_set_prefill_path(-1) == cg.ERR_INVALID_ARG
         for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
             assert lib.cgdr_set_prefill_path(path) == cg.OK
@@ -167,6 +167,19 @@ def test_prefill_path_choice(lib):
             for other in (_args(T=100, chunk=32), _args(T=100, dv=64),
                           _args(T=100, dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128)):
                 assert lib.cgdr_prefill_path_for(ctypes.byref(other)) == cg.PREFILL_SIMT
+        # 1 <= T <= 8: the token recurrence under the automatic choice (or when forced); a forced
+        # chunked kernel still runs chunked; RECURRENT forced on a longer T means the automatic choice
+        assert lib.cgdr_set_prefill_path(cg.PREFILL_AUTO) == cg.OK
+        for T in (1, 2, 8):
+            for kw in ({}, dict(dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128), dict(dk=32, dv=64)):
+                assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=T, **kw))) == cg.PREFILL_RECURRENT
+            assert lib.cgdr_prefill_workspace_size(ctypes.byref(_args(T=T))) == 0
+        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=9))) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
+        assert lib.cgdr_set_prefill_path(cg.PREFILL_PER_HEAD) == cg.OK
+        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=2))) == cg.PREFILL_PER_HEAD
+        assert lib.cgdr_set_prefill_path(cg.PREFILL_RECURRENT) == cg.OK
+        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=3))) == cg.PREFILL_RECURRENT
+        assert lib.cgdr_prefill_path_for(ctypes.byref(A)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
         assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=0))) == cg.PREFILL_AUTO
         assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, dk=96))) == cg.PREFILL_AUTO
         assert lib.cgdr_prefill_path_for(None) == cg.PREFILL_AUTO

@@ -34,6 +34,14 @@ def tc_path(request):
     cg.set_prefill_path(cg.PREFILL_AUTO)
 
 
+@pytest.fixture
+def simt_path():
+    """Forces the chunked CUDA-core kernel (a small T would otherwise run the token recurrence)."""
+    cg.set_prefill_path(cg.PREFILL_SIMT)
+    yield cg.PREFILL_SIMT
+    cg.set_prefill_path(cg.PREFILL_AUTO)
+
+
 def _expect_path(inp, path):
     o = torch.empty(inp["v"].shape, device=inp["v"].device)
     assert cg.prefill_path_for(inp["q"], inp["k"], inp["v"], inp["S0"], o, chunk=64, **gate_kwargs(inp)) == path
@@ -70,9 +78,10 @@ def test_tiny_f32_chunk16():
 @pytest.mark.parametrize("chunk", [16, 32, 64])
 @pytest.mark.parametrize("T", [1, 2, 17, 64, 100])
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 32), (128, 64)])
-def test_fp32_chunk_sizes_and_tails(chunk, T, dk, dv):
+def test_fp32_chunk_sizes_and_tails(chunk, T, dk, dv, simt_path):
     w = Workload("f32", B=2, Hk=1, Hv=2, dk=dk, dv=dv, T=T, dtype="f32", gate="channel", seed=T + chunk)
     inp = make_inputs(w, device="cuda")
+    _expect_path(inp, cg.PREFILL_SIMT)
     o, s = _prefill(inp, chunk)
     _check(w, inp, o, s)
 
@@ -235,3 +244,39 @@ def test_both_tensor_core_kernels_agree():
     eo, es = rel_err(o2, o1.double().cpu().numpy()), rel_err(s2, s1.double().cpu().numpy())
     print("[kernels] o %.3e S %.3e" % (eo, es))
     assert eo <= 5e-3 and es <= 5e-3
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("dtype,gate,dk,dv", [("bf16", "channel", 128, 128), ("bf16", "gdn", 128, 128),
+                                              ("f32", "channel", 32, 64), ("f32", "gdn", 64, 32)])
+def test_recurrent_small_T(T, dtype, gate, dk, dv):
+    """1 <= T <= 8 runs the token recurrence (the decode kernel stepping through the tokens with
+    the state tile held on chip): parity with the oracle, and the result of T
+    single-token decode calls (up to the compiler's choice of fused multiply-adds)."""
+    w = Workload("rec", B=3, Hk=2, Hv=4, dk=dk, dv=dv, T=T, dtype=dtype, gate=gate, seed=40 + T)
+    inp = make_inputs(w, device="cuda")
+    _expect_path(inp, cg.PREFILL_RECURRENT)
+    o, s = _prefill(inp, 64)
+    _check(w, inp, o, s, tol=TOL[torch.float32])
+    s_d = inp["S0"].clone()
+    o_d = decode_steps(cg, inp, T, s_d)
+    torch.cuda.synchronize()
+    # the same per-token arithmetic in both launches (the compiler may contract it differently)
+    assert rel_err(s, s_d.double().cpu().numpy()) <= 1e-5
+    assert rel_err(o, o_d.double().cpu().numpy()) <= 1e-5
+
+
+def test_recurrent_matches_chunked_kernels():
+    """T = 8 by the token recurrence and by each chunked kernel: the same result up to rounding."""
+    w = Workload("rec8", B=2, Hk=2, Hv=2, dk=128, dv=128, T=8, dtype="bf16", gate="channel", seed=77)
+    inp = make_inputs(w, device="cuda")
+    o_r, s_r = _prefill(inp, 64)
+    try:
+        for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
+            cg.set_prefill_path(path)
+            _expect_path(inp, path)
+            o_c, s_c = _prefill(inp, 64)
+            assert rel_err(o_c, o_r.double().cpu().numpy()) <= 2e-2
+            assert rel_err(s_c, s_r.double().cpu().numpy()) <= 2e-2
+    finally:
+        cg.set_prefill_path(cg.PREFILL_AUTO)
