@@ -58,7 +58,7 @@ constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned
 constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
 constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_VT = R_A1 + 32768;
 static_assert(A1_Z + 6 * 16 * LDZ * 4 <= A1_VT, "A1 overflow");
-// Staged raw inputs of a chunk (cp.async, issued while an earlier chunk is finishing):
+// Staged raw inputs of a chunk (TMA tiles; beta by cp.async), loaded while an earlier chunk finishes:
 // q rows -> F, k rows -> G (bf16 [64][128]); g rows -> A2 (fp32 [64][128]);
 // v rows -> B (bf16 [64][128]); beta -> B + 16 KB (fp32 [64]).
 constexpr int ST_Q = R_F, ST_K = R_G, ST_G = R_A2, ST_V = R_B, ST_BETA = R_B + 16384;
