@@ -280,3 +280,24 @@ def test_recurrent_matches_chunked_kernels():
             assert rel_err(s_c, s_r.double().cpu().numpy()) <= 2e-2
     finally:
         cg.set_prefill_path(cg.PREFILL_AUTO)
+
+
+@pytest.mark.parametrize("T", [5, 200])
+def test_packed_gdn_prefill(T, tc_path):
+    """The fused GatedDeltaNet layout in prefill: q | k | v views into one packed bf16 row per
+    token (16 k-heads repeated to 32 v-heads), scalar gate; the tensor maps take the row's
+    strides.  T = 5 is one ragged chunk, T = 200 four chunks."""
+    w = Workload("pk", B=2, Hk=16, Hv=32, dk=128, dv=128, T=T, dtype="bf16", gate="gdn", packed=True, seed=90 + T)
+    inp = make_inputs(w, device="cuda")
+    assert inp["q"].stride(1) == 16 * 128 * 2 + 32 * 128          # a view into the packed row
+    o, s = _prefill(inp, 64)
+    _check(w, inp, o, s, units=[(0, 0), (0, 1), (1, 17), (1, 31)])
+
+
+def test_packed_gdn_prefill_recurrent():
+    """The same packed layout with T = 5 under the automatic choice: the token recurrence."""
+    w = Workload("pkr", B=2, Hk=16, Hv=32, dk=128, dv=128, T=5, dtype="bf16", gate="gdn", packed=True, seed=97)
+    inp = make_inputs(w, device="cuda")
+    _expect_path(inp, cg.PREFILL_RECURRENT)
+    o, s = _prefill(inp, 64)
+    _check(w, inp, o, s, units=[(0, 0), (0, 1), (1, 17), (1, 31)], tol=TOL[torch.float32])
