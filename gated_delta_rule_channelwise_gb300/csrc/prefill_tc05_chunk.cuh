@@ -280,38 +280,29 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
         }
         if (p.gate == CGDR_GATE_CHANNEL) tma_prefetch(&p.tm.g, t_pf, hd.h, hd.b);
     }
-    // row norms (a warp per 4 rows) from the staged raw q/k rows
+    // row norms from the staged raw q/k rows: four threads per row (q rows on warps 0-7, k rows
+    // on warps 8-15), each summing 32 channels from four 16-byte pieces taken in a row-rotated
+    // order (so a warp's loads spread over all banks), then two shuffle steps
     {
-        uint2 qr[4], kr[4];
+        const int rn = tid >> 2, part = tid & 3, row = rn & 63;
+        const char *src = sm + (rn < 64 ? ST_Q : ST_K) + row * 256 + part * 64;
+        float ss = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int r = 4 * warp + jj;
-            qr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_Q + r * 256 + 8 * lane);
-            kr[jj] = *reinterpret_cast<const uint2 *>(sm + ST_K + r * 256 + 8 * lane);
+        for (int i = 0; i < 4; ++i) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(src + 16 * ((i + rn) & 3));
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[e]));
+                ss = fmaf(f.x, f.x, ss);
+                ss = fmaf(f.y, f.y, ss);
+            }
         }
-        float ss[8];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].x));
-            const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qr[jj].y));
-            const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].x));
-            const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr[jj].y));
-            ss[2 * jj] = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
-            ss[2 * jj + 1] = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss[e] += __shfl_xor_sync(0xffffffffu, ss[e], o);
-        }
-        if (lane < 4) {
-            const int r = 4 * warp + lane;
-            float sq = ss[0], sk = ss[1];
-#pragma unroll
-            for (int jj = 1; jj < 4; ++jj)
-                if (lane == jj) { sq = ss[2 * jj]; sk = ss[2 * jj + 1]; }
-            sRq[r] = (p.l2norm ? rsqrtf(sq + p.eps) : 1.f) * p.q_scale;
-            sRk[r] = p.l2norm ? rsqrtf(sk + p.eps) : 1.f;
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (part == 0) {
+            if (rn < 64) sRq[row] = (p.l2norm ? rsqrtf(ss + p.eps) : 1.f) * p.q_scale;
+            else sRk[row] = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
         }
     }
     if (tid < C) {
