@@ -53,6 +53,17 @@ PREFILL_KERNELS = {1: ("prefill_tc05_kernel", ["prefill_tc05.cu", "prefill_tc05_
 DECODE_KERNEL = ("decode_kernel", ["decode.cu", "cgdr_internal.cuh"])
 
 
+def bench_config(world):
+    """The workload both arms report (the reference arm times bounded samples of it)."""
+    return {"workload": "decode_b64 + prefill_t4000",
+            "decode": {"B": 64, "H": 32, "dk": 128, "dv": 128, "state": "fp32", "inputs": "bf16",
+                       "gate": "per-channel fp32"},
+            "prefill": {"B": 1, "H": 32, "T": 4000, "dk": 128, "dv": 128, "chunk": 64, "inputs": "bf16",
+                        "o": "fp32"},
+            "l2": "flushed before every kernel (256 MiB written, then read back), outside the timed brackets",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def max_over_ranks(values, world, device):
     """The element-wise max over ranks of this rank's timing totals (one all_reduce)."""
     import torch
@@ -253,13 +264,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(dec_gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_total / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "decode_b64 + prefill_t4000",
-                   "decode": {"B": 64, "H": 32, "dk": 128, "dv": 128, "state": "fp32", "inputs": "bf16",
-                              "gate": "per-channel fp32"},
-                   "prefill": {"B": 1, "H": 32, "T": 4000, "dk": 128, "dv": 128, "chunk": 64, "inputs": "bf16",
-                               "o": "fp32"},
-                   "l2": "flushed before every kernel (256 MiB written, then read back), outside the timed brackets",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": bench_config(world),
         "pct_hbm_peak": round(100.0 * dec_gbs / world / hbm, 2),
         "prefill": {"metric": "prefill tokens/s at T=4000, 32 heads", "value": round(pre_tps, 1),
                     "unit": "tokens/s", "ms_per_launch": round(pre_launch_s * 1e3, 5), "kernel": pre_kernel[0]},
@@ -563,7 +568,7 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round((dsum + psum) / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode_b64 + prefill_t4000 (bounded samples)"},
+            "config": bench_config(1),
             "prefill": {"value": round(tps, 2), "unit": "tokens/s"},
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
