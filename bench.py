@@ -367,10 +367,11 @@ def run_secondary(cg, dev, stream, flush_l2):
     out["prefill_t4000_by_kernel"] = {"ms_per_launch_cluster_kernel": time_prefill(inp, st, o, cg.PREFILL_CLUSTER),
                                       "ms_per_launch_per_head_kernel": time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)}
     del inp, st, o
-    # prefill over a range of lengths (same shapes and distributions as the T = 4000 workload), by the
-    # kernel the library picks, and small T at B = 64 by the token recurrence against the chunked kernels
+    # prefill over a range of lengths and batches (same shapes and distributions as the T = 4000
+    # workload), by the kernel the library picks; small T at B = 64 also by the chunked kernel, and
+    # B = 2, 3 (64 and 96 heads: two and three waves of clusters) by both tensor-core kernels
     sweep = {}
-    for B, T in ((1, 8), (1, 16), (1, 128), (1, 512), (1, 4000), (64, 2), (64, 4), (64, 8)):
+    for B, T in ((1, 8), (1, 16), (1, 128), (1, 512), (1, 4000), (2, 4000), (3, 4000), (64, 2), (64, 4), (64, 8)):
         wl = Workload("sweep", B=B, Hk=32, Hv=32, dk=128, dv=128, T=T, dtype="bf16", gate="channel",
                       s0_std=0.0, seed=5000 + T)
         inp = make_inputs(wl, device=dev)
@@ -384,6 +385,9 @@ def run_secondary(cg, dev, stream, flush_l2):
                       "ms": t_auto, "tokens_per_s": round(B * T / (t_auto / 1e3), 1)}
         if pth == cg.PREFILL_RECURRENT:
             sweep[key]["ms_chunked_per_head"] = time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)
+        elif B > 1:
+            sweep[key]["ms_per_head"] = time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)
+            sweep[key]["ms_cluster"] = time_prefill(inp, st, o, cg.PREFILL_CLUSTER)
         del inp, st, o
     out["prefill_sweep"] = sweep
     torch.cuda.empty_cache()

@@ -86,9 +86,20 @@ int prefill_path(const cgdr_args &a, bool allow_cluster) {
     if (choice == CGDR_PREFILL_SIMT || !prefill_tc05_supported(a)) return CGDR_PREFILL_SIMT;
     int path = choice == CGDR_PREFILL_RECURRENT ? CGDR_PREFILL_AUTO : choice;
     if (path == CGDR_PREFILL_AUTO) {
+        // Whichever finishes first in waves of resident work: a four-CTA cluster carries a head
+        // about 3.3 times faster per chunk than one CTA (7.2 K against 24 K cycles measured on
+        // GB300), but four times fewer clusters than CTAs are resident at once.
         const int64_t units = (int64_t)a.B * a.Hv;
         const int cap = prefill_cluster_capacity();
-        path = (cap > 0 && units <= cap) ? CGDR_PREFILL_CLUSTER : CGDR_PREFILL_PER_HEAD;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                         cudaSuccess)
+            sms = 0;
+        path = CGDR_PREFILL_PER_HEAD;
+        if (cap > 0 && sms > 0) {
+            const int64_t waves_cluster = (units + cap - 1) / cap, waves_head = (units + sms - 1) / sms;
+            if (10 * waves_cluster <= 33 * waves_head) path = CGDR_PREFILL_CLUSTER;
+        }
     }
     if (path == CGDR_PREFILL_CLUSTER && !allow_cluster) path = CGDR_PREFILL_PER_HEAD;
     return path;

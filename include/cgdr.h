@@ -163,9 +163,10 @@ cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspac
  * (Summary); running them on different SMs has no counterpart there.
  */
 typedef enum cgdr_prefill_path {
-    CGDR_PREFILL_AUTO = 0,      /* per call: RECURRENT when 1 <= T <= 8; else CLUSTER when every
-                                   (batch, v-head) cluster is resident on the GPU at once, else
-                                   PER_HEAD (SIMT for shapes the tensor-core kernels do not cover) */
+    CGDR_PREFILL_AUTO = 0,      /* per call: RECURRENT when 1 <= T <= 8; else CLUSTER or PER_HEAD,
+                                   whichever needs less time in waves of resident work (a cluster
+                                   carries a head ~3.3x faster per chunk, but 4x fewer are
+                                   resident); SIMT for shapes the tensor-core kernels do not cover */
     CGDR_PREFILL_PER_HEAD = 1,  /* tensor cores, one CTA per (batch, v-head) */
     CGDR_PREFILL_CLUSTER = 2,   /* tensor cores, a cluster of four CTAs per (batch, v-head):
                                    one carries the state, three prepare chunks for it */
