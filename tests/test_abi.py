@@ -196,3 +196,24 @@ def test_prefill_path_choice(lib):
     finally:
         lib.cgdr_set_prefill_path(cg.PREFILL_AUTO)
     assert lib.cgdr_prefill_path_for(ctypes.byref(A)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
+
+
+def test_tensor_maps_cover_strides_or_fall_back(lib):
+    """The tensor-core prefill stages rows with TMA tensor maps; strides a map cannot take
+    (a zero or negative stride over an extent above one, or one of 2^40 bytes or more) send
+    the call to the CUDA-core kernel, and a dimension of extent one may carry any stride."""
+    A = _args(T=100)
+    try:
+        assert lib.cgdr_set_prefill_path(cg.PREFILL_PER_HEAD) == cg.OK
+        assert lib.cgdr_prefill_path_for(ctypes.byref(A)) == cg.PREFILL_PER_HEAD
+        # q heads sharing one row (head stride 0) with Hk = 2: valid input, no tensor map
+        assert cg.validate(_args(T=100, q_sh=0), True) == cg.OK
+        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, q_sh=0))) == cg.PREFILL_SIMT
+        # a batch stride of 2^40 bytes and more (bf16: 2^39 elements)
+        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, k_sb=1 << 39))) == cg.PREFILL_SIMT
+        # extent-one dimensions: their strides never step, so any value is fine
+        one = dict(T=100, B=1, Hk=1, Hv=1)
+        for kw in (dict(q_sh=0, k_sh=0, v_sh=0, g_sh=0), dict(q_sb=0, k_sb=0, v_sb=0, g_sb=0)):
+            assert lib.cgdr_prefill_path_for(ctypes.byref(_args(**one, **kw))) == cg.PREFILL_PER_HEAD
+    finally:
+        lib.cgdr_set_prefill_path(cg.PREFILL_AUTO)
