@@ -12,9 +12,13 @@ back during its run; kernels are timed with CUDA events on the stream they
 run on.
 
 Headline value: decode state GB/s = 2*B*H*dk*dv*4 bytes per step / decode
-time.  The prefill rate (tokens/s) is reported beside it.  `roofline` is for
-the kernel with the larger share of the step (the prefill kernel); the
-decode kernel's roofline is under `decode_roofline`.
+time, sustained: back-to-back decode steps rotating over three distinct
+134 MB states (402 MB, larger than L2), so that no step finds its state in L2
+and the write-back of one step's dirty lines is paid inside the next step.
+The per-launch time after an L2 flush (median) is reported beside it.  The
+prefill rate (tokens/s, o in bf16 as a bf16 model runs it) is reported beside
+it too.  `roofline` is for the kernel with the larger share of the step (the
+prefill kernel); the decode kernel's roofline is under `decode_roofline`.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -41,9 +45,14 @@ METRIC = "decode state GB/s (% HBM peak) at B=64; prefill tokens/s at T=4000, 32
 DEC = dict(B=64, H=32, dk=128, dv=128)
 PRE = dict(B=1, H=32, T=4000, dk=128, dv=128, chunk=64)
 DEC_STATE_BYTES = 2 * DEC["B"] * DEC["H"] * DEC["dk"] * DEC["dv"] * 4           # 268,435,456
-# prefill algorithmic bytes: q,k,v bf16 + g fp32 + beta fp32 + o fp32 + state in and out fp32
-PRE_BYTES = (PRE["B"] * PRE["T"] * PRE["H"] * (3 * 128 * 2 + 128 * 4 + 4 + 128 * 4)
-             + 2 * PRE["B"] * PRE["H"] * 128 * 128 * 4)                           # 234,082,304
+# prefill algorithmic bytes: q,k,v bf16 + g fp32 + beta fp32 + o + state in and out fp32;
+# o in bf16 (the timed configuration) or fp32 (reported beside it)
+def prefill_bytes(B, T, H, o_bytes):
+    return B * T * H * (3 * 128 * 2 + 128 * 4 + 4 + 128 * o_bytes) + 2 * B * H * 128 * 128 * 4
+
+
+PRE_BYTES = prefill_bytes(PRE["B"], PRE["T"], PRE["H"], 2)                        # 201,314,304
+PRE_BYTES_F32O = prefill_bytes(PRE["B"], PRE["T"], PRE["H"], 4)                   # 234,082,304
 # prefill tensor flops per token-head: 10*C*d (intra-chunk) + 6*dk*dv (carry)
 PRE_FLOPS = PRE["B"] * PRE["T"] * PRE["H"] * (10 * PRE["chunk"] * 128 + 6 * 128 * 128)
 L2_FLUSH_BYTES = 256 << 20
@@ -59,8 +68,10 @@ def bench_config(world):
             "decode": {"B": 64, "H": 32, "dk": 128, "dv": 128, "state": "fp32", "inputs": "bf16",
                        "gate": "per-channel fp32"},
             "prefill": {"B": 1, "H": 32, "T": 4000, "dk": 128, "dv": 128, "chunk": 64, "inputs": "bf16",
-                        "o": "fp32"},
-            "l2": "flushed before every kernel (256 MiB written, then read back), outside the timed brackets",
+                        "o": "bf16"},
+            "l2": "decode (headline): inputs larger than L2 (three 134 MB states in rotation, back to back); "
+                  "per-launch decode and prefill: L2 flushed before every kernel (256 MiB written, then read "
+                  "back), outside the timed brackets",
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
@@ -195,10 +206,14 @@ def run_ours(args, rank, world, local_rank):
     dsteps = 16                                   # distinct decode inputs, cycled
     dinp = make_inputs(wd, T=dsteps, device=dev, seed=wd.seed + 97 * rank)
     dstate = dinp["S0"].clone()
+    dstates = [dstate, dinp["S0"].clone(), dinp["S0"].clone()]    # 3 x 134 MB, rotated back to back
     dout = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.float32, device=dev)
     pinp = make_inputs(wp, device=dev, seed=wp.seed + 97 * rank)
     pstate = torch.zeros_like(pinp["S0"])
-    pout = torch.empty(pinp["v"].shape, dtype=torch.float32, device=dev)
+    pout = torch.empty(pinp["v"].shape, dtype=torch.bfloat16, device=dev)
+    pkw = dict(g=pinp["g"], beta=pinp["beta"], chunk=64)
+    pws = torch.empty(max(1, cg.prefill_workspace_size(pinp["q"], pinp["k"], pinp["v"], pstate, pout, **pkw)),
+                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     sink = torch.empty((), dtype=torch.float32, device=dev)
 
@@ -206,28 +221,31 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()                         # write > L2 ...
         torch.sum(flush, dim=0, out=sink)     # ... then read it back: L2 holds clean flush lines only
 
-    def decode(i):
+    def decode(i, state=dstate):
         t = i % dsteps
-        cg.decode(dinp["q"][:, t], dinp["k"][:, t], dinp["v"][:, t], dstate, dout,
+        cg.decode(dinp["q"][:, t], dinp["k"][:, t], dinp["v"][:, t], state, dout,
                   g=dinp["g"][:, t], beta=dinp["beta"][:, t])
 
     def prefill():
-        pstate.zero_()                            # zero initial state (outside the timed bracket)
-        cg.prefill(pinp["q"], pinp["k"], pinp["v"], pstate, pout, g=pinp["g"], beta=pinp["beta"], chunk=64)
+        cg.prefill(pinp["q"], pinp["k"], pinp["v"], pstate, pout, workspace=pws, **pkw)
 
-    pre_path = cg.prefill_path_for(pinp["q"], pinp["k"], pinp["v"], pstate, pout, g=pinp["g"], beta=pinp["beta"],
-                                   chunk=64)
+    pre_path = cg.prefill_path_for(pinp["q"], pinp["k"], pinp["v"], pstate, pout, **pkw)
     pre_kernel = PREFILL_KERNELS[pre_path]
-    for i in range(args.warmup):
-        flush_l2(); decode(i); flush_l2(); prefill()
-    torch.cuda.synchronize()
-
     K = args.steps
+    NS = max(64, K)                               # sustained back-to-back decode steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    es0, es1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the clock sampler runs from before the warm-up, so that its start-up pause is not an idle gap
+    # between the warm-up and the timed launches
     with ClockSampler(local_rank) as clk:
+        for i in range(args.warmup):
+            flush_l2(); decode(i); flush_l2(); pstate.zero_(); prefill()
+        for i in range(3):
+            decode(i, dstates[i % 3])
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         t_wall = time.perf_counter()
         for i in range(K):
             flush_l2()
@@ -235,16 +253,20 @@ def run_ours(args, rank, world, local_rank):
             flush_l2()
             pstate.zero_()
             ev[i][2].record(stream)
-            cg.prefill(pinp["q"], pinp["k"], pinp["v"], pstate, pout, g=pinp["g"], beta=pinp["beta"], chunk=64)
+            prefill()
             ev[i][3].record(stream)
+        es0.record(stream)
+        for i in range(NS):
+            decode(i, dstates[i % 3])
+        es1.record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     if world > 1:
         dist.barrier()
     dec_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     pre_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
-    dec_total, pre_total, step_total = max_over_ranks([sum(dec_ms), sum(pre_ms), sum(dec_ms) + sum(pre_ms)], world,
-                                                      dev)
+    sus_ms = es0.elapsed_time(es1)
+    dec_total, pre_total, sus_total = max_over_ranks([sum(dec_ms), sum(pre_ms), sus_ms], world, dev)
 
     # ---- end to end: host (pinned) buffers, copies inside the timed region
     e2e = run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world)
@@ -253,32 +275,43 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     hbm, tflops, peak_kind = _peaks()
-    dec_gbs, pre_tps = job_rates(dec_total, pre_total, world, K)
-    dec_launch_s = statistics.mean(dec_ms) / 1e3
-    pre_launch_s = statistics.mean(pre_ms) / 1e3
+    sus_step_s = sus_total / NS / 1e3
+    dec_gbs = world * DEC_STATE_BYTES / sus_step_s / 1e9              # whole job, sustained
+    _, pre_tps = job_rates(dec_total, pre_total, world, K)
+    dec_launch_s = statistics.median(dec_ms) / 1e3
+    pre_launch_s = statistics.median(pre_ms) / 1e3
     pre_ach = PRE_BYTES / pre_launch_s / 1e9
-    dec_ach = DEC_STATE_BYTES / dec_launch_s / 1e9
+    dec_ach_flushed = DEC_STATE_BYTES / dec_launch_s / 1e9
+    dec_ach_sus = DEC_STATE_BYTES / sus_step_s / 1e9
     tr_pre = _traffic(*pre_kernel)
     tr_dec = _traffic(*DECODE_KERNEL)
     out = {
         "metric": METRIC, "value": round(dec_gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(step_total / K, 5), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(sus_step_s * 1e3 + pre_total / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": bench_config(world),
         "pct_hbm_peak": round(100.0 * dec_gbs / world / hbm, 2),
         "prefill": {"metric": "prefill tokens/s at T=4000, 32 heads", "value": round(pre_tps, 1),
-                    "unit": "tokens/s", "ms_per_launch": round(pre_launch_s * 1e3, 5), "kernel": pre_kernel[0]},
-        "decode_ms_per_launch": round(dec_launch_s * 1e3, 5),
+                    "unit": "tokens/s", "ms_per_launch_median": round(pre_launch_s * 1e3, 5),
+                    "ms_per_launch_mean": round(statistics.mean(pre_ms), 5), "o_dtype": "bf16",
+                    "kernel": pre_kernel[0]},
+        "decode": {"ms_per_step_sustained": round(sus_step_s * 1e3, 5), "sustained_steps": NS,
+                   "ms_per_launch_flushed_median": round(dec_launch_s * 1e3, 5),
+                   "ms_per_launch_flushed_mean": round(statistics.mean(dec_ms), 5)},
         "roofline": {"kernel": pre_kernel[0], "bound": "hbm", "achieved": round(pre_ach, 2), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(pre_ach / hbm, 4),
-                     "traffic": tr_pre, "algorithmic_bytes": PRE_BYTES,
+                     "traffic": tr_pre, "algorithmic_bytes": PRE_BYTES, "o_dtype": "bf16",
+                     "time": "median per-launch CUDA-event time after an L2 flush",
                      "tensor_flops": PRE_FLOPS, "tensor_frac": round(PRE_FLOPS / pre_launch_s / 1e12 / tflops, 4)},
-        "decode_roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": round(dec_ach, 2), "peak": hbm,
-                            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
+        "decode_roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": round(dec_ach_sus, 2),
+                            "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_ach_sus / hbm, 4),
+                            "time": "sustained: %d back-to-back steps over three rotating states" % NS,
+                            "achieved_flushed": round(dec_ach_flushed, 2),
+                            "frac_flushed": round(dec_ach_flushed / hbm, 4),
                             "traffic": tr_dec, "algorithmic_bytes": DEC_STATE_BYTES},
         "e2e": e2e,
         "secondary": secondary,
-        "gpu_launches": 2 * K,
+        "gpu_launches": 2 * K + NS,
         "wall_s_timed_region": round(t_wall, 3),
     }
     out["clocks"] = clk.summary()
@@ -320,52 +353,52 @@ def run_secondary(cg, dev, stream, flush_l2):
     out["gdn_decode_b1"] = {"workload": "fused GatedDeltaNet decode B=1, 16 k-heads -> 32 v-heads, packed bf16 qkv",
                             "us_per_step_eager": round(eager_us, 3),
                             "us_per_step_cuda_graph": round(graph_us, 3) if isinstance(graph_us, float) else graph_us,
-                            "state_bytes_per_step": state_bytes, "steps": w.T}
+                            "state_bytes_per_step": state_bytes, "steps": w.T,
+                            "note": "the 4.2 MB state stays resident in the 129 MB L2 from step to step: "
+                                    "these are L2 rates, not HBM rates"}
     del inp, st, o
+    hbm, _, _ = _peaks()
+
+    def time_prefill(inp, st, o, path):
+        ws = torch.empty(max(1, cg.prefill_workspace_size(inp["q"], inp["k"], inp["v"], st, o, chunk=64, path=path,
+                                                          **gate_kwargs(inp))), dtype=torch.uint8, device=dev)
+        ms = []
+        for _ in range(3):
+            st.copy_(inp["S0"])
+            flush_l2()
+            e0.record(stream)
+            cg.prefill(inp["q"], inp["k"], inp["v"], st, o, chunk=64, path=path, workspace=ws, **gate_kwargs(inp))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return round(min(ms[1:]), 4)
+
     w = WORKLOADS["prefill_long"]
     inp = make_inputs(w, device=dev)
     st = torch.empty_like(inp["S0"])
-    o = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
-    ms = []
-    for _ in range(3):
-        st.copy_(inp["S0"])
-        flush_l2()
-        e0.record(stream)
-        cg.prefill(inp["q"], inp["k"], inp["v"], st, o, chunk=64, **gate_kwargs(inp))
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
-    t = min(ms[1:])
-    nbytes = w.B * w.T * w.Hv * (3 * 128 * 2 + 128 * 4 + 4 + 128 * 4) + 2 * w.B * w.Hv * 128 * 128 * 4
-    hbm, _, _ = _peaks()
-    out["prefill_long"] = {"workload": "prefill B=4 H=32 T=16411 chunk 64, g = -softplus(N(1,1))",
-                           "ms_per_launch": round(t, 4), "tokens_per_s": round(w.B * w.T / (t / 1e3), 1),
-                           "algorithmic_bytes": nbytes, "roofline_frac": round(nbytes / (t / 1e3) / 1e9 / hbm, 4)}
-    def time_prefill(inp, st, o, path):
-        cg.set_prefill_path(path)
-        try:
-            ms = []
-            for _ in range(3):
-                st.copy_(inp["S0"])
-                flush_l2()
-                e0.record(stream)
-                cg.prefill(inp["q"], inp["k"], inp["v"], st, o, chunk=64, **gate_kwargs(inp))
-                e1.record(stream)
-                torch.cuda.synchronize()
-                ms.append(e0.elapsed_time(e1))
-        finally:
-            cg.set_prefill_path(cg.PREFILL_AUTO)
-        return round(min(ms[1:]), 4)
-
-    out["prefill_long"]["ms_per_launch_cluster_kernel"] = time_prefill(inp, st, o, cg.PREFILL_CLUSTER)
-    out["prefill_long"]["ms_per_launch_per_head_kernel"] = time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)
-    del inp, st, o
+    o = torch.empty(inp["v"].shape, dtype=torch.bfloat16, device=dev)
+    o32 = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
+    t = time_prefill(inp, st, o, cg.PREFILL_AUTO)
+    nbytes = prefill_bytes(w.B, w.T, w.Hv, 2)
+    out["prefill_long"] = {"workload": "prefill B=4 H=32 T=16411 chunk 64, g = -softplus(N(1,1)), o bf16",
+                           "ms_per_launch": t, "tokens_per_s": round(w.B * w.T / (t / 1e3), 1),
+                           "algorithmic_bytes": nbytes, "roofline_frac": round(nbytes / (t / 1e3) / 1e9 / hbm, 4),
+                           "ms_per_launch_cluster_kernel": time_prefill(inp, st, o, cg.PREFILL_CLUSTER),
+                           "ms_per_launch_per_head_kernel": time_prefill(inp, st, o, cg.PREFILL_PER_HEAD),
+                           "ms_per_launch_o_fp32": time_prefill(inp, st, o32, cg.PREFILL_AUTO),
+                           "algorithmic_bytes_o_fp32": prefill_bytes(w.B, w.T, w.Hv, 4)}
+    del inp, st, o, o32
     w = WORKLOADS["prefill_t4000"]
     inp = make_inputs(w, device=dev)
     st = torch.empty_like(inp["S0"])
-    o = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
-    out["prefill_t4000_by_kernel"] = {"ms_per_launch_cluster_kernel": time_prefill(inp, st, o, cg.PREFILL_CLUSTER),
-                                      "ms_per_launch_per_head_kernel": time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)}
+    o = torch.empty(inp["v"].shape, dtype=torch.bfloat16, device=dev)
+    o32 = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
+    out["prefill_t4000_by_kernel"] = {"o": "bf16",
+                                      "ms_per_launch_cluster_kernel": time_prefill(inp, st, o, cg.PREFILL_CLUSTER),
+                                      "ms_per_launch_per_head_kernel": time_prefill(inp, st, o, cg.PREFILL_PER_HEAD),
+                                      "ms_per_launch_o_fp32": time_prefill(inp, st, o32, cg.PREFILL_AUTO),
+                                      "algorithmic_bytes_o_fp32": PRE_BYTES_F32O}
+    del o32
     del inp, st, o
     # prefill over a range of lengths and batches (same shapes and distributions as the T = 4000
     # workload), by the kernel the library picks; small T at B = 64 also by the chunked kernel, and
@@ -376,7 +409,7 @@ def run_secondary(cg, dev, stream, flush_l2):
                       s0_std=0.0, seed=5000 + T)
         inp = make_inputs(wl, device=dev)
         st = torch.empty_like(inp["S0"])
-        o = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
+        o = torch.empty(inp["v"].shape, dtype=torch.bfloat16, device=dev)
         key = "B%d_T%d" % (B, T)
         pth = cg.prefill_path_for(inp["q"], inp["k"], inp["v"], st, o, chunk=64, **gate_kwargs(inp))
         t_auto = time_prefill(inp, st, o, cg.PREFILL_AUTO)
@@ -469,13 +502,14 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
                                                       stream=stream), True)
     # prefill: q, k, v, g, beta in, o out (zero initial state each step, as in the timed kernel)
     hp = {k: pinp[k].contiguous().cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
-    po_like = torch.empty(pinp["v"].shape, dtype=torch.float32)
+    po_like = torch.empty(pinp["v"].shape, dtype=torch.bfloat16)
     ps = torch.zeros_like(pinp["S0"])
     h2d_pre = sum(x.numel() * x.element_size() for x in hp.values())
     d2h_pre = po_like.numel() * po_like.element_size()
     ws = torch.empty(max(1, cg.prefill_workspace_size(pinp["q"], pinp["k"], pinp["v"], ps,
-                                                      torch.empty(pinp["v"].shape, device=dev), g=pinp["g"],
-                                                      beta=pinp["beta"], chunk=64)), dtype=torch.uint8, device=dev)
+                                                      torch.empty(pinp["v"].shape, dtype=torch.bfloat16, device=dev),
+                                                      g=pinp["g"], beta=pinp["beta"], chunk=64)),
+                     dtype=torch.uint8, device=dev)
 
     def pcompute(d, o):
         ps.zero_()
@@ -587,13 +621,13 @@ def run_case(name):
     from gated_delta_rule_channelwise_gb300.synth import Workload, gate_kwargs, make_inputs
     cbuild.build()
     if name.startswith("prefill_t1024"):
-        if name == "prefill_t1024_per_head":
-            cg.set_prefill_path(cg.PREFILL_PER_HEAD)
+        path = cg.PREFILL_PER_HEAD if name == "prefill_t1024_per_head" else cg.PREFILL_AUTO
         w = Workload("p", B=1, Hk=32, Hv=32, dk=128, dv=128, T=1024, dtype="bf16", gate="channel", seed=1)
         inp = make_inputs(w, device="cuda")
+        o = torch.empty(inp["v"].shape, dtype=torch.bfloat16, device="cuda")
         for _ in range(2):
             st = torch.zeros_like(inp["S0"])
-            cg.prefill(inp["q"], inp["k"], inp["v"], st, chunk=64, **gate_kwargs(inp))
+            cg.prefill(inp["q"], inp["k"], inp["v"], st, o, chunk=64, path=path, **gate_kwargs(inp))
     elif name == "decode_b16":
         w = Workload("d", B=16, Hk=32, Hv=32, dk=128, dv=128, T=2, dtype="bf16", gate="channel", seed=1)
         inp = make_inputs(w, device="cuda")

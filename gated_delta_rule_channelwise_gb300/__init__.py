@@ -11,8 +11,13 @@ Public calls (same names as the C ABI without the ``cgdr_`` prefix):
 
 * :func:`decode` -- one T = 1 step for every (batch, v-head).
 * :func:`prefill` -- chunked prefill over T tokens.
-* :func:`prefill_workspace_size`, :func:`validate`, :func:`status_string`.
-* :func:`set_prefill_path`, :func:`prefill_path_for` -- which prefill kernel runs.
+* :func:`prefill_noalloc` -- prefill with the library's static scratch instead of a workspace.
+* :func:`prefill_workspace_size`, :func:`workspace_status`, :func:`validate`, :func:`status_string`.
+* :func:`prefill_path_for` -- which prefill kernel a call runs.
+
+The prefill kernel is chosen per call (``path=``, one of the ``PREFILL_*``
+codes; ``PREFILL_AUTO`` by default): the choice travels in the argument
+block, so concurrent calls never affect each other.
 """
 from __future__ import annotations
 
@@ -37,6 +42,7 @@ class CgdrArgs(ctypes.Structure):
         ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("gate", ctypes.c_int32), ("l2norm_qk", ctypes.c_int32),
         ("chunk", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
+        ("prefill_path", ctypes.c_int32), ("wait_polls", ctypes.c_int32),
         ("q_scale", ctypes.c_float), ("eps", ctypes.c_float),
         ("q", ctypes.c_void_p), ("q_sb", _i64), ("q_st", _i64), ("q_sh", _i64),
         ("k", ctypes.c_void_p), ("k_sb", _i64), ("k_st", _i64), ("k_sh", _i64),
@@ -48,6 +54,7 @@ class CgdrArgs(ctypes.Structure):
         ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
         ("state", ctypes.c_void_p),
         ("o", ctypes.c_void_p), ("o_sb", _i64), ("o_st", _i64), ("o_sh", _i64),
+        ("status", ctypes.c_void_p),
     ]
 
 
@@ -64,7 +71,6 @@ _SIGNATURES = [
     ("cgdr_prefill", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("cgdr_workspace_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("cgdr_prefill_noalloc", ctypes.c_int, [ctypes.POINTER(CgdrArgs), ctypes.c_void_p]),
-    ("cgdr_set_prefill_path", ctypes.c_int, [ctypes.c_int]),
     ("cgdr_prefill_path_for", ctypes.c_int, [ctypes.POINTER(CgdrArgs)]),
 ]
 
@@ -121,6 +127,12 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+def _check_status(status):
+    import torch
+    if status is not None and (not status.is_cuda or status.dtype != torch.int32 or status.numel() < 1):
+        raise TypeError("status must be an int32 CUDA tensor")
+
+
 def _need_cuda(*ts):
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -139,11 +151,15 @@ _NONE4 = (None, 0, 0, 0)
 
 
 def make_args(q, k, v, state, o, *, T, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
-              l2norm=True, q_scale=None, eps=None, chunk=0) -> CgdrArgs:
+              l2norm=True, q_scale=None, eps=None, chunk=0, path=PREFILL_AUTO, wait_polls=0,
+              status=None) -> CgdrArgs:
     """Fill a ``cgdr_args`` block from 4-d views ``[B, T, H, d]`` (token dim included).
 
     Gate tensors are ``g [B,T,Hv,dk]`` and ``beta [B,T,Hv]`` (channel gate) or
-    ``a, b [B,T,Hv]`` with ``A_log, dt_bias [Hv]`` (GatedDeltaNet gate).
+    ``a, b [B,T,Hv]`` with ``A_log, dt_bias [Hv]`` (GatedDeltaNet gate).  ``path`` is the
+    prefill kernel of the call, ``wait_polls`` the polls of a bounded device wait (0: the
+    library's default; small values are for failure-path tests) and ``status`` an optional
+    int32 device tensor that receives ``ERR_TIMEOUT`` if a wait gives up.
     The block is built in one constructor call (field order of ``struct cgdr_args``).
     """
     B, _, Hk, dk = q.shape
@@ -165,9 +181,11 @@ def make_args(q, k, v, state, o, *, T, g=None, beta=None, a=None, b=None, A_log=
         ab = (b.data_ptr(), sb[0], sb[1], sb[2])
         alog, dtb = A_log.data_ptr(), dt_bias.data_ptr()
     return CgdrArgs(B, T, Hk, Hv, dk, dv, _dtype_code(q), gate, 1 if l2norm else 0, int(chunk), _dtype_code(o),
+                    int(path), int(wait_polls),
                     float(q_scale) if q_scale is not None else 0.0, float(eps) if eps is not None else -1.0,
                     *_ptr_strides(q, "q"), *_ptr_strides(k, "k"), *_ptr_strides(v, "v"), *gg, *bb, *aa, *ab,
-                    alog, dtb, state.data_ptr(), *_ptr_strides(o, "o"))
+                    alog, dtb, state.data_ptr(), *_ptr_strides(o, "o"),
+                    status.data_ptr() if status is not None else None)
 
 
 def _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias):
@@ -188,18 +206,21 @@ def _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias):
 
 
 def decode(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
-           l2norm=True, q_scale=None, eps=None, stream=None):
+           l2norm=True, q_scale=None, eps=None, status=None, wait_polls=0, stream=None):
     """One decode step.  q, k ``[B,Hk,dk]``; v ``[B,Hv,dv]``; state ``[B,Hv,dk,dv]`` fp32
     (updated in place); gate ``g [B,Hv,dk]`` + ``beta [B,Hv]`` or ``a, b [B,Hv]`` +
     ``A_log, dt_bias [Hv]``.  Returns o ``[B,Hv,dv]``: the given ``o`` (fp32 or bf16) or a
-    new fp32 tensor."""
+    new fp32 tensor (allocated through torch's caching allocator).  ``status``: optional
+    int32 device tensor that receives ``ERR_TIMEOUT`` if a bounded wait gives up."""
     import torch
     if o is None:
         o = torch.empty(v.shape, dtype=torch.float32, device=v.device)
     _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
+    _check_status(status)
     u = lambda t: None if t is None else t.unsqueeze(1)
     A = make_args(u(q), u(k), u(v), state, u(o), T=1, g=u(g), beta=u(beta), a=u(a), b=u(b),
-                  A_log=A_log, dt_bias=dt_bias, l2norm=l2norm, q_scale=q_scale, eps=eps)
+                  A_log=A_log, dt_bias=dt_bias, l2norm=l2norm, q_scale=q_scale, eps=eps,
+                  wait_polls=wait_polls, status=status)
     _check(lib().cgdr_decode(ctypes.byref(A), _stream_handle(stream)), "cgdr_decode")
     return o
 
@@ -210,17 +231,25 @@ def prefill_workspace_size(q, k, v, state, o, **kw) -> int:
 
 
 def prefill(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
-            l2norm=True, q_scale=None, eps=None, chunk=64, workspace=None, stream=None):
+            l2norm=True, q_scale=None, eps=None, chunk=64, path=PREFILL_AUTO, workspace=None, status=None,
+            wait_polls=0, stream=None):
     """Chunked prefill.  q, k ``[B,T,Hk,dk]``; v ``[B,T,Hv,dv]``; state ``[B,Hv,dk,dv]``
     fp32 (updated in place); gate ``g [B,T,Hv,dk]`` + ``beta [B,T,Hv]`` or
-    ``a, b [B,T,Hv]`` + ``A_log, dt_bias [Hv]``.  Returns o ``[B,T,Hv,dv]``: the given ``o``
-    (fp32 or bf16) or a new fp32 tensor."""
+    ``a, b [B,T,Hv]`` + ``A_log, dt_bias [Hv]``.  ``path`` forces a kernel for this call.
+    Returns o ``[B,T,Hv,dv]``: the given ``o`` (fp32 or bf16) or a new fp32 tensor.
+
+    The library itself allocates nothing.  This binding is a convenience: when ``o`` is not
+    given, or ``workspace`` is missing or smaller than :func:`prefill_workspace_size`, it
+    allocates them through torch's caching allocator (a ``cudaMalloc`` the first time a size
+    is seen).  Pass both to keep the call free of allocations."""
     import torch
     if o is None:
         o = torch.empty(v.shape, dtype=torch.float32, device=v.device)
     _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
+    _check_status(status)
     A = make_args(q, k, v, state, o, T=q.shape[1], g=g, beta=beta, a=a, b=b, A_log=A_log, dt_bias=dt_bias,
-                  l2norm=l2norm, q_scale=q_scale, eps=eps, chunk=chunk)
+                  l2norm=l2norm, q_scale=q_scale, eps=eps, chunk=chunk, path=path, wait_polls=wait_polls,
+                  status=status)
     L = lib()
     need = int(L.cgdr_prefill_workspace_size(ctypes.byref(A)))
     if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
@@ -233,28 +262,23 @@ def prefill(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=
 
 
 def prefill_noalloc(q, k, v, state, o=None, *, g=None, beta=None, a=None, b=None, A_log=None, dt_bias=None,
-                    l2norm=True, q_scale=None, eps=None, chunk=64, stream=None):
+                    l2norm=True, q_scale=None, eps=None, chunk=64, path=PREFILL_AUTO, status=None, stream=None):
     """`prefill` with the library's static scratch instead of a workspace (allocates nothing
     on the device when ``o`` is given).  Calls that overlap on the GPU race on that scratch."""
     import torch
     if o is None:
         o = torch.empty(v.shape, dtype=torch.float32, device=v.device)
     _check_types(q, k, v, state, o, g, beta, a, b, A_log, dt_bias)
+    _check_status(status)
     A = make_args(q, k, v, state, o, T=q.shape[1], g=g, beta=beta, a=a, b=b, A_log=A_log, dt_bias=dt_bias,
-                  l2norm=l2norm, q_scale=q_scale, eps=eps, chunk=chunk)
+                  l2norm=l2norm, q_scale=q_scale, eps=eps, chunk=chunk, path=path, status=status)
     _check(lib().cgdr_prefill_noalloc(ctypes.byref(A), _stream_handle(stream)), "cgdr_prefill_noalloc")
     return o
 
 
-def set_prefill_path(path: int) -> None:
-    """Process-wide prefill kernel choice: PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT or
-    PREFILL_RECURRENT (the token recurrence for 1 <= T <= 8)."""
-    _check(lib().cgdr_set_prefill_path(int(path)), "cgdr_set_prefill_path")
-
-
 def prefill_path_for(q, k, v, state, o, **kw) -> int:
-    """The kernel (PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT or PREFILL_RECURRENT) a prefill with these arguments
-    runs under the current choice; PREFILL_AUTO if the arguments are invalid or there is no work."""
+    """The kernel (PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT or PREFILL_RECURRENT) a prefill with these
+    arguments (``path=`` included) runs; PREFILL_AUTO if the arguments are invalid or there is no work."""
     A = make_args(q, k, v, state, o, T=q.shape[1], **kw)
     return int(lib().cgdr_prefill_path_for(ctypes.byref(A)))
 
@@ -268,6 +292,6 @@ def validate(A: CgdrArgs, for_prefill: bool) -> int:
     return int(lib().cgdr_validate(ctypes.byref(A), 1 if for_prefill else 0))
 
 
-__all__ = ["decode", "prefill", "prefill_noalloc", "prefill_workspace_size", "workspace_status", "validate", "status_string", "make_args",
-           "set_prefill_path", "prefill_path_for",
+__all__ = ["decode", "prefill", "prefill_noalloc", "prefill_workspace_size", "workspace_status", "validate",
+           "status_string", "make_args", "prefill_path_for",
            "CgdrArgs", "CgdrError", "lib", "LIB_PATH"]

@@ -7,8 +7,6 @@
 
 namespace {
 
-std::atomic<int> g_prefill_path{CGDR_PREFILL_AUTO};
-
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
 bool aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -28,7 +26,10 @@ cgdr_status check(const cgdr_args *a, bool prefill) {
     if (a->gate != CGDR_GATE_CHANNEL && a->gate != CGDR_GATE_GDN) return CGDR_ERR_UNSUPPORTED;
     if (prefill && !(a->chunk == 0 || a->chunk == 16 || a->chunk == 32 || a->chunk == 64))
         return CGDR_ERR_UNSUPPORTED;
+    if (prefill && (a->prefill_path < CGDR_PREFILL_AUTO || a->prefill_path > CGDR_PREFILL_RECURRENT))
+        return CGDR_ERR_INVALID_ARG;
     if (a->B == 0 || a->T == 0) return CGDR_OK;  // nothing to do: no pointer is touched
+    if (!aligned(a->status, 4)) return CGDR_ERR_ALIGNMENT;
 
     if (!a->q || !a->k || !a->v || !a->state || !a->o) return CGDR_ERR_INVALID_ARG;
     if (a->gate == CGDR_GATE_CHANNEL && (!a->g || !a->beta)) return CGDR_ERR_INVALID_ARG;
@@ -79,8 +80,40 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int device_sms() {
+    static std::atomic<int> cache[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    int sms = cache[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev].store(sms, std::memory_order_relaxed);
+    }
+    return sms;
+}
+
+bool smem_limit_once(SmemOnce &once, const void *fn, int bytes) {
+    const int dev = current_device();
+    if (dev < 0) return false;
+    const uint64_t bit = 1ull << dev;
+    if (once.mask.load(std::memory_order_acquire) & bit) return true;
+    // idempotent: two threads racing here both set the same attribute
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    once.mask.fetch_or(bit, std::memory_order_acq_rel);
+    return true;
+}
+
 int prefill_path(const cgdr_args &a, bool allow_cluster) {
-    const int choice = g_prefill_path.load();
+    const int choice = a.prefill_path;
     const bool few = a.T >= 1 && a.T <= kRecurrentMaxT;
     if (few && (choice == CGDR_PREFILL_AUTO || choice == CGDR_PREFILL_RECURRENT)) return CGDR_PREFILL_RECURRENT;
     if (choice == CGDR_PREFILL_SIMT || !prefill_tc05_supported(a)) return CGDR_PREFILL_SIMT;
@@ -91,10 +124,7 @@ int prefill_path(const cgdr_args &a, bool allow_cluster) {
         // GB300), but four times fewer clusters than CTAs are resident at once.
         const int64_t units = (int64_t)a.B * a.Hv;
         const int cap = prefill_cluster_capacity();
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                         cudaSuccess)
-            sms = 0;
+        const int sms = device_sms();
         path = CGDR_PREFILL_PER_HEAD;
         if (cap > 0 && sms > 0) {
             const int64_t waves_cluster = (units + cap - 1) / cap, waves_head = (units + sms - 1) / sms;
@@ -111,8 +141,7 @@ size_t prefill_workspace_for(const cgdr_args &a, int path) {
     return 0;
 }
 
-cgdr_status prefill_dispatch(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s, bool allow_cluster) {
-    const int path = prefill_path(a, allow_cluster);
+cgdr_status prefill_dispatch(const cgdr_args &a, int path, void *ws, size_t ws_bytes, cudaStream_t s) {
     if (path == CGDR_PREFILL_RECURRENT) return launch_recurrent(a, s);
     if (path == CGDR_PREFILL_SIMT) return launch_prefill_simt(a, s);
     const size_t need = prefill_workspace_for(a, path);
@@ -154,12 +183,6 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *a) {
     return cgdr::prefill_workspace_for(*a, cgdr::prefill_path(*a, true));
 }
 
-cgdr_status cgdr_set_prefill_path(int path) {
-    if (path < CGDR_PREFILL_AUTO || path > CGDR_PREFILL_RECURRENT) return CGDR_ERR_INVALID_ARG;
-    g_prefill_path.store(path);
-    return CGDR_OK;
-}
-
 int cgdr_prefill_path_for(const cgdr_args *a) {
     if (check(a, true) != CGDR_OK || a->B == 0 || a->T == 0) return CGDR_PREFILL_AUTO;
     return cgdr::prefill_path(*a, true);
@@ -168,7 +191,7 @@ int cgdr_prefill_path_for(const cgdr_args *a) {
 cgdr_status cgdr_prefill(const cgdr_args *a, void *ws, size_t ws_bytes, void *stream) {
     cgdr_status st = check(a, true);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
-    return cgdr::prefill_dispatch(*a, ws, ws_bytes, static_cast<cudaStream_t>(stream), true);
+    return cgdr::prefill_dispatch(*a, cgdr::prefill_path(*a, true), ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 cgdr_status cgdr_workspace_status(const void *ws, void *stream) {

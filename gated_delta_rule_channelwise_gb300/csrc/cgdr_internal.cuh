@@ -1,6 +1,8 @@
 // Internal declarations and device helpers shared by the libcgdr kernels.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -11,6 +13,26 @@
 namespace cgdr {
 
 // ---------------------------------------------------------------- host side
+constexpr int kMaxDevices = 64;
+// The calling thread's current device, or -1 (also for an index past kMaxDevices).
+int current_device();
+// SM count of the current device, queried once per device; 0 if unknown.
+int device_sms();
+// Per-kernel record of the devices whose dynamic shared-memory limit has been raised.
+struct SmemOnce {
+    std::atomic<uint64_t> mask{0};
+};
+// Raises `fn`'s dynamic shared-memory limit to `bytes` once per device; false on failure.
+bool smem_limit_once(SmemOnce &once, const void *fn, int bytes);
+// Polls of a bounded device wait on a kernel's own data (args.wait_polls, 0 = default; a
+// negative value also asks for the injected first wait, see inject_of).
+constexpr uint32_t kDefaultPolls = 1u << 20;
+inline uint32_t polls_of(const cgdr_args &a) {
+    return a.wait_polls > 0 ? (uint32_t)a.wait_polls : (a.wait_polls < 0 ? (uint32_t)(-(int64_t)a.wait_polls) : kDefaultPolls);
+}
+// Test hook: the first main-loop wait of every block waits on a barrier nothing completes.
+inline int inject_of(const cgdr_args &a) { return a.wait_polls < 0 ? 1 : 0; }
+
 cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s);
 // Prefill with 1 <= T <= kRecurrentMaxT: the decode kernel stepping through the tokens.
 constexpr int kRecurrentMaxT = 8;
@@ -21,11 +43,12 @@ size_t prefill_tc05_workspace(const cgdr_args &a);
 cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s);
 int prefill_cluster_capacity();
 size_t prefill_cluster_workspace(const cgdr_args &a);
-// The prefill kernel for `a` under the process-wide choice (CGDR_PREFILL_PER_HEAD,
-// _CLUSTER or _SIMT); allow_cluster = false maps the cluster kernel to the per-head one.
+// The prefill kernel for `a` given a.prefill_path (CGDR_PREFILL_PER_HEAD, _CLUSTER, _SIMT or
+// _RECURRENT); allow_cluster = false maps the cluster kernel to the per-head one.
 int prefill_path(const cgdr_args &a, bool allow_cluster);
 size_t prefill_workspace_for(const cgdr_args &a, int path);
-cgdr_status prefill_dispatch(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s, bool allow_cluster);
+// Runs the kernel `path` (as prefill_path returned it) with the given workspace.
+cgdr_status prefill_dispatch(const cgdr_args &a, int path, void *ws, size_t ws_bytes, cudaStream_t s);
 cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s);
 
 // The driver's tiled tensor-map encoder, looked up once through the runtime (nullptr if

@@ -38,6 +38,9 @@ struct DecodeParams {
     float *state;
     void *o;
     int64_t o_sb, o_sh, o_st;
+    int *status;                                      // optional: CGDR_ERR_TIMEOUT if a wait gave up
+    uint32_t polls;                                   // polls of the main-loop tile waits
+    int inject;                                       // test hook: the first tile wait targets a dead barrier
 };
 
 template <int DK, int DV>
@@ -94,7 +97,7 @@ struct PipeShape {
     static constexpr int SMALL1 = 2 * ROWQ + ROWV + ROWG;      // one token's q, k, v, g rows
     static constexpr int SMALL = NTOK * SMALL1;
     static constexpr int STAGE = ((TILE + SMALL + 127) / 128) * 128;
-    static constexpr int BYTES = NS * STAGE + 64 + 128;   // stages, mbarriers, alignment slack
+    static constexpr int BYTES = NS * STAGE + 64 + 128;   // stages, mbarriers (NS + 1 <= 8), alignment slack
 };
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
     constexpr int CL = Sh::CL, RW = Sh::RW, NW = Sh::NW, RPT = Sh::RPT, NT = Sh::NT, NS = Ps::NS;
     static_assert(NTOK <= NT, "one thread per token holds its scalars");
     const int ntok = NTOK == 1 ? 1 : p.ntok;
-    constexpr uint32_t kSpin = 1u << 20;
+    constexpr uint32_t kSpin = kDefaultPolls;         // drain waits always use the full limit
     extern __shared__ __align__(128) char dsm_raw[];
     char *dsm = dsm_raw + ((128 - (smem_u32(dsm_raw) & 127)) & 127);
     const uint32_t sb = smem_u32(dsm);
@@ -134,8 +137,9 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
     const int c = lane % CL, r = lane / CL;
     const int G = gridDim.x;
 
+    // mbar0 + 8 * NS: a barrier nothing ever arrives on (the target of the injected failure)
     if (tid == 0) {
-        for (int st = 0; st < NS; ++st) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * st));
+        for (int st = 0; st <= NS; ++st) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * st));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
     for (int st = 0; st < NS - 1; ++st) issue(u0 + st * G, st);
     float2 sc0 = scalars(u0), sc1 = scalars(u0 + G);
     bool failed = false;
+    int kf = 0;                                       // iteration whose tile wait gave up
 
     for (int k = 0;; ++k) {
         const int u = u0 + k * G;
@@ -199,11 +204,14 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
         sc0 = sc1;
         sc1 = scalars(u0 + (k + 2) * G);
 
-        const bool got = mbar_wait_parity(mbar0 + 8 * st, (uint32_t)((k / NS) & 1), kSpin);
+        const bool dead = p.inject && k == 0;
+        const bool got = mbar_wait_parity(dead ? mbar0 + 8 * NS : mbar0 + 8 * st,
+                                          dead ? 0u : (uint32_t)((k / NS) & 1), p.polls);
         cp_async_wait_groups<NS - 1>();
         const int b = u / p.Hv, h = u % p.Hv;
         if (__syncthreads_or(!got)) {
             failed = true;
+            kf = k;
             break;
         }
         const char *stage = dsm + st * Ps::STAGE;
@@ -330,9 +338,12 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
     }
 
     if (failed) {
-        // A tile never arrived: mark this CTA's remaining outputs with NaN, then give the
-        // copies in flight a bounded chance to land before the CTA's shared memory is released.
-        for (int k = 0;; ++k) {
+        // A tile did not arrive in time at iteration kf: mark this CTA's outputs from there on with
+        // NaN and report it, then wait for every tile copy still in flight (iterations kf ..
+        // kf + NS - 1 were issued, each into stage j % NS as that stage's use j / NS) before the
+        // CTA's shared memory is released.
+        if (tid == 0 && p.status != nullptr) atomicExch(p.status, (int)CGDR_ERR_TIMEOUT);
+        for (int k = kf;; ++k) {
             const int u = u0 + k * G;
             if (u >= units) break;
             const int b = u / p.Hv, h = u % p.Hv;
@@ -342,7 +353,9 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
                 else static_cast<__nv_bfloat16 *>(p.o)[off] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
             }
         }
-        for (int st = 0; st < NS; ++st) mbar_wait_parity(mbar0 + 8 * st, 0u, kSpin);
+        if (tid == 0)
+            for (int j = kf; j < kf + NS; ++j)
+                if (u0 + j * G < units) mbar_wait_parity(mbar0 + 8 * (j % NS), (uint32_t)((j / NS) & 1), kSpin);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -351,13 +364,13 @@ template <int DK, int DV, typename T, int NTOK>
 cgdr_status launch_t(const DecodeParams &p, int units, cudaStream_t s) {
     using Sh = DecodeShape<DK, DV>;
     using Ps = PipeShape<DK, DV, T, NTOK>;
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static SmemOnce smem_once;
+    const int sms = device_sms();
+    if (sms <= 0) return CGDR_ERR_CUDA;
     // units per CTA as even as the SM count allows
     const int per = (units + sms - 1) / sms;
     const int grid = (units + per - 1) / per;
-    if (cudaFuncSetAttribute(decode_kernel<DK, DV, T, NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Ps::BYTES) != cudaSuccess)
+    if (!smem_limit_once(smem_once, reinterpret_cast<const void *>(decode_kernel<DK, DV, T, NTOK>), Ps::BYTES))
         return CGDR_ERR_CUDA;
     decode_kernel<DK, DV, T, NTOK><<<grid, Sh::NT, Ps::BYTES, s>>>(p, units);
     return cudaGetLastError() == cudaSuccess ? CGDR_OK : CGDR_ERR_CUDA;
@@ -387,6 +400,7 @@ DecodeParams params_of(const cgdr_args &a, int ntok) {
     p.a_sb = a.a_sb; p.a_sh = a.a_sh; p.b_sb = a.b_sb; p.b_sh = a.b_sh;
     p.A_log = a.A_log; p.dt_bias = a.dt_bias;
     p.state = a.state; p.o = a.o; p.o_sb = a.o_sb; p.o_sh = a.o_sh;
+    p.status = a.status; p.polls = polls_of(a); p.inject = inject_of(a);
     // token strides: a single token never steps them (decode ignores them)
     const bool one = ntok == 1;
     p.q_st = one ? 0 : a.q_st; p.k_st = one ? 0 : a.k_st; p.v_st = one ? 0 : a.v_st; p.g_st = one ? 0 : a.g_st;

@@ -96,9 +96,10 @@ __device__ __forceinline__ bool cl_test(uint32_t mbar, uint32_t parity) {
         : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
     return done != 0;
 }
-// Bounded wait, with cluster-scope acquire, for the phase of a local barrier with the given parity.
-__device__ __forceinline__ bool cl_wait(uint32_t mbar, uint32_t parity) {
-    for (uint32_t it = 0; it < kSpin; ++it) {
+// Bounded wait (`polls` polls), with cluster-scope acquire, for the phase of a local barrier
+// with the given parity.
+__device__ __forceinline__ bool cl_wait(uint32_t mbar, uint32_t parity, uint32_t polls) {
+    for (uint32_t it = 0; it < polls; ++it) {
         uint32_t done;
         asm volatile(
             "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
@@ -183,7 +184,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     {
         int okw = 1;
         if (tid == 0 && n > 0) {
-            okw = cl_wait(ready(0), slot_parity(0));
+            okw = cl_wait(ready(0), slot_parity(0), p.polls);
             if (okw) {
                 fence_global_to_async();
                 load_a(0);
@@ -196,7 +197,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     for (int c = 0; c < n; ++c) {
         // ---------------------------------------------------------- inbox A: Qg, Kg^T, V^T, Tb, e^gC
         {
-            const bool done = cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1));
+            const bool done = cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1), p.polls);
             if (__syncthreads_or(!done)) return false;
         }
         {
@@ -267,7 +268,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         fence_before_sync();
         // ---------------------------------------------------------- inbox B: [Kend^T; P]
         {
-            const bool done = cl_wait(sbase + CH_FULL_B, (uint32_t)(c & 1));
+            const bool done = cl_wait(sbase + CH_FULL_B, (uint32_t)(c & 1), p.polls);
             if (__syncthreads_or(!done)) return false;
         }
         if (tid == 0) {
@@ -284,7 +285,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         int okw = 1;
         if (tid == 0 && c + 1 < n) {
             if (!next_a) {
-                okw = cl_wait(ready(c + 1), slot_parity(c + 1));
+                okw = cl_wait(ready(c + 1), slot_parity(c + 1), p.polls);
                 if (okw) {
                     fence_global_to_async();
                     load_a(c + 1);
@@ -347,14 +348,14 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
     for (int c = c_first; c < n; c += NPREP, ++k) {
         const int t0 = c * C, L = min(C, p.T - t0), tn = t0 + NPREP * C;
         char *slot = slot_ptr(c);
-        if (!st.wait(sbase)) return false;
+        if (!st.wait(sbase, p.polls, p.inject && k == 0)) return false;
         // operand tiles; prefetch the next own chunk's g rows into L2 (they are staged last)
         prep_chunk<false>(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
         if (tid == kIO) {
             if (k > 0) announce(c - NPREP);
             // the slot's previous chunk (own chunk k - NSLOTP) has been pulled by rank 0
             int okw = 1;
-            if (k >= NSLOTP) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1));
+            if (k >= NSLOTP) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1), p.polls);
             if (okw) {
                 // Qg (64-row tile: 8 KB per K block) into rows 0..63 of [Qg; -W]; Kg^T; e^gC
 #pragma unroll
@@ -422,7 +423,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
     const int tid = threadIdx.x, warp = tid >> 5;
     const int n = (p.T + C - 1) / C;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + (chain ? CH_TMEM : M_TMEM));
-    MmaBar mb{sbase + (chain ? CH_MBAR : M_MBAR), 0u};
+    MmaBar mb{sbase + (chain ? CH_MBAR : M_MBAR), 0u, p.polls};
     if (tid == 0) {
         mbar_init(mb.mbar, 1);
         if (chain) {
@@ -432,6 +433,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
         } else {
             for (int i = 0; i < NSLOTP; ++i) mbar_init(sbase + M_SLOTFREE + 8 * i, 1);
             mbar_init(sbase + M_STAGE, 1);
+            mbar_init(sbase + M_DEAD, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -449,10 +451,10 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
     if (!ok && tid == 0) {
         // a wait gave up: record it, give the tensor core and the last bulk load on
         // each inbox (at most one can be outstanding) a bounded chance to finish
-        atomicExch(p.err, (int)CGDR_ERR_TIMEOUT);
+        record_timeout(p);
         mbar_wait(mb.mbar, mb.phase ^ 1u, kSpin);
-        if (ia > 0) cl_wait(sbase + CH_FULL_A, (uint32_t)((ia - 1) & 1));
-        if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1));
+        if (ia > 0) cl_wait(sbase + CH_FULL_A, (uint32_t)((ia - 1) & 1), kSpin);
+        if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1), kSpin);
         if (!chain) st.drain(sbase);
     }
     if (!chain && tid == kIO) bulk_store_wait();   // no bulk store may still read this CTA's shared memory
@@ -464,14 +466,14 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
 }
 
 std::mutex g_cluster_mutex;
-int g_cluster_fit[64];                         // per device: clusters resident at once, + 1 (0 = not queried)
+int g_cluster_fit[kMaxDevices];                         // per device: clusters resident at once, + 1 (0 = not queried)
 
 }  // namespace
 
 // Number of four-CTA clusters of this kernel the current device runs at once (0 if none fit).
 int prefill_cluster_capacity() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int dev = current_device();
+    if (dev < 0) return 0;
     std::lock_guard<std::mutex> lock(g_cluster_mutex);
     if (g_cluster_fit[dev] == 0) {
         int fit = 0;
@@ -497,9 +499,9 @@ cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s)
     Tc05Params p;
     if (!make_params(a, ws, p)) return CGDR_ERR_ALIGNMENT;
     p.slots = static_cast<unsigned char *>(ws) + WS_HEADER;
+    static SmemOnce smem_once;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CGDR_ERR_CUDA;
-    if (cudaFuncSetAttribute(prefill_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CL_SMEM_BYTES) !=
-        cudaSuccess)
+    if (!smem_limit_once(smem_once, reinterpret_cast<const void *>(prefill_cluster_kernel), CL_SMEM_BYTES))
         return CGDR_ERR_CUDA;
     dim3 grid(CLUSTER * a.Hv, a.B);
     prefill_cluster_kernel<<<grid, NT, CL_SMEM_BYTES, s>>>(p);

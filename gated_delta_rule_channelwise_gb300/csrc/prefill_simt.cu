@@ -235,9 +235,9 @@ __global__ void __launch_bounds__(SIMT_NT) prefill_simt_kernel(const PrefillPara
 
 template <int DK, int C, typename T>
 cgdr_status launch_t(const PrefillParams &p, int B, cudaStream_t s) {
+    static SmemOnce smem_once;
     const size_t smem = SimtSmem<DK, C>::bytes;
-    if (cudaFuncSetAttribute(prefill_simt_kernel<DK, C, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    if (!smem_limit_once(smem_once, reinterpret_cast<const void *>(prefill_simt_kernel<DK, C, T>), (int)smem))
         return CGDR_ERR_CUDA;
     dim3 grid(p.dv / SIMT_WS, p.Hv, B);
     prefill_simt_kernel<DK, C, T><<<grid, SIMT_NT, smem, s>>>(p);

@@ -35,10 +35,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     float *state = p.state + ((size_t)hd.b * p.Hv + hd.h) * DK * DV;
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
 
-    MmaBar mb{sbase + M_MBAR, 0u};
+    MmaBar mb{sbase + M_MBAR, 0u, p.polls};
     if (tid == 0) {
         mbar_init(mb.mbar, 1);
         mbar_init(sbase + M_STAGE, 1);
+        mbar_init(sbase + M_DEAD, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), T_COLS);
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     ChunkRegs cr;
     for (int t0 = 0; t0 < p.T && ok; t0 += C) {
         const int L = min(C, p.T - t0);
-        if (!(ok = st.wait(sbase))) break;
+        if (!(ok = st.wait(sbase, p.polls, p.inject && t0 == 0))) break;
         prep_chunk<true>(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
         if (!(ok = causal_terms<false>(sm, tmem, mb, cr, sm + R_F, 64, 0))) break;
         solve_tb(sm);
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     } else {
         // a wait gave up: record it, give the tensor core a bounded chance to finish, release TMEM
         if (tid == 0) {
-            atomicExch(p.err, (int)CGDR_ERR_TIMEOUT);
+            record_timeout(p);
             mbar_wait(mb.mbar, mb.phase ^ 1u, kSpin);
             st.drain(sbase);
         }
@@ -246,17 +247,20 @@ bool make_params(const cgdr_args &a, void *ws, Tc05Params &p) {
     p.state = a.state; p.o = a.o;
     p.o_sb = a.o_sb; p.o_st = a.o_st; p.o_sh = a.o_sh;
     p.err = static_cast<int *>(ws);
+    p.status = a.status;
+    p.polls = polls_of(a);
+    p.inject = inject_of(a);
     p.slots = nullptr;
     return true;
 }
 }  // namespace tc05c
 
 cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s) {
+    static SmemOnce smem_once;
     tc05c::Tc05Params p;
     if (!tc05c::make_params(a, ws, p)) return CGDR_ERR_ALIGNMENT;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CGDR_ERR_CUDA;
-    if (cudaFuncSetAttribute(prefill_tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc05c::PREP_SMEM_BYTES) != cudaSuccess)
+    if (!smem_limit_once(smem_once, reinterpret_cast<const void *>(prefill_tc05_kernel), tc05c::PREP_SMEM_BYTES))
         return CGDR_ERR_CUDA;
     dim3 grid(a.Hv, a.B);
     prefill_tc05_kernel<<<grid, tc05c::NT, tc05c::PREP_SMEM_BYTES, s>>>(p);
@@ -272,7 +276,6 @@ namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[CGDR_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_ptr[kMaxDevices] = {};
 
@@ -296,16 +299,17 @@ cgdr_status noalloc_scratch(int dev, void **out) {
 extern "C" cgdr_status cgdr_prefill_noalloc(const cgdr_args *a, void *stream) {
     const cgdr_status st = cgdr_validate(a, 1);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
-    // the cluster kernel's hand-off ring does not fit the static scratch: per-head kernel instead
+    // the cluster kernel's hand-off ring does not fit the static scratch: per-head kernel instead;
+    // the kernel is chosen once and that choice is what runs
     const int path = cgdr::prefill_path(*a, false);
     const size_t need = cgdr::prefill_workspace_for(*a, path);
     if (need > CGDR_NOALLOC_SCRATCH_BYTES) return CGDR_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (need == 0) return cgdr::prefill_dispatch(*a, nullptr, 0, s, false);
+    if (need == 0) return cgdr::prefill_dispatch(*a, path, nullptr, 0, s);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return CGDR_ERR_CUDA;
     void *scratch = nullptr;
     const cgdr_status s2 = cgdr::noalloc_scratch(dev, &scratch);
     if (s2 != CGDR_OK) return s2;
-    return cgdr::prefill_dispatch(*a, scratch, CGDR_NOALLOC_SCRATCH_BYTES, s, false);
+    return cgdr::prefill_dispatch(*a, path, scratch, CGDR_NOALLOC_SCRATCH_BYTES, s);
 }

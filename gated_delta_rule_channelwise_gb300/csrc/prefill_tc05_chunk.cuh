@@ -36,7 +36,7 @@ using namespace tc05;
 
 constexpr int C = 64, DK = 128, DV = 128, NT = 512;
 constexpr float kRange = 80.f;           // max |gamma_r - gamma_mid| for the tensor-core causal terms
-constexpr uint32_t kSpin = 1u << 20;     // bounded mbarrier wait (iterations)
+constexpr uint32_t kSpin = kDefaultPolls;   // bounded mbarrier wait (polls) of the drains after a failure
 
 // shared memory map of a CTA that prepares chunks (bytes from a 1024-aligned base)
 constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, V^T | U^T ; wide: q~, k~
@@ -52,7 +52,8 @@ constexpr int M_H0 = M_GS + 256, M_GM = M_H0 + 2048, M_GC = M_GM + 512, M_DEC = 
 constexpr int M_MBAR = M_DEC + 512, M_TMEM = M_MBAR + 8, M_SLOTFREE = M_TMEM + 8;   // 4 barriers
 constexpr int M_STAGE = M_SLOTFREE + 32;  // staging barrier: the TMA tiles of the next chunk's rows
 constexpr int M_FLAG = M_STAGE + 8;       // int flag passed between threads across a barrier
-constexpr int M_END = M_FLAG + 8;
+constexpr int M_DEAD = M_FLAG + 8;        // a barrier nothing arrives on (target of the injected failure)
+constexpr int M_END = M_DEAD + 8;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
 constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned)
 constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
@@ -88,8 +89,17 @@ struct Tc05Params {
     void *o;
     int64_t o_sb, o_st, o_sh;
     int *err;                            // device word set to CGDR_ERR_TIMEOUT if a wait gives up
+    int *status;                         // the caller's optional status word (the same code)
+    uint32_t polls;                      // polls of the main-loop waits (drains use kSpin)
+    int inject;                          // test hook: the first staging wait targets M_DEAD
     unsigned char *slots;                // cluster kernel: hand-off ring in the workspace (unused per head)
 };
+
+// Records a wait that gave up (one thread per CTA).
+__device__ __forceinline__ void record_timeout(const Tc05Params &p) {
+    atomicExch(p.err, (int)CGDR_ERR_TIMEOUT);
+    if (p.status != nullptr) atomicExch(p.status, (int)CGDR_ERR_TIMEOUT);
+}
 
 bool make_params(const cgdr_args &a, void *ws, Tc05Params &p);   // false if a tensor map cannot be encoded
 // Whether every input's strides can be described by a tensor map (host arithmetic only).
@@ -207,15 +217,18 @@ struct StageTrack {
     template <int PARTS>
     __device__ __forceinline__ void stage(const Tc05Params &p, const Head &hd, uint32_t sbase, int tn);
     // Waits for the staged rows of the next chunk (the oldest closed phase and this
-    // thread's beta copies); every thread calls it.  False if the wait gave up.
-    __device__ __forceinline__ bool wait(uint32_t sbase) {
-        const bool done = mbar_wait(sbase + M_STAGE, waited & 1u, kSpin);
+    // thread's beta copies); every thread calls it.  False if the wait gave up in any
+    // thread: the phase then still counts as not waited for, so that drain() waits for it.
+    __device__ __forceinline__ bool wait(uint32_t sbase, uint32_t polls, bool dead = false) {
+        const bool done = dead ? mbar_wait(sbase + M_DEAD, 0u, polls) : mbar_wait(sbase + M_STAGE, waited & 1u, polls);
         cp_async_wait_all();
-        ++waited;
-        return __syncthreads_or(!done) == 0;
+        const bool ok = __syncthreads_or(!done) == 0;
+        if (ok) ++waited;
+        return ok;
     }
-    // After a failure (thread 0): closes an open phase and gives the tiles of a phase that
-    // was not waited for a bounded chance to land before the CTA leaves.
+    // After a failure (thread 0): closes an open phase, then waits (full limit) for the one
+    // phase that can still be outstanding -- at most one is, closed or open -- so that no
+    // tile is still landing in this CTA's shared memory when it leaves.
     __device__ __forceinline__ void drain(uint32_t sbase) {
         if (half) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sbase + M_STAGE) : "memory");
         if (half || issued > waited) mbar_wait(sbase + M_STAGE, waited & 1u, kSpin);
@@ -233,15 +246,18 @@ __device__ __forceinline__ void StageTrack::stage(const Tc05Params &p, const Hea
     }
 }
 
-// The CTA's tensor-core completion barrier and the parity it waits for next.
+// The CTA's tensor-core completion barrier, the parity it waits for next and the polls of
+// that wait.
 struct MmaBar {
     uint32_t mbar;
     uint32_t phase;
+    uint32_t polls;
 };
 
-// Every thread waits (bounded) for the committed MMAs; false if any thread gave up.
+// Every thread waits (bounded) for the committed MMAs; false if any thread gave up.  The phase
+// advances either way, so after a failure the outstanding commit is phase ^ 1.
 __device__ __forceinline__ bool mma_wait(MmaBar &mb) {
-    const bool done = mbar_wait(mb.mbar, mb.phase, kSpin);
+    const bool done = mbar_wait(mb.mbar, mb.phase, mb.polls);
     mb.phase ^= 1u;
     const bool bad = __syncthreads_or(!done) != 0;
     fence_after_sync();

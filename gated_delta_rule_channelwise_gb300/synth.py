@@ -1,9 +1,13 @@
 """Seeded synthetic inputs for the channelwise gated delta rule.
 
-This module only draws random numbers and shapes them; it holds none of the
-method's arithmetic (no normalisation, no decay, no state update).  Both the
-GPU path and the CPU oracle consume exactly the tensors it returns (the
-oracle upcasts them exactly to fp64), so the two sides see identical inputs.
+This module only draws random numbers and shapes their distributions; it
+holds none of the method's arithmetic (no decay, no state update).  Where a
+workload states "q, k L2-normalised", q and k rows are drawn N(0,1), scaled to
+unit length in fp32 and then cast to the input dtype: that shapes the input
+distribution, and the library still L2-normalises them itself (idempotent up
+to eps and the cast).  Both the GPU path and the CPU oracle consume exactly the
+tensors it returns (the oracle upcasts them exactly to fp64), so the two sides
+see identical inputs.
 
 Workloads (named by what they are):
 
@@ -18,7 +22,9 @@ Workloads (named by what they are):
                    stronger decay g = -softplus(N(1,1)); then 64 decode steps
 =================  ===================================================================
 
-Distributions: q, k, v ~ N(0,1) (the library L2-normalises q and k itself);
+Distributions: q, k, v ~ N(0,1), with q and k rows scaled to unit length in
+fp32 before the cast (all but the packed fused-decode row, whose projection is
+raw; the library L2-normalises q and k itself either way);
 per-channel log-decay g = -softplus(N(mu,1)) * scale; beta = sigmoid(N(0,1));
 GatedDeltaNet gate inputs A_log ~ U(-1,1), dt_bias ~ N(0,1), a, b ~ N(0,1);
 initial state ~ 0.1 * N(0,1) (std 0.1).  Draw order per seed: S0, then
@@ -50,6 +56,7 @@ class Workload:
     s0_std: float = 0.1
     seed: int = 0
     tail_steps: int = 0    # decode steps that follow a prefill
+    qk_unit: bool = True   # q, k rows drawn at unit L2 length (fp32, before the cast); not for packed rows
 
     @property
     def torch_dtype(self):
@@ -106,8 +113,13 @@ def make_inputs(w: Workload, *, T: Optional[int] = None, B: Optional[int] = None
         out["k"] = qkv[..., nq:2 * nq].unflatten(-1, (w.Hk, w.dk))
         out["v"] = qkv[..., 2 * nq:].unflatten(-1, (w.Hv, w.dv))
     else:
-        out["q"] = randn(B, T, w.Hk, w.dk).to(dt)
-        out["k"] = randn(B, T, w.Hk, w.dk).to(dt)
+        def qk_rows():
+            x = randn(B, T, w.Hk, w.dk)
+            if w.qk_unit:
+                x = x / torch.linalg.vector_norm(x, dim=-1, keepdim=True).clamp_min(1e-12)
+            return x.to(dt)
+        out["q"] = qk_rows()
+        out["k"] = qk_rows()
         out["v"] = randn(B, T, w.Hv, w.dv).to(dt)
     if w.gate == "gdn":
         out["a"] = randn(B, T, w.Hv).to(dt)

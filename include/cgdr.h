@@ -38,10 +38,14 @@
  *  - No input may alias `state` or `o`.
  *
  * Ownership and threading: the caller owns every buffer and the stream.
- * The library allocates nothing, keeps no mutable global state, and is safe
- * to call from several host threads.  Calls are asynchronous on `stream`
- * (a cudaStream_t; NULL is the legacy default stream) and launch on the
- * calling thread's current device.
+ * The library allocates no device memory and keeps no mutable global state
+ * that changes results: the kernel choice travels in each call's argument
+ * block, and the only library-wide data are per-device caches of launch
+ * attributes and, for cgdr_prefill_noalloc, its static scratch area (calls of
+ * that entry point whose kernels overlap on the GPU race on it).  Calls are
+ * safe from several host threads, are asynchronous on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and launch on the calling
+ * thread's current device.
  *
  * Errors: arguments are checked on the host before any launch; a failing
  * check returns its code and launches nothing.  CGDR_ERR_CUDA reports a
@@ -58,7 +62,7 @@
 extern "C" {
 #endif
 
-#define CGDR_ABI_VERSION 1
+#define CGDR_ABI_VERSION 2
 
 typedef enum cgdr_status {
     CGDR_OK = 0,
@@ -67,7 +71,7 @@ typedef enum cgdr_status {
     CGDR_ERR_ALIGNMENT = 3,     /* misaligned pointer, stride or non-unit inner stride */
     CGDR_ERR_WORKSPACE = 4,     /* workspace smaller than cgdr_prefill_workspace_size() */
     CGDR_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
-    CGDR_ERR_TIMEOUT = 6        /* reserved: a bounded device-side wait gave up */
+    CGDR_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up (reported through a status word) */
 } cgdr_status;
 
 typedef enum cgdr_dtype { CGDR_F32 = 0, CGDR_BF16 = 1 } cgdr_dtype;
@@ -76,11 +80,19 @@ typedef enum cgdr_gate { CGDR_GATE_CHANNEL = 0, CGDR_GATE_GDN = 1 } cgdr_gate;
 /* One argument block for both calls.  Zero-initialise it, then fill in. */
 typedef struct cgdr_args {
     int32_t B, T, Hk, Hv, dk, dv;   /* dk, dv in {32, 64, 128}; T == 1 for decode */
-    int32_t dtype;                  /* cgdr_dtype of q, k, v, o (and a, b) */
+    int32_t dtype;                  /* cgdr_dtype of q, k, v (and a, b) */
     int32_t gate;                   /* cgdr_gate */
     int32_t l2norm_qk;              /* nonzero: L2-normalise q and k (the usual setting) */
     int32_t chunk;                  /* prefill chunk length 16, 32 or 64; 0 selects 64 */
     int32_t o_dtype;                /* cgdr_dtype of o; zero-initialised = CGDR_F32 */
+    int32_t prefill_path;           /* cgdr_prefill_path of this call; zero-initialised = automatic */
+    int32_t wait_polls;             /* polls before a bounded device wait on the kernel's own data
+                                       gives up; 0 selects 2^20.  A negative value is a test hook for
+                                       the failure path: the first such wait of every block is made
+                                       on a barrier that nothing completes and gives up after
+                                       -wait_polls polls.  After a wait gives up, copies still in
+                                       flight are waited for with the default limit before the
+                                       kernel exits */
     float q_scale;                  /* applied to q after the norm; <= 0 selects 1/sqrt(dk) */
     float eps;                      /* added to |x|^2 in the L2 norm; < 0 selects 1e-6 */
     const void *q;     int64_t q_sb, q_st, q_sh;        /* [B,T,Hk,dk] */
@@ -94,6 +106,10 @@ typedef struct cgdr_args {
     const float *dt_bias;                               /* [Hv]        (GDN) */
     float *state;                                       /* [B,Hv,dk,dv] in/out */
     void *o;           int64_t o_sb, o_st, o_sh;        /* [B,T,Hv,dv] out, o_dtype */
+    int32_t *status;   /* optional DEVICE int32: a kernel whose bounded wait gave up stores
+                          CGDR_ERR_TIMEOUT here (its outputs are then invalid).  The library never
+                          clears it: zero it before the calls it should cover.  NULL: not reported
+                          (the prefill workspace keeps its own status word either way) */
 } cgdr_args;
 
 /* ABI version of the loaded library (CGDR_ABI_VERSION it was built with). */
@@ -117,7 +133,11 @@ cgdr_status cgdr_validate(const cgdr_args *args, int for_prefill);
  * channelwise gated delta rule kernel": one pass forms S^T(exp(g) * kn) from
  * the state as read, the other decays, writes and accumulates o.  Each
  * state element is read once from and written once to HBM.
- * The token-stride fields (q_st, ...) are ignored.
+ * The token-stride fields (q_st, ...), chunk and prefill_path are ignored.
+ * A state tile whose copy into shared memory never completes (a bounded wait
+ * gives up) leaves that tile's state untouched, sets o of every (b, h) the
+ * affected block had not finished to NaN and stores CGDR_ERR_TIMEOUT in
+ * `status` when that is given.
  */
 cgdr_status cgdr_decode(const cgdr_args *args, void *stream);
 
@@ -146,7 +166,7 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
  * the chunk length plays no part); otherwise bf16 inputs with dk = dv = 128
  * and chunk 64 run one of the two tensor-core kernels (tcgen05, TF32
  * operands, fp32 accumulation and state), and every other case an fp32
- * CUDA-core kernel; cgdr_set_prefill_path can force a kernel.
+ * CUDA-core kernel; args->prefill_path can force a kernel for this call.
  * Workspace: the tensor-core path needs cgdr_prefill_workspace_size() bytes
  * (16-byte aligned); its first int32 is set to CGDR_ERR_TIMEOUT if a bounded
  * device wait gave up (see cgdr_workspace_status).  `workspace` may be NULL
@@ -176,19 +196,13 @@ typedef enum cgdr_prefill_path {
 } cgdr_prefill_path;
 
 /*
- * Process-wide kernel choice for later cgdr_prefill and cgdr_prefill_noalloc
- * calls (default CGDR_PREFILL_AUTO).  A tensor-core choice for a shape those
- * kernels do not cover runs the CUDA-core kernel.  Returns
- * CGDR_ERR_INVALID_ARG (and keeps the current choice) for any other value.
- */
-cgdr_status cgdr_set_prefill_path(int path);
-
-/*
- * The kernel cgdr_prefill would run for `args` on the current device under
- * the current choice: CGDR_PREFILL_PER_HEAD, CGDR_PREFILL_CLUSTER,
- * CGDR_PREFILL_SIMT or CGDR_PREFILL_RECURRENT; CGDR_PREFILL_AUTO (0) if `args` is invalid or there is
- * nothing to do (B == 0 or T == 0).  Queries the device once per device for
- * the cluster capacity.
+ * The kernel cgdr_prefill would run for `args` on the current device, given
+ * args->prefill_path: CGDR_PREFILL_PER_HEAD, CGDR_PREFILL_CLUSTER,
+ * CGDR_PREFILL_SIMT or CGDR_PREFILL_RECURRENT; CGDR_PREFILL_AUTO (0) if `args`
+ * is invalid or there is nothing to do (B == 0 or T == 0).  A forced
+ * tensor-core kernel applies only to the shapes it covers (else SIMT);
+ * RECURRENT applies only to 1 <= T <= 8 (else the automatic choice).  Queries
+ * the SM count and the cluster capacity once per device.
  */
 int cgdr_prefill_path_for(const cgdr_args *args);
 
@@ -224,8 +238,8 @@ cgdr_status cgdr_workspace_status(const void *workspace, void *stream);
  * the last call's contents; the call clears what must start at zero before
  * its kernel runs.  Calls whose kernels overlap on the GPU (other streams,
  * other host threads) race on the array: serialise them.  A device-side
- * wait that gives up is recorded only in the static area, so use cgdr_prefill
- * with a workspace when that status must be read back.
+ * wait that gives up is recorded in the static area, which the caller cannot
+ * read, and in args->status when that is given.
  *
  * Arguments and results are those of cgdr_prefill, except that a choice of
  * the cluster kernel (automatic or forced) runs the per-head tensor-core

@@ -30,7 +30,7 @@ def test_header_declares_the_abi():
     assert declared_functions() == sorted([
         "cgdr_abi_version", "cgdr_status_string", "cgdr_validate", "cgdr_decode",
         "cgdr_prefill_workspace_size", "cgdr_prefill", "cgdr_workspace_status", "cgdr_prefill_noalloc",
-        "cgdr_set_prefill_path", "cgdr_prefill_path_for"])
+        "cgdr_prefill_path_for"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -110,6 +110,9 @@ def test_validation_accepts_good_args(lib):
     (dict(v_st=12), True, cg.ERR_ALIGNMENT),
     (dict(g_sb=2), False, cg.ERR_ALIGNMENT),
     (dict(o_sb=-8), False, cg.ERR_ALIGNMENT),
+    (dict(prefill_path=5), True, cg.ERR_INVALID_ARG),
+    (dict(prefill_path=-1), True, cg.ERR_INVALID_ARG),
+    (dict(status=(9 << 20) + 2), False, cg.ERR_ALIGNMENT),
 ])
 def test_validation_rejects(lib, kw, prefill, code):
     A = _args(**kw)
@@ -143,6 +146,12 @@ def test_workspace_rules(lib):
     assert lib.cgdr_workspace_status(None, None) == cg.ERR_INVALID_ARG
 
 
+def test_wait_polls_values_are_accepted(lib):
+    # 0: default limit; > 0: that many polls; < 0: the injected-failure test hook
+    for polls in (0, 1, 1000, -1, -(1 << 31)):
+        assert cg.validate(_args(wait_polls=polls), False) == cg.OK
+
+
 def test_output_dtype_strides(lib):
     assert cg.validate(_args(o_dtype=cg.F32, o_sh=132), False) == cg.OK     # fp32 o: 4-element strides
     assert cg.validate(_args(o_dtype=cg.BF16, o_sh=136), False) == cg.OK
@@ -153,67 +162,78 @@ def test_token_strides_ignored_by_decode(lib):
 
 
 def test_prefill_path_choice(lib):
-    """Kernel selection is host logic: a forced tensor-core kernel applies only to the shapes it
-    covers (bf16, dk = dv = 128, chunk 64); unknown choices are rejected and change nothing."""
-    A = _args(T=100)
-    try:
-        assert lib.cgdr_set_prefill_path(5) == cg.ERR_INVALID_ARG
-        assert lib.cgdr_set_prefill_path(-1) == cg.ERR_INVALID_ARG
-        for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
-            assert lib.cgdr_set_prefill_path(path) == cg.OK
-            assert lib.cgdr_prefill_path_for(ctypes.byref(A)) == path
-            assert lib.cgdr_set_prefill_path(9) == cg.ERR_INVALID_ARG
-            assert lib.cgdr_prefill_path_for(ctypes.byref(A)) == path
-            for other in (_args(T=100, chunk=32), _args(T=100, dv=64),
-                          _args(T=100, dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128)):
-                assert lib.cgdr_prefill_path_for(ctypes.byref(other)) == cg.PREFILL_SIMT
-        # 1 <= T <= 8: the token recurrence under the automatic choice (or when forced); a forced
-        # chunked kernel still runs chunked; RECURRENT forced on a longer T means the automatic choice
-        assert lib.cgdr_set_prefill_path(cg.PREFILL_AUTO) == cg.OK
-        for T in (1, 2, 8):
-            for kw in ({}, dict(dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128), dict(dk=32, dv=64)):
-                assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=T, **kw))) == cg.PREFILL_RECURRENT
-            assert lib.cgdr_prefill_workspace_size(ctypes.byref(_args(T=T))) == 0
-        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=9))) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
-        assert lib.cgdr_set_prefill_path(cg.PREFILL_PER_HEAD) == cg.OK
-        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=2))) == cg.PREFILL_PER_HEAD
-        assert lib.cgdr_set_prefill_path(cg.PREFILL_RECURRENT) == cg.OK
-        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=3))) == cg.PREFILL_RECURRENT
-        assert lib.cgdr_prefill_path_for(ctypes.byref(A)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
-        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=0))) == cg.PREFILL_AUTO
-        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, dk=96))) == cg.PREFILL_AUTO
-        assert lib.cgdr_prefill_path_for(None) == cg.PREFILL_AUTO
-        # workspace by kernel: status word; status word + six hand-off slots per (batch, v-head)
-        assert lib.cgdr_set_prefill_path(cg.PREFILL_PER_HEAD) == cg.OK
-        assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 256
-        assert lib.cgdr_set_prefill_path(cg.PREFILL_CLUSTER) == cg.OK
-        need = 256 + A.B * A.Hv * 9 * 197120
-        assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == need
-        assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
-        assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(1 << 30), need - 16, None) == cg.ERR_WORKSPACE
-        assert lib.cgdr_set_prefill_path(cg.PREFILL_SIMT) == cg.OK
-        assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 0
-    finally:
-        lib.cgdr_set_prefill_path(cg.PREFILL_AUTO)
-    assert lib.cgdr_prefill_path_for(ctypes.byref(A)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
+    """Kernel selection is host logic, taken from the call's own argument block: a forced
+    tensor-core kernel applies only to the shapes it covers (bf16, dk = dv = 128, chunk 64);
+    out-of-range choices are rejected."""
+    path_for = lambda A: lib.cgdr_prefill_path_for(ctypes.byref(A))
+    for bad in (5, -1, 9):
+        assert path_for(_args(T=100, prefill_path=bad)) == cg.PREFILL_AUTO       # invalid arguments
+    for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
+        assert path_for(_args(T=100, prefill_path=path)) == path
+        for other in (dict(T=100, chunk=32), dict(T=100, dv=64),
+                      dict(T=100, dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128)):
+            assert path_for(_args(prefill_path=path, **other)) == cg.PREFILL_SIMT
+    # 1 <= T <= 8: the token recurrence under the automatic choice (or when forced); a forced
+    # chunked kernel still runs chunked; RECURRENT forced on a longer T means the automatic choice
+    for T in (1, 2, 8):
+        for kw in ({}, dict(dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128), dict(dk=32, dv=64)):
+            assert path_for(_args(T=T, **kw)) == cg.PREFILL_RECURRENT
+        assert lib.cgdr_prefill_workspace_size(ctypes.byref(_args(T=T))) == 0
+    assert path_for(_args(T=9)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
+    assert path_for(_args(T=2, prefill_path=cg.PREFILL_PER_HEAD)) == cg.PREFILL_PER_HEAD
+    assert path_for(_args(T=3, prefill_path=cg.PREFILL_RECURRENT)) == cg.PREFILL_RECURRENT
+    assert path_for(_args(T=100, prefill_path=cg.PREFILL_RECURRENT)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
+    assert path_for(_args(T=0)) == cg.PREFILL_AUTO
+    assert path_for(_args(T=100, dk=96)) == cg.PREFILL_AUTO
+    assert lib.cgdr_prefill_path_for(None) == cg.PREFILL_AUTO
+    # workspace by kernel: status word; status word + nine hand-off slots per (batch, v-head)
+    A = _args(T=100, prefill_path=cg.PREFILL_PER_HEAD)
+    assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 256
+    A = _args(T=100, prefill_path=cg.PREFILL_CLUSTER)
+    need = 256 + A.B * A.Hv * 9 * 197120
+    assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == need
+    assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
+    assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(1 << 30), need - 16, None) == cg.ERR_WORKSPACE
+    assert lib.cgdr_prefill_workspace_size(ctypes.byref(_args(T=100, prefill_path=cg.PREFILL_SIMT))) == 0
+
+
+def test_calls_from_two_threads_do_not_interfere(lib):
+    """The kernel choice lives in each call's argument block: two host threads asking for
+    different kernels (and their workspace sizes) at the same time each get their own answer."""
+    import threading
+    errors = []
+
+    def worker(path, expect_ws):
+        A = _args(T=100, prefill_path=path)
+        for _ in range(2000):
+            if lib.cgdr_prefill_path_for(ctypes.byref(A)) != path or \
+                    lib.cgdr_prefill_workspace_size(ctypes.byref(A)) != expect_ws:
+                errors.append(path)
+                return
+
+    ts = [threading.Thread(target=worker, args=(cg.PREFILL_PER_HEAD, 256)),
+          threading.Thread(target=worker, args=(cg.PREFILL_CLUSTER, 256 + 2 * 4 * 9 * 197120)),
+          threading.Thread(target=worker, args=(cg.PREFILL_SIMT, 0))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
 
 
 def test_tensor_maps_cover_strides_or_fall_back(lib):
     """The tensor-core prefill stages rows with TMA tensor maps; strides a map cannot take
     (a zero or negative stride over an extent above one, or one of 2^40 bytes or more) send
     the call to the CUDA-core kernel, and a dimension of extent one may carry any stride."""
-    A = _args(T=100)
-    try:
-        assert lib.cgdr_set_prefill_path(cg.PREFILL_PER_HEAD) == cg.OK
-        assert lib.cgdr_prefill_path_for(ctypes.byref(A)) == cg.PREFILL_PER_HEAD
-        # q heads sharing one row (head stride 0) with Hk = 2: valid input, no tensor map
-        assert cg.validate(_args(T=100, q_sh=0), True) == cg.OK
-        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, q_sh=0))) == cg.PREFILL_SIMT
-        # a batch stride of 2^40 bytes and more (bf16: 2^39 elements)
-        assert lib.cgdr_prefill_path_for(ctypes.byref(_args(T=100, k_sb=1 << 39))) == cg.PREFILL_SIMT
-        # extent-one dimensions: their strides never step, so any value is fine
-        one = dict(T=100, B=1, Hk=1, Hv=1)
-        for kw in (dict(q_sh=0, k_sh=0, v_sh=0, g_sh=0), dict(q_sb=0, k_sb=0, v_sb=0, g_sb=0)):
-            assert lib.cgdr_prefill_path_for(ctypes.byref(_args(**one, **kw))) == cg.PREFILL_PER_HEAD
-    finally:
-        lib.cgdr_set_prefill_path(cg.PREFILL_AUTO)
+    P = cg.PREFILL_PER_HEAD
+    path_for = lambda **kw: lib.cgdr_prefill_path_for(ctypes.byref(_args(prefill_path=P, **kw)))
+    assert path_for(T=100) == P
+    # q heads sharing one row (head stride 0) with Hk = 2: valid input, no tensor map
+    assert cg.validate(_args(T=100, q_sh=0), True) == cg.OK
+    assert path_for(T=100, q_sh=0) == cg.PREFILL_SIMT
+    # a batch stride of 2^40 bytes and more (bf16: 2^39 elements)
+    assert path_for(T=100, k_sb=1 << 39) == cg.PREFILL_SIMT
+    # extent-one dimensions: their strides never step, so any value is fine
+    one = dict(T=100, B=1, Hk=1, Hv=1)
+    for kw in (dict(q_sh=0, k_sh=0, v_sh=0, g_sh=0), dict(q_sb=0, k_sb=0, v_sb=0, g_sb=0)):
+        assert path_for(**one, **kw) == P

@@ -60,6 +60,37 @@ def test_gdn_packed_decode_b1_full():
     _run_and_compare(w, w.T, inp=inp)
 
 
+def test_gdn_decode_b1_cuda_graph_sequence():
+    """The fused decode at B=1 as the benchmark times it: 256 consecutive steps captured once
+    as a CUDA graph and replayed from the initial state (the kernel-count reduction of "Add
+    fused GatedDeltaNet decode Triton kernel", description).  Every step's o and the final
+    state are checked against the oracle."""
+    w = WORKLOADS["gdn_decode_b1"]
+    inp = make_inputs(w, device="cuda")
+    st = inp["S0"].clone()
+    o = torch.empty(w.T, 1, w.Hv, w.dv, dtype=torch.float32, device="cuda")
+
+    def steps():
+        for t in range(w.T):
+            cg.decode(inp["q"][:, t], inp["k"][:, t], inp["v"][:, t], st, o[t], a=inp["a"][:, t], b=inp["b"][:, t],
+                      A_log=inp["A_log"], dt_bias=inp["dt_bias"])
+
+    steps()                                   # eager first: per-device set-up happens outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        steps()
+    st.copy_(inp["S0"])
+    o.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle_run(inp, rep=w.Hv // w.Hk)
+    got_o = o.permute(1, 0, 2, 3)             # [1, 256, 32, 128]
+    eo, es = rel_err(got_o, o_ref), rel_err(st, S_ref)
+    print("[parity] gdn_decode_b1 graph err_o=%.3e err_S=%.3e" % (eo, es))
+    assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
+
+
 def test_decode_b64_full_size_sampled():
     """B=64, H=32, 128 steps on the GPU; the oracle checks 24 sampled (b, h) units."""
     w = WORKLOADS["decode_b64"]

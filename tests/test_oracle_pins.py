@@ -203,6 +203,39 @@ def test_gdn_gate_special_points():
     np.testing.assert_allclose(S, Sc, rtol=1e-12, atol=1e-13)
 
 
+def test_gdn_gate_generic_points():
+    """The scalar gate at points that are not symmetric, so that a flipped sigmoid or a
+    softplus of the negated argument fails ("Add fused GatedDeltaNet decode Triton kernel",
+    description, gating: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)).
+
+    b = ln 3 gives beta = 3/4 exactly (1/(1+e^b) would give 1/4); a + dt_bias = ln(e - 1)
+    gives softplus = 1 (softplus(-x) there is 1 - ln(e - 1) = 0.459), so g = -e^A_log; with
+    A_log = 0.7 and -0.4 the factor e^A_log is not 1.  The result must equal the channel
+    gate with those closed-form g and beta broadcast over dk.
+    """
+    B, T, Hk, Hv, dk, dv = 1, 5, 1, 2, 4, 3
+    r = np.random.default_rng(17)
+    q = r.standard_normal((B, T, Hk, dk))
+    k = r.standard_normal((B, T, Hk, dk))
+    v = r.standard_normal((B, T, Hv, dv))
+    S0 = r.standard_normal((B, Hv, dk, dv))
+    A_log = np.array([0.7, -0.4])
+    dt_bias = np.array([0.25, -1.5])
+    a = np.tile(math.log(math.e - 1.0) - dt_bias, (B, T, 1))
+    b = np.full((B, T, Hv), math.log(3.0))
+    o, S = oracle.recurrence(q, k, v, a=a, b=b, A_log=A_log, dt_bias=dt_bias, S0=S0)
+    g = np.broadcast_to((-np.exp(A_log))[None, None, :, None], (B, T, Hv, dk)).copy()
+    oc, Sc = oracle.recurrence(q, k, v, g=g, beta=np.full((B, T, Hv), 0.75), S0=S0)
+    np.testing.assert_allclose(o, oc, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S, Sc, rtol=1e-12, atol=1e-13)
+    # the flipped readings give a different result on this case (the pin can fail)
+    of, _ = oracle.recurrence(q, k, v, g=g, beta=np.full((B, T, Hv), 0.25), S0=S0)
+    gs = np.broadcast_to((-np.exp(A_log) * (1.0 - math.log(math.e - 1.0)))[None, None, :, None],
+                         (B, T, Hv, dk)).copy()
+    os_, _ = oracle.recurrence(q, k, v, g=gs, beta=np.full((B, T, Hv), 0.75), S0=S0)
+    assert np.max(np.abs(of - o)) > 1e-3 and np.max(np.abs(os_ - o)) > 1e-3
+
+
 def test_gdn_chunkwise_equals_recurrence():
     r = np.random.default_rng(9)
     B, T, Hk, Hv, dk, dv = 1, 13, 2, 4, 4, 3

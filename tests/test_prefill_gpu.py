@@ -28,28 +28,25 @@ TC_PATHS = [pytest.param(cg.PREFILL_PER_HEAD, id="per_head"), pytest.param(cg.PR
 
 @pytest.fixture(params=TC_PATHS)
 def tc_path(request):
-    """Runs the test once per tensor-core prefill kernel (restores automatic choice after)."""
-    cg.set_prefill_path(request.param)
-    yield request.param
-    cg.set_prefill_path(cg.PREFILL_AUTO)
+    """Runs the test once per tensor-core prefill kernel (the choice is passed with each call)."""
+    return request.param
 
 
 @pytest.fixture
 def simt_path():
-    """Forces the chunked CUDA-core kernel (a small T would otherwise run the token recurrence)."""
-    cg.set_prefill_path(cg.PREFILL_SIMT)
-    yield cg.PREFILL_SIMT
-    cg.set_prefill_path(cg.PREFILL_AUTO)
+    """The chunked CUDA-core kernel (a small T would otherwise run the token recurrence)."""
+    return cg.PREFILL_SIMT
 
 
-def _expect_path(inp, path):
+def _expect_path(inp, expected, path=cg.PREFILL_AUTO):
     o = torch.empty(inp["v"].shape, device=inp["v"].device)
-    assert cg.prefill_path_for(inp["q"], inp["k"], inp["v"], inp["S0"], o, chunk=64, **gate_kwargs(inp)) == path
+    got = cg.prefill_path_for(inp["q"], inp["k"], inp["v"], inp["S0"], o, chunk=64, path=path, **gate_kwargs(inp))
+    assert got == expected
 
 
-def _prefill(inp, chunk, state=None, **kw):
+def _prefill(inp, chunk, state=None, path=cg.PREFILL_AUTO, **kw):
     state = inp["S0"].clone() if state is None else state
-    o = cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=chunk, **gate_kwargs(inp), **kw)
+    o = cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=chunk, path=path, **gate_kwargs(inp), **kw)
     torch.cuda.synchronize()
     return o, state
 
@@ -81,8 +78,8 @@ def test_tiny_f32_chunk16():
 def test_fp32_chunk_sizes_and_tails(chunk, T, dk, dv, simt_path):
     w = Workload("f32", B=2, Hk=1, Hv=2, dk=dk, dv=dv, T=T, dtype="f32", gate="channel", seed=T + chunk)
     inp = make_inputs(w, device="cuda")
-    _expect_path(inp, cg.PREFILL_SIMT)
-    o, s = _prefill(inp, chunk)
+    _expect_path(inp, cg.PREFILL_SIMT, simt_path)
+    o, s = _prefill(inp, chunk, path=simt_path)
     _check(w, inp, o, s)
 
 
@@ -94,8 +91,8 @@ def test_tensor_core_path_tails(T, dv, gate, tc_path):
         pytest.skip("dv < 128 runs the CUDA-core kernel whatever the choice")
     w = Workload("tc", B=2, Hk=1, Hv=2, dk=128, dv=dv, T=T, dtype="bf16", gate=gate, seed=T * 3 + dv)
     inp = make_inputs(w, device="cuda")
-    _expect_path(inp, tc_path if dv == 128 else cg.PREFILL_SIMT)
-    o, s = _prefill(inp, 64)
+    _expect_path(inp, tc_path if dv == 128 else cg.PREFILL_SIMT, tc_path)
+    o, s = _prefill(inp, 64, path=tc_path)
     _check(w, inp, o, s)
 
 
@@ -115,14 +112,14 @@ def test_strong_decay_anchoring(tc_path):
     w = Workload("strong", B=1, Hk=2, Hv=2, dk=128, dv=128, T=300, dtype="bf16", gate="channel",
                  g_mu=3.0, g_scale=1.0, seed=77)
     inp = make_inputs(w, device="cuda")
-    o, s = _prefill(inp, 64)
+    o, s = _prefill(inp, 64, path=tc_path)
     _check(w, inp, o, s)
 
 
 def test_head_repeat_prefill(tc_path):
     w = Workload("rep", B=2, Hk=2, Hv=8, dk=128, dv=128, T=90, dtype="bf16", gate="channel", seed=3)
     inp = make_inputs(w, device="cuda")
-    o, s = _prefill(inp, 64)
+    o, s = _prefill(inp, 64, path=tc_path)
     _check(w, inp, o, s)
 
 
@@ -130,8 +127,8 @@ def test_prefill_t4000_full(tc_path):
     """B=1, H=32, dk=dv=128, T=4000, chunk 64 (ragged 32), zero initial state: every unit checked."""
     w = WORKLOADS["prefill_t4000"]
     inp = make_inputs(w, device="cuda")
-    _expect_path(inp, tc_path)
-    o, s = _prefill(inp, 64)
+    _expect_path(inp, tc_path, tc_path)
+    o, s = _prefill(inp, 64, path=tc_path)
     _check(w, inp, o, s)
 
 
@@ -140,7 +137,7 @@ def test_prefill_long_then_decode_sampled(tc_path):
     Eight sampled (b, h) units are checked against the oracle over all T + 64 tokens."""
     w = WORKLOADS["prefill_long"]
     inp = make_inputs(w, device="cuda")
-    o, s = _prefill(inp, 64)
+    o, s = _prefill(inp, 64, path=tc_path)
     units = [(0, 0), (0, 31), (1, 7), (2, 16), (3, 3), (3, 30), (1, 22), (2, 9)]
     tail = make_inputs(w, T=w.tail_steps, device="cuda", seed=w.seed + 1)
     o_tail = decode_steps(cg, tail, w.tail_steps, s)
@@ -177,8 +174,8 @@ def test_prefill_continuation(tc_path):
     inp = make_inputs(w, device="cuda")
     first = {k: (v[:, :100] if v.dim() >= 2 and v.shape[1] == 230 else v) for k, v in inp.items()}
     second = {k: (v[:, 100:] if v.dim() >= 2 and v.shape[1] == 230 else v) for k, v in inp.items()}
-    o1, s = _prefill(first, 64)
-    o2, s = _prefill(second, 64, state=s)
+    o1, s = _prefill(first, 64, path=tc_path)
+    o2, s = _prefill(second, 64, state=s, path=tc_path)
     _check(w, inp, torch.cat([o1, o2], dim=1), s)
 
 
@@ -194,10 +191,10 @@ def test_zero_length_is_noop():
 def test_bf16_output_is_the_rounded_fp32_output(dtype, chunk, tc_path):
     w = Workload("obf", B=1, Hk=2, Hv=2, dk=128, dv=128, T=77, dtype=dtype, gate="channel", seed=23)
     inp = make_inputs(w, device="cuda")
-    o32, s1 = _prefill(inp, chunk)
+    o32, s1 = _prefill(inp, chunk, path=tc_path)
     o16 = torch.empty(o32.shape, dtype=torch.bfloat16, device="cuda")
     s2 = inp["S0"].clone()
-    cg.prefill(inp["q"], inp["k"], inp["v"], s2, o16, chunk=chunk, **gate_kwargs(inp))
+    cg.prefill(inp["q"], inp["k"], inp["v"], s2, o16, chunk=chunk, path=tc_path, **gate_kwargs(inp))
     torch.cuda.synchronize()
     assert torch.equal(s1, s2)
     assert torch.equal(o16, o32.to(torch.bfloat16))
@@ -209,10 +206,10 @@ def test_tensor_core_path_reports_ok_status(tc_path):
     inp = make_inputs(w, device="cuda")
     state = inp["S0"].clone()
     n = cg.prefill_workspace_size(inp["q"], inp["k"], inp["v"], state, torch.empty(inp["v"].shape, device="cuda"),
-                                  **gate_kwargs(inp))
+                                  path=tc_path, **gate_kwargs(inp))
     assert n == (256 if tc_path == cg.PREFILL_PER_HEAD else 256 + 9 * 197120)   # + hand-off slots
     ws = torch.full((n,), 0x7F, dtype=torch.uint8, device="cuda")
-    cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, workspace=ws, **gate_kwargs(inp))
+    cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=tc_path, workspace=ws, **gate_kwargs(inp))
     assert cg.workspace_status(ws) == cg.OK
 
 
@@ -223,7 +220,7 @@ def test_mixed_wide_and_narrow_chunks(tc_path):
     g = inp["g"].clone()
     g[:, 64:128] *= 12.0          # second chunk: ~ -5 per token on average
     inp["g"] = g
-    o, s = _prefill(inp, 64)
+    o, s = _prefill(inp, 64, path=tc_path)
     _check(w, inp, o, s)
 
 
@@ -233,13 +230,7 @@ def test_both_tensor_core_kernels_agree():
     inside the oracle tolerance (on GB300 they agree exactly)."""
     w = Workload("agree", B=1, Hk=2, Hv=4, dk=128, dv=128, T=700, dtype="bf16", gate="channel", seed=55)
     inp = make_inputs(w, device="cuda")
-    outs = []
-    try:
-        for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER):
-            cg.set_prefill_path(path)
-            outs.append(_prefill(inp, 64))
-    finally:
-        cg.set_prefill_path(cg.PREFILL_AUTO)
+    outs = [_prefill(inp, 64, path=path) for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)]
     (o1, s1), (o2, s2) = outs
     eo, es = rel_err(o2, o1.double().cpu().numpy()), rel_err(s2, s1.double().cpu().numpy())
     print("[kernels] o %.3e S %.3e" % (eo, es))
@@ -271,15 +262,11 @@ def test_recurrent_matches_chunked_kernels():
     w = Workload("rec8", B=2, Hk=2, Hv=2, dk=128, dv=128, T=8, dtype="bf16", gate="channel", seed=77)
     inp = make_inputs(w, device="cuda")
     o_r, s_r = _prefill(inp, 64)
-    try:
-        for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
-            cg.set_prefill_path(path)
-            _expect_path(inp, path)
-            o_c, s_c = _prefill(inp, 64)
-            assert rel_err(o_c, o_r.double().cpu().numpy()) <= 2e-2
-            assert rel_err(s_c, s_r.double().cpu().numpy()) <= 2e-2
-    finally:
-        cg.set_prefill_path(cg.PREFILL_AUTO)
+    for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
+        _expect_path(inp, path, path)
+        o_c, s_c = _prefill(inp, 64, path=path)
+        assert rel_err(o_c, o_r.double().cpu().numpy()) <= 2e-2
+        assert rel_err(s_c, s_r.double().cpu().numpy()) <= 2e-2
 
 
 @pytest.mark.parametrize("T", [5, 200])
@@ -290,7 +277,7 @@ def test_packed_gdn_prefill(T, tc_path):
     w = Workload("pk", B=2, Hk=16, Hv=32, dk=128, dv=128, T=T, dtype="bf16", gate="gdn", packed=True, seed=90 + T)
     inp = make_inputs(w, device="cuda")
     assert inp["q"].stride(1) == 16 * 128 * 2 + 32 * 128          # a view into the packed row
-    o, s = _prefill(inp, 64)
+    o, s = _prefill(inp, 64, path=tc_path)
     _check(w, inp, o, s, units=[(0, 0), (0, 1), (1, 17), (1, 31)])
 
 
