@@ -204,9 +204,11 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
         sc0 = sc1;
         sc1 = scalars(u0 + (k + 2) * G);
 
+        // thread 0 polls the tile's barrier; the other warps sleep at the barrier below, which
+        // carries the outcome and orders the tile's bytes before their reads
         const bool dead = p.inject && k == 0;
-        const bool got = mbar_wait_parity(dead ? mbar0 + 8 * NS : mbar0 + 8 * st,
-                                          dead ? 0u : (uint32_t)((k / NS) & 1), p.polls);
+        const bool got = tid != 0 || mbar_wait_parity(dead ? mbar0 + 8 * NS : mbar0 + 8 * st,
+                                                      dead ? 0u : (uint32_t)((k / NS) & 1), p.polls);
         cp_async_wait_groups<NS - 1>();
         const int b = u / p.Hv, h = u % p.Hv;
         if (__syncthreads_or(!got)) {

@@ -197,7 +197,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     for (int c = 0; c < n; ++c) {
         // ---------------------------------------------------------- inbox A: Qg, Kg^T, V^T, Tb, e^gC
         {
-            const bool done = cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1), p.polls);
+            const bool done = tid != 0 || cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1), p.polls);
             if (__syncthreads_or(!done)) return false;
         }
         {
@@ -268,7 +268,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         fence_before_sync();
         // ---------------------------------------------------------- inbox B: [Kend^T; P]
         {
-            const bool done = cl_wait(sbase + CH_FULL_B, (uint32_t)(c & 1), p.polls);
+            const bool done = tid != 0 || cl_wait(sbase + CH_FULL_B, (uint32_t)(c & 1), p.polls);
             if (__syncthreads_or(!done)) return false;
         }
         if (tid == 0) {

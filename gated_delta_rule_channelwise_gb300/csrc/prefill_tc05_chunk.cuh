@@ -219,8 +219,13 @@ struct StageTrack {
     // Waits for the staged rows of the next chunk (the oldest closed phase and this
     // thread's beta copies); every thread calls it.  False if the wait gave up in any
     // thread: the phase then still counts as not waited for, so that drain() waits for it.
+    // Thread 0 polls the barrier; the other warps sleep at the CTA barrier that carries the
+    // outcome (the tiles' writes, acquired by thread 0, are ordered before every thread's reads
+    // by that barrier).
     __device__ __forceinline__ bool wait(uint32_t sbase, uint32_t polls, bool dead = false) {
-        const bool done = dead ? mbar_wait(sbase + M_DEAD, 0u, polls) : mbar_wait(sbase + M_STAGE, waited & 1u, polls);
+        bool done = true;
+        if (threadIdx.x == 0)
+            done = dead ? mbar_wait(sbase + M_DEAD, 0u, polls) : mbar_wait(sbase + M_STAGE, waited & 1u, polls);
         cp_async_wait_all();
         const bool ok = __syncthreads_or(!done) == 0;
         if (ok) ++waited;
@@ -254,10 +259,13 @@ struct MmaBar {
     uint32_t polls;
 };
 
-// Every thread waits (bounded) for the committed MMAs; false if any thread gave up.  The phase
-// advances either way, so after a failure the outstanding commit is phase ^ 1.
+// Waits (bounded) for the committed MMAs: thread 0 polls, the other warps sleep at the CTA
+// barrier that carries the outcome, then every thread fences its later tensor-memory accesses
+// after it.  False if the wait gave up.  The phase advances either way, so after a failure
+// the outstanding commit is phase ^ 1.
 __device__ __forceinline__ bool mma_wait(MmaBar &mb) {
-    const bool done = mbar_wait(mb.mbar, mb.phase, mb.polls);
+    bool done = true;
+    if (threadIdx.x == 0) done = mbar_wait(mb.mbar, mb.phase, mb.polls);
     mb.phase ^= 1u;
     const bool bad = __syncthreads_or(!done) != 0;
     fence_after_sync();

@@ -50,15 +50,19 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b
 }
 
 // D[128 x N] (+)= A[128 x K] * B[N x K]^T; A and B are K-major swizzled tiles
-// with 128 and N rows.  Issued by one thread.
+// with 128 and N rows.  Issued by one thread.  The descriptors are built once: a byte offset
+// o (a multiple of 16) moves a descriptor's start-address field by o / 16, and shared
+// addresses stay below 2^18, so the field never carries into the next one.
 template <int N, int K>
 __device__ __forceinline__ void gemm(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, bool accumulate) {
     constexpr uint32_t idesc = idesc_tf32(N);
+    const uint64_t ad = smem_desc(a_smem), bd = smem_desc(b_smem);
 #pragma unroll
     for (int ks = 0; ks < K / 8; ++ks) {
-        const uint32_t aoff = (uint32_t)((ks >> 2) * 128 * 128 + (ks & 3) * 32);
-        const uint32_t boff = (uint32_t)((ks >> 2) * N * 128 + (ks & 3) * 32);
-        mma_tf32(d_tmem, smem_desc(a_smem + aoff), smem_desc(b_smem + boff), idesc, (accumulate || ks > 0) ? 1u : 0u);
+        constexpr int kAStep = 128 * 128 / 16, kBStep = N * 128 / 16;
+        const uint64_t a = ad + (uint64_t)((ks >> 2) * kAStep + (ks & 3) * 2);
+        const uint64_t b = bd + (uint64_t)((ks >> 2) * kBStep + (ks & 3) * 2);
+        mma_tf32(d_tmem, a, b, idesc, (accumulate || ks > 0) ? 1u : 0u);
     }
 }
 
@@ -74,10 +78,11 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 template <int N, int K>
 __device__ __forceinline__ void gemm_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
     constexpr uint32_t idesc = idesc_tf32(N);
+    const uint64_t bd = smem_desc(b_smem);
 #pragma unroll
     for (int ks = 0; ks < K / 8; ++ks) {
-        const uint32_t boff = (uint32_t)((ks >> 2) * N * 128 + (ks & 3) * 32);
-        mma_tf32_ts(d_tmem, a_tmem + 8 * ks, smem_desc(b_smem + boff), idesc, (accumulate || ks > 0) ? 1u : 0u);
+        const uint64_t b = bd + (uint64_t)((ks >> 2) * (N * 128 / 16) + (ks & 3) * 2);
+        mma_tf32_ts(d_tmem, a_tmem + 8 * ks, b, idesc, (accumulate || ks > 0) ? 1u : 0u);
     }
 }
 
