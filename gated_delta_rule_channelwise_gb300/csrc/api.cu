@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "cgdr_internal.cuh"
+#include "cgdr_debug.h"
 
 namespace {
 
@@ -80,6 +81,37 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+namespace {
+int64_t footprint(const void *p, int64_t B, int64_t T, int64_t H, int64_t d, int64_t sb, int64_t st, int64_t sh) {
+    if (p == nullptr || B <= 0 || T <= 0 || H <= 0) return 0;
+    return (B - 1) * sb + (T - 1) * st + (H - 1) * sh + d;
+}
+}  // namespace
+
+// Debug builds: elements taken off o's footprint for the current thread's call (the test entry
+// point of cgdr_debug.h sets it around one call; thread-local, so other threads are unaffected).
+thread_local int64_t t_debug_o_shrink = 0;
+
+Extents extents_of(const cgdr_args &a, bool prefill, size_t ws_bytes) {
+    const int64_t T = prefill ? a.T : 1;
+    Extents e;
+    e.q = footprint(a.q, a.B, T, a.Hk, a.dk, a.q_sb, a.q_st, a.q_sh);
+    e.k = footprint(a.k, a.B, T, a.Hk, a.dk, a.k_sb, a.k_st, a.k_sh);
+    e.v = footprint(a.v, a.B, T, a.Hv, a.dv, a.v_sb, a.v_st, a.v_sh);
+    e.o = footprint(a.o, a.B, T, a.Hv, a.dv, a.o_sb, a.o_st, a.o_sh);
+    const bool chan = a.gate == CGDR_GATE_CHANNEL;
+    e.g = chan ? footprint(a.g, a.B, T, a.Hv, a.dk, a.g_sb, a.g_st, a.g_sh) : 0;
+    e.beta = chan ? footprint(a.beta, a.B, T, a.Hv, 1, a.beta_sb, a.beta_st, a.beta_sh) : 0;
+    e.a = chan ? 0 : footprint(a.a, a.B, T, a.Hv, 1, a.a_sb, a.a_st, a.a_sh);
+    e.b = chan ? 0 : footprint(a.b, a.B, T, a.Hv, 1, a.b_sb, a.b_st, a.b_sh);
+    e.A_log = chan || a.A_log == nullptr ? 0 : a.Hv;
+    e.dt_bias = chan || a.dt_bias == nullptr ? 0 : a.Hv;
+    e.state = a.state == nullptr ? 0 : (int64_t)a.B * a.Hv * a.dk * a.dv;
+    e.ws = (int64_t)ws_bytes;
+    e.o -= t_debug_o_shrink;
+    return e;
+}
+
 int current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
@@ -146,7 +178,8 @@ cgdr_status prefill_dispatch(const cgdr_args &a, int path, void *ws, size_t ws_b
     if (path == CGDR_PREFILL_SIMT) return launch_prefill_simt(a, s);
     const size_t need = prefill_workspace_for(a, path);
     if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
-    const cgdr_status st = path == CGDR_PREFILL_CLUSTER ? launch_prefill_cluster(a, ws, s) : launch_prefill_tc05(a, ws, s);
+    const cgdr_status st = path == CGDR_PREFILL_CLUSTER ? launch_prefill_cluster(a, ws, ws_bytes, s)
+                                                        : launch_prefill_tc05(a, ws, ws_bytes, s);
     // the driver's tensor-map encoder refused a tensor that the host check accepted: CUDA-core kernel
     return st == CGDR_ERR_ALIGNMENT ? launch_prefill_simt(a, s) : st;
 }
@@ -166,6 +199,7 @@ const char *cgdr_status_string(int s) {
         case CGDR_ERR_WORKSPACE: return "CGDR_ERR_WORKSPACE: workspace too small";
         case CGDR_ERR_CUDA: return "CGDR_ERR_CUDA: a CUDA call or kernel launch failed";
         case CGDR_ERR_TIMEOUT: return "CGDR_ERR_TIMEOUT: a bounded device wait gave up";
+        case CGDR_ERR_BOUNDS: return "CGDR_ERR_BOUNDS: a debug build's device index check failed";
         default: return "unknown cgdr status";
     }
 }
@@ -192,6 +226,18 @@ cgdr_status cgdr_prefill(const cgdr_args *a, void *ws, size_t ws_bytes, void *st
     cgdr_status st = check(a, true);
     if (st != CGDR_OK || a->B == 0 || a->T == 0) return st;
     return cgdr::prefill_dispatch(*a, cgdr::prefill_path(*a, true), ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+cgdr_status cgdr_debug_decode_shrunk_o(const cgdr_args *a, int64_t o_shrink, void *stream) {
+#ifdef CGDR_DEBUG_CHECKS
+    cgdr::t_debug_o_shrink = o_shrink;
+    const cgdr_status st = cgdr_decode(a, stream);
+    cgdr::t_debug_o_shrink = 0;
+    return st;
+#else
+    (void)a; (void)o_shrink; (void)stream;
+    return CGDR_ERR_UNSUPPORTED;
+#endif
 }
 
 cgdr_status cgdr_workspace_status(const void *ws, void *stream) {

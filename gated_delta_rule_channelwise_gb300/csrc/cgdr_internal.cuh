@@ -33,6 +33,14 @@ inline uint32_t polls_of(const cgdr_args &a) {
 // Test hook: the first main-loop wait of every block waits on a barrier nothing completes.
 inline int inject_of(const cgdr_args &a) { return a.wait_polls < 0 ? 1 : 0; }
 
+// Element counts of each tensor's footprint ((B-1) sb + (T-1) st + (H-1) sh + d for a strided
+// [B,T,H,d] view; 0 for an absent tensor) and the workspace bytes.  Kernels built with
+// CGDR_DEBUG_CHECKS test every global access against them.
+struct Extents {
+    int64_t q, k, v, g, beta, a, b, o, state, A_log, dt_bias, ws;
+};
+Extents extents_of(const cgdr_args &a, bool prefill, size_t ws_bytes);
+
 cgdr_status launch_decode(const cgdr_args &a, cudaStream_t s);
 // Prefill with 1 <= T <= kRecurrentMaxT: the decode kernel stepping through the tokens.
 constexpr int kRecurrentMaxT = 8;
@@ -40,7 +48,7 @@ cgdr_status launch_recurrent(const cgdr_args &a, cudaStream_t s);
 cgdr_status launch_prefill_simt(const cgdr_args &a, cudaStream_t s);
 bool prefill_tc05_supported(const cgdr_args &a);
 size_t prefill_tc05_workspace(const cgdr_args &a);
-cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s);
+cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
 int prefill_cluster_capacity();
 size_t prefill_cluster_workspace(const cgdr_args &a);
 // The prefill kernel for `a` given a.prefill_path (CGDR_PREFILL_PER_HEAD, _CLUSTER, _SIMT or
@@ -49,7 +57,7 @@ int prefill_path(const cgdr_args &a, bool allow_cluster);
 size_t prefill_workspace_for(const cgdr_args &a, int path);
 // Runs the kernel `path` (as prefill_path returned it) with the given workspace.
 cgdr_status prefill_dispatch(const cgdr_args &a, int path, void *ws, size_t ws_bytes, cudaStream_t s);
-cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s);
+cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
 
 // The driver's tiled tensor-map encoder, looked up once through the runtime (nullptr if
 // the driver does not provide it).
@@ -62,6 +70,25 @@ inline float qscale_of(const cgdr_args &a) {
 inline int chunk_of(const cgdr_args &a) { return a.chunk == 0 ? 64 : a.chunk; }
 
 // ---------------------------------------------------------------- device side
+// Debug builds (CGDR_DEBUG_CHECKS): `off` must lie in [0, n); a failed check stores
+// CGDR_ERR_BOUNDS in the given status words (either may be null) and the caller skips the
+// access.  Release builds: always true, no code.
+__device__ __forceinline__ bool in_bounds(int64_t off, int64_t n, int *st0, int *st1) {
+#ifdef CGDR_DEBUG_CHECKS
+    if (off >= 0 && off < n) return true;
+    if (st0 != nullptr) atomicExch(st0, (int)CGDR_ERR_BOUNDS);
+    if (st1 != nullptr) atomicExch(st1, (int)CGDR_ERR_BOUNDS);
+    return false;
+#else
+    (void)off; (void)n; (void)st0; (void)st1;
+    return true;
+#endif
+}
+// Both ends of an access of `count` elements starting at `off`.
+__device__ __forceinline__ bool range_in_bounds(int64_t off, int64_t count, int64_t n, int *st0, int *st1) {
+    return in_bounds(off, n, st0, st1) && in_bounds(off + count - 1, n, st0, st1);
+}
+
 template <typename T> struct Cvt;
 template <> struct Cvt<float> {
     static __device__ __forceinline__ float to_f(float x) { return x; }

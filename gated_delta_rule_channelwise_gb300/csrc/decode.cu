@@ -41,6 +41,7 @@ struct DecodeParams {
     int *status;                                      // optional: CGDR_ERR_TIMEOUT if a wait gave up
     uint32_t polls;                                   // polls of the main-loop tile waits
     int inject;                                       // test hook: the first tile wait targets a dead barrier
+    Extents ext;                                      // footprints for the index checks of a debug build
 };
 
 template <int DK, int DV>
@@ -149,26 +150,34 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
         if (u < units) {
             const int b = u / p.Hv, h = u % p.Hv, hk = h / (p.Hv / p.Hk);
             const uint32_t base = sb + st * Ps::STAGE;
-            if (tid == 0) bulk_g2s(base, p.state + (size_t)u * DK * DV, Ps::TILE, mbar0 + 8 * st);
+            if (tid == 0) {
+                if (range_in_bounds((int64_t)u * DK * DV, DK * DV, p.ext.state, p.status, nullptr))
+                    bulk_g2s(base, p.state + (size_t)u * DK * DV, Ps::TILE, mbar0 + 8 * st);
+                else   // (debug build) a tile outside the state: no copy, the stage's phase still completes
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar0 + 8 * st) : "memory");
+            }
             constexpr int nq = Ps::ROWQ / 16, nv = Ps::ROWV / 16, ng = Ps::ROWG / 16;
+            constexpr int eq = 16 / (int)sizeof(T);                  // elements per 16-byte piece (q, k, v)
             const int per = 2 * nq + nv + (p.gate == CGDR_GATE_CHANNEL ? ng : 0);   // 16-byte pieces per token
             for (int x = tid; x < ntok * per; x += NT) {
                 const int t = x / per, y = x - t * per;
                 const uint32_t sm0 = base + Ps::TILE + t * Ps::SMALL1;
                 if (y < nq) {
-                    const T *src = static_cast<const T *>(p.q) + b * p.q_sb + t * p.q_st + hk * p.q_sh;
-                    cp_async16(sm0 + 16 * y, reinterpret_cast<const char *>(src) + 16 * y, true);
+                    const int64_t e = b * p.q_sb + t * p.q_st + hk * p.q_sh + eq * y;
+                    cp_async16(sm0 + 16 * y, static_cast<const T *>(p.q) + e,
+                               range_in_bounds(e, eq, p.ext.q, p.status, nullptr));
                 } else if (y < 2 * nq) {
-                    const T *src = static_cast<const T *>(p.k) + b * p.k_sb + t * p.k_st + hk * p.k_sh;
-                    cp_async16(sm0 + Ps::ROWQ + 16 * (y - nq), reinterpret_cast<const char *>(src) + 16 * (y - nq), true);
+                    const int64_t e = b * p.k_sb + t * p.k_st + hk * p.k_sh + eq * (y - nq);
+                    cp_async16(sm0 + Ps::ROWQ + 16 * (y - nq), static_cast<const T *>(p.k) + e,
+                               range_in_bounds(e, eq, p.ext.k, p.status, nullptr));
                 } else if (y < 2 * nq + nv) {
-                    const T *src = static_cast<const T *>(p.v) + b * p.v_sb + t * p.v_st + h * p.v_sh;
-                    cp_async16(sm0 + 2 * Ps::ROWQ + 16 * (y - 2 * nq), reinterpret_cast<const char *>(src) + 16 * (y - 2 * nq),
-                               true);
+                    const int64_t e = b * p.v_sb + t * p.v_st + h * p.v_sh + eq * (y - 2 * nq);
+                    cp_async16(sm0 + 2 * Ps::ROWQ + 16 * (y - 2 * nq), static_cast<const T *>(p.v) + e,
+                               range_in_bounds(e, eq, p.ext.v, p.status, nullptr));
                 } else {
-                    const float *src = p.g + b * p.g_sb + t * p.g_st + h * p.g_sh;
-                    cp_async16(sm0 + 2 * Ps::ROWQ + Ps::ROWV + 16 * (y - 2 * nq - nv),
-                               reinterpret_cast<const char *>(src) + 16 * (y - 2 * nq - nv), true);
+                    const int64_t e = b * p.g_sb + t * p.g_st + h * p.g_sh + 4 * (y - 2 * nq - nv);
+                    cp_async16(sm0 + 2 * Ps::ROWQ + Ps::ROWV + 16 * (y - 2 * nq - nv), p.g + e,
+                               range_in_bounds(e, 4, p.ext.g, p.status, nullptr));
                 }
             }
         }
@@ -180,10 +189,13 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
         float2 x = make_float2(0.f, 0.f);
         if (tid < ntok && u < units) {
             const int b = u / p.Hv, h = u % p.Hv, t = tid;
-            if (p.gate == CGDR_GATE_CHANNEL) x.x = p.beta[b * p.beta_sb + t * p.beta_st + h * p.beta_sh];
-            else {
-                x.x = Cvt<T>::to_f(static_cast<const T *>(p.ga)[b * p.a_sb + t * p.a_st + h * p.a_sh]);
-                x.y = Cvt<T>::to_f(static_cast<const T *>(p.gb)[b * p.b_sb + t * p.b_st + h * p.b_sh]);
+            if (p.gate == CGDR_GATE_CHANNEL) {
+                const int64_t e = b * p.beta_sb + t * p.beta_st + h * p.beta_sh;
+                if (in_bounds(e, p.ext.beta, p.status, nullptr)) x.x = p.beta[e];
+            } else {
+                const int64_t ea = b * p.a_sb + t * p.a_st + h * p.a_sh, eb = b * p.b_sb + t * p.b_st + h * p.b_sh;
+                if (in_bounds(ea, p.ext.a, p.status, nullptr)) x.x = Cvt<T>::to_f(static_cast<const T *>(p.ga)[ea]);
+                if (in_bounds(eb, p.ext.b, p.status, nullptr)) x.y = Cvt<T>::to_f(static_cast<const T *>(p.gb)[eb]);
             }
         }
         return x;
@@ -255,7 +267,8 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
                 if (tid == t) s_beta = sc.x;
             } else {
                 if (tid == t) {
-                    s_alpha[0] = expf(gdn_gate(p.A_log[h], sc.x, p.dt_bias[h]));
+                    const bool hin = in_bounds(h, p.ext.A_log, p.status, nullptr) && in_bounds(h, p.ext.dt_bias, p.status, nullptr);
+                    s_alpha[0] = expf(gdn_gate(hin ? p.A_log[h] : 0.f, sc.x, hin ? p.dt_bias[h] : 0.f));
                     s_beta = sigmoid_f(sc.y);
                 }
                 __syncthreads();
@@ -313,7 +326,8 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
                 o.z = fmaf(qn, x.z, o.z);
                 o.w = fmaf(qn, x.w, o.w);
                 s[ii] = x;
-                if (last) st_stream(Sg + (size_t)row * DV + 4 * c, x);
+                if (last && range_in_bounds((int64_t)u * DK * DV + row * DV + 4 * c, 4, p.ext.state, p.status, nullptr))
+                    st_stream(Sg + (size_t)row * DV + 4 * c, x);
             }
 #pragma unroll
             for (int off = CL; off < 32; off <<= 1) {
@@ -332,8 +346,10 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
                     tt.x += y.x; tt.y += y.y; tt.z += y.z; tt.w += y.w;
                 }
                 const int64_t off = b * p.o_sb + t * p.o_st + h * p.o_sh + 4 * c;
-                if (p.o_f32) store4<float>(static_cast<float *>(p.o) + off, tt);
-                else store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(p.o) + off, tt);
+                if (range_in_bounds(off, 4, p.ext.o, p.status, nullptr)) {
+                    if (p.o_f32) store4<float>(static_cast<float *>(p.o) + off, tt);
+                    else store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(p.o) + off, tt);
+                }
             }
             __syncthreads();  // the token's rows, the norms and s_red are free again
         }
@@ -351,6 +367,7 @@ __global__ void __launch_bounds__(DecodeShape<DK, DV>::NT, 1) decode_kernel(cons
             const int b = u / p.Hv, h = u % p.Hv;
             for (int j = tid; j < ntok * DV; j += NT) {
                 const int64_t off = b * p.o_sb + (j / DV) * p.o_st + h * p.o_sh + j % DV;
+                if (!in_bounds(off, p.ext.o, p.status, nullptr)) continue;
                 if (p.o_f32) static_cast<float *>(p.o)[off] = __int_as_float(0x7fc00000);
                 else static_cast<__nv_bfloat16 *>(p.o)[off] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
             }
@@ -403,6 +420,7 @@ DecodeParams params_of(const cgdr_args &a, int ntok) {
     p.A_log = a.A_log; p.dt_bias = a.dt_bias;
     p.state = a.state; p.o = a.o; p.o_sb = a.o_sb; p.o_sh = a.o_sh;
     p.status = a.status; p.polls = polls_of(a); p.inject = inject_of(a);
+    p.ext = extents_of(a, ntok > 1, 0);
     // token strides: a single token never steps them (decode ignores them)
     const bool one = ntok == 1;
     p.q_st = one ? 0 : a.q_st; p.k_st = one ? 0 : a.k_st; p.v_st = one ? 0 : a.v_st; p.g_st = one ? 0 : a.g_st;

@@ -131,6 +131,11 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
                  ::"l"(dst), "r"(src), "r"(bytes), "l"(l2_evict_last()) : "memory");
 }
+// bulk_store into the workspace, skipped (debug build) when it would leave the workspace
+__device__ __forceinline__ void ring_store(const Tc05Params &p, char *dst, uint32_t src, uint32_t bytes) {
+    const int64_t off = (int64_t)(dst - reinterpret_cast<const char *>(p.err));
+    if (range_in_bounds(off, bytes, p.ext.ws, p.err, p.status)) bulk_store(dst, src, bytes);
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
@@ -159,18 +164,31 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     const uint32_t sbase = smem_u32(sm);
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const int trow = 32 * wq + lane;
-    float *state = p.state + ((size_t)hd.b * p.Hv + hd.h) * DK * DV;
+    const int64_t sbase_e = ((int64_t)hd.b * p.Hv + hd.h) * DK * DV;   // the head's state tile (elements)
+    float *state = p.state + sbase_e;
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
     float *dec = f32p(sm, CH_DECC);
+    // (debug build) a ring access outside the workspace is skipped; its barrier phase still completes
+    const int64_t ring0 = (int64_t)(hslots - reinterpret_cast<const unsigned char *>(p.err));   // bytes into the workspace
     auto load_a = [&](int c) {
         ++ia;
-        arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
-        bulk_load(sbase + CH_IN_A, hslots + slot_of(c) * SLOT_BYTES + SL_QW, A_BYTES, sbase + CH_FULL_A);
+        const int64_t off = ring0 + (int64_t)slot_of(c) * SLOT_BYTES + SL_QW;
+        if (range_in_bounds(off, A_BYTES, p.ext.ws, p.err, p.status)) {
+            arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
+            bulk_load(sbase + CH_IN_A, hslots + slot_of(c) * SLOT_BYTES + SL_QW, A_BYTES, sbase + CH_FULL_A);
+        } else {
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sbase + CH_FULL_A) : "memory");
+        }
     };
     auto load_b = [&](int c) {
         ++ib;
-        arrive_expect_tx(sbase + CH_FULL_B, B_BYTES);
-        bulk_load(sbase + CH_IN_B, hslots + slot_of(c) * SLOT_BYTES + SL_KP, B_BYTES, sbase + CH_FULL_B);
+        const int64_t off = ring0 + (int64_t)slot_of(c) * SLOT_BYTES + SL_KP;
+        if (range_in_bounds(off, B_BYTES, p.ext.ws, p.err, p.status)) {
+            arrive_expect_tx(sbase + CH_FULL_B, B_BYTES);
+            bulk_load(sbase + CH_IN_B, hslots + slot_of(c) * SLOT_BYTES + SL_KP, B_BYTES, sbase + CH_FULL_B);
+        } else {
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sbase + CH_FULL_B) : "memory");
+        }
     };
     auto ready = [&](int c) { return sbase + CH_READY + 8 * slot_of(c); };
 
@@ -178,7 +196,10 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     {
         float v[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(32 * wc + c) * DV + trow];
+        for (int c = 0; c < 32; ++c) {
+            const int64_t e = (int64_t)(32 * wc + c) * DV + trow;
+            v[c] = in_bounds(sbase_e + e, p.ext.state, p.err, p.status) ? state[e] : 0.f;
+        }
         tmem_st32(tmem + lane_off + T_S + 32 * wc, v);
     }
     {
@@ -220,11 +241,13 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             if (p.o_f32) {
                 float *op = static_cast<float *>(p.o) + off0;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) op[k * p.o_st] = oprev[k];
+                for (int k = 0; k < 16; ++k)
+                    if (in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = oprev[k];
             } else {
                 __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
+                for (int k = 0; k < 16; ++k)
+                    if (in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
             }
         }
         if (!mma_wait(mb)) return false;
@@ -302,18 +325,21 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             float *op = static_cast<float *>(p.o) + off0;
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-                if (k < nv) op[k * p.o_st] = oprev[k];
+                if (k < nv && in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = oprev[k];
         } else {
             __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-                if (k < nv) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
+                if (k < nv && in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
         }
     }
     float v[32];
     tmem_ld32(tmem + lane_off + T_S + 32 * wc, v);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) state[(size_t)(32 * wc + c) * DV + trow] = v[c];
+    for (int c = 0; c < 32; ++c) {
+        const int64_t e = (int64_t)(32 * wc + c) * DV + trow;
+        if (in_bounds(sbase_e + e, p.ext.state, p.err, p.status)) state[e] = v[c];
+    }
     return true;
 }
 
@@ -359,9 +385,9 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             if (okw) {
                 // Qg (64-row tile: 8 KB per K block) into rows 0..63 of [Qg; -W]; Kg^T; e^gC
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb) bulk_store(slot + SL_QW + kb * 16384, sbase + R_B + kb * 8192, 8192);
-                bulk_store(slot + SL_KG, sbase + R_C, 32768);
-                bulk_store(slot + SL_DEC, sbase + M_DEC, 512);
+                for (int kb = 0; kb < 4; ++kb) ring_store(p, slot + SL_QW + kb * 16384, sbase + R_B + kb * 8192, 8192);
+                ring_store(p, slot + SL_KG, sbase + R_C, 32768);
+                ring_store(p, slot + SL_DEC, sbase + M_DEC, 512);
                 bulk_commit();
             }
             *slot_ok = okw;                                              // read after the next barrier
@@ -371,13 +397,13 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         if (tid == kIO) {
             // P (64-row tile) into rows 128..191 of [Kend^T; P]; V^T
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576 + 16384, sbase + R_F + kb * 8192, 8192);
-            bulk_store(slot + SL_VT, sbase + A1_VT, 32768);
+            for (int kb = 0; kb < 2; ++kb) ring_store(p, slot + SL_KP + kb * 24576 + 16384, sbase + R_F + kb * 8192, 8192);
+            ring_store(p, slot + SL_VT, sbase + A1_VT, 32768);
             bulk_commit();
         }
         solve_tb(sm);
         if (tid == kIO) {
-            bulk_store(slot + SL_TB, sbase + R_G, 16384);
+            ring_store(p, slot + SL_TB, sbase + R_G, 16384);
             bulk_commit();
             bulk_wait_read<0>();                                           // R_B, R_C, R_F, A1_VT, R_G read
         }
@@ -402,7 +428,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         if (tid == kIO) {
             // Kend^T (128-row tile: 16 KB per K block) into rows 0..127 of [Kend^T; P]
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) bulk_store(slot + SL_KP + kb * 24576, sbase + R_C + kb * 16384, 16384);
+            for (int kb = 0; kb < 2; ++kb) ring_store(p, slot + SL_KP + kb * 24576, sbase + R_C + kb * 16384, 16384);
             bulk_commit();
         }
         if (tn < p.T) st.stage<STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, tn);        // A2 is free
@@ -495,9 +521,9 @@ size_t prefill_cluster_workspace(const cgdr_args &a) {
     return WS_HEADER + (size_t)a.B * a.Hv * NSLOT * SLOT_BYTES;
 }
 
-cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, cudaStream_t s) {
+cgdr_status launch_prefill_cluster(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s) {
     Tc05Params p;
-    if (!make_params(a, ws, p)) return CGDR_ERR_ALIGNMENT;
+    if (!make_params(a, ws, ws_bytes, p)) return CGDR_ERR_ALIGNMENT;
     p.slots = static_cast<unsigned char *>(ws) + WS_HEADER;
     static SmemOnce smem_once;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CGDR_ERR_CUDA;

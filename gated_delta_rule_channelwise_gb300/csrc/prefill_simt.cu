@@ -37,6 +37,8 @@ struct PrefillParams {
     float *state;
     void *o;
     int64_t o_sb, o_st, o_sh;
+    int *status;                 // the caller's optional status word (debug-build index checks)
+    Extents ext;                 // footprints for the index checks of a debug build
 };
 
 template <int DK, int C>
@@ -71,16 +73,20 @@ __global__ void __launch_bounds__(SIMT_NT) prefill_simt_kernel(const PrefillPara
     const int hk = h / (p.Hv / p.Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int col0 = slab * WS;
-    float *state = p.state + ((size_t)b * p.Hv + h) * DK * p.dv;
+    const int64_t sbase_e = ((int64_t)b * p.Hv + h) * DK * p.dv;
+    float *state = p.state + sbase_e;
+    int *const st0 = p.status;
 
     for (int idx = tid; idx < DK * WS; idx += SIMT_NT) {
         const int i = idx / WS, j = idx % WS;
-        sS[idx] = state[(size_t)i * p.dv + col0 + j];
+        const int64_t e = (int64_t)i * p.dv + col0 + j;
+        sS[idx] = in_bounds(sbase_e + e, p.ext.state, st0, nullptr) ? state[e] : 0.f;
     }
 
-    const T *qb = static_cast<const T *>(p.q) + b * p.q_sb + hk * p.q_sh;
-    const T *kb = static_cast<const T *>(p.k) + b * p.k_sb + hk * p.k_sh;
-    const T *vb = static_cast<const T *>(p.v) + b * p.v_sb + h * p.v_sh + col0;
+    const int64_t qo = b * p.q_sb + hk * p.q_sh, ko = b * p.k_sb + hk * p.k_sh, vo = b * p.v_sb + h * p.v_sh + col0;
+    const T *qb = static_cast<const T *>(p.q) + qo;
+    const T *kb = static_cast<const T *>(p.k) + ko;
+    const T *vb = static_cast<const T *>(p.v) + vo;
     const int64_t obase = b * p.o_sb + h * p.o_sh + col0;
 
     for (int t0 = 0; t0 < p.T; t0 += C) {
@@ -92,29 +98,37 @@ __global__ void __launch_bounds__(SIMT_NT) prefill_simt_kernel(const PrefillPara
             float qv = 0.f, kv = 0.f, gv = 0.f;
             if (r < L) {
                 const int64_t t = t0 + r;
-                qv = Cvt<T>::to_f(qb[t * p.q_st + i]);
-                kv = Cvt<T>::to_f(kb[t * p.k_st + i]);
+                if (in_bounds(qo + t * p.q_st + i, p.ext.q, st0, nullptr)) qv = Cvt<T>::to_f(qb[t * p.q_st + i]);
+                if (in_bounds(ko + t * p.k_st + i, p.ext.k, st0, nullptr)) kv = Cvt<T>::to_f(kb[t * p.k_st + i]);
                 if (p.gate == CGDR_GATE_CHANNEL) {
-                    gv = p.g[b * p.g_sb + t * p.g_st + h * p.g_sh + i];
+                    const int64_t e = b * p.g_sb + t * p.g_st + h * p.g_sh + i;
+                    if (in_bounds(e, p.ext.g, st0, nullptr)) gv = p.g[e];
                 } else {
-                    const float av = Cvt<T>::to_f(static_cast<const T *>(p.ga)[b * p.a_sb + t * p.a_st + h * p.a_sh]);
-                    gv = gdn_gate(p.A_log[h], av, p.dt_bias[h]);
+                    const int64_t e = b * p.a_sb + t * p.a_st + h * p.a_sh;
+                    if (in_bounds(e, p.ext.a, st0, nullptr) && in_bounds(h, p.ext.A_log, st0, nullptr) &&
+                        in_bounds(h, p.ext.dt_bias, st0, nullptr))
+                        gv = gdn_gate(p.A_log[h], Cvt<T>::to_f(static_cast<const T *>(p.ga)[e]), p.dt_bias[h]);
                 }
             }
             sQ[idx] = qv; sK[idx] = kv; sG[idx] = gv;
         }
         for (int idx = tid; idx < C * WS; idx += SIMT_NT) {
             const int r = idx / WS, j = idx % WS;
-            sV[idx] = r < L ? Cvt<T>::to_f(vb[(int64_t)(t0 + r) * p.v_st + j]) : 0.f;
+            const int64_t e = (int64_t)(t0 + r) * p.v_st + j;
+            sV[idx] = r < L && in_bounds(vo + e, p.ext.v, st0, nullptr) ? Cvt<T>::to_f(vb[e]) : 0.f;
         }
         for (int r = tid; r < C; r += SIMT_NT) {
             float be = 0.f;
             if (r < L) {
                 const int64_t t = t0 + r;
-                if (p.gate == CGDR_GATE_CHANNEL)
-                    be = p.beta[b * p.beta_sb + t * p.beta_st + h * p.beta_sh];
-                else
-                    be = sigmoid_f(Cvt<T>::to_f(static_cast<const T *>(p.gb)[b * p.b_sb + t * p.b_st + h * p.b_sh]));
+                if (p.gate == CGDR_GATE_CHANNEL) {
+                    const int64_t e = b * p.beta_sb + t * p.beta_st + h * p.beta_sh;
+                    if (in_bounds(e, p.ext.beta, st0, nullptr)) be = p.beta[e];
+                } else {
+                    const int64_t e = b * p.b_sb + t * p.b_st + h * p.b_sh;
+                    if (in_bounds(e, p.ext.b, st0, nullptr))
+                        be = sigmoid_f(Cvt<T>::to_f(static_cast<const T *>(p.gb)[e]));
+                }
             }
             sBeta[r] = be;
         }
@@ -212,6 +226,7 @@ __global__ void __launch_bounds__(SIMT_NT) prefill_simt_kernel(const PrefillPara
             for (int i = 0; i < DK; ++i) acc = fmaf(sQ[r * DK + i], sS[i * WS + j], acc);
             for (int s = 0; s <= r; ++s) acc = fmaf(sP[r * LC + s], sV[s * WS + j], acc);
             const int64_t off = obase + (int64_t)(t0 + r) * p.o_st + j;
+            if (!in_bounds(off, p.ext.o, st0, nullptr)) continue;
             if (p.o_f32)
                 static_cast<float *>(p.o)[off] = acc;
             else
@@ -229,7 +244,8 @@ __global__ void __launch_bounds__(SIMT_NT) prefill_simt_kernel(const PrefillPara
     __syncthreads();
     for (int idx = tid; idx < DK * WS; idx += SIMT_NT) {
         const int i = idx / WS, j = idx % WS;
-        state[(size_t)i * p.dv + col0 + j] = sS[idx];
+        const int64_t e = (int64_t)i * p.dv + col0 + j;
+        if (in_bounds(sbase_e + e, p.ext.state, st0, nullptr)) state[e] = sS[idx];
     }
 }
 
@@ -274,6 +290,8 @@ cgdr_status launch_prefill_simt(const cgdr_args &a, cudaStream_t s) {
     p.b_sb = a.b_sb; p.b_st = a.b_st; p.b_sh = a.b_sh;
     p.A_log = a.A_log; p.dt_bias = a.dt_bias;
     p.state = a.state; p.o = a.o; p.o_sb = a.o_sb; p.o_st = a.o_st; p.o_sh = a.o_sh;
+    p.status = a.status;
+    p.ext = extents_of(a, true, 0);
     const int C = chunk_of(a);
     if (a.dtype == CGDR_BF16) return launch_dtype<__nv_bfloat16>(p, a.B, a.dk, C, s);
     return launch_dtype<float>(p, a.B, a.dk, C, s);

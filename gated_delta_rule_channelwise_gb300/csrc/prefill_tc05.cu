@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;                 // TMEM lane quarter, column quarter
     const int ci = tid & 127, cq = tid >> 7;                 // channel (or column), row quarter (16 rows)
-    float *state = p.state + ((size_t)hd.b * p.Hv + hd.h) * DK * DV;
+    const int64_t sbase_e = ((int64_t)hd.b * p.Hv + hd.h) * DK * DV;   // the head's state tile (elements)
+    float *state = p.state + sbase_e;
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
 
     MmaBar mb{sbase + M_MBAR, 0u, p.polls};
@@ -54,7 +55,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     {
         float v[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = state[(size_t)(32 * wc + c) * DV + trow];
+        for (int c = 0; c < 32; ++c) {
+            const int64_t e = (int64_t)(32 * wc + c) * DV + trow;
+            v[c] = in_bounds(sbase_e + e, p.ext.state, p.err, p.status) ? state[e] : 0.f;
+        }
         tmem_st32(tmem + lane_off + T_D0 + 32 * wc, v);
     }
     StageTrack st;
@@ -143,7 +147,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
         float v[32];
         tmem_ld32(tmem + lane_off + T_D0 + 32 * wc, v);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) state[(size_t)(32 * wc + c) * DV + trow] = v[c];
+        for (int c = 0; c < 32; ++c) {
+            const int64_t e = (int64_t)(32 * wc + c) * DV + trow;
+            if (in_bounds(sbase_e + e, p.ext.state, p.err, p.status)) state[e] = v[c];
+        }
     } else {
         // a wait gave up: record it, give the tensor core a bounded chance to finish, release TMEM
         if (tid == 0) {
@@ -225,7 +232,7 @@ bool make_maps(const cgdr_args &a, Tc05Maps &tm) {
     return ok;
 }
 
-bool make_params(const cgdr_args &a, void *ws, Tc05Params &p) {
+bool make_params(const cgdr_args &a, void *ws, size_t ws_bytes, Tc05Params &p) {
     if (!make_maps(a, p.tm)) return false;
     p.T = a.T; p.Hk = a.Hk; p.Hv = a.Hv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate;
     p.o_f32 = a.o_dtype == CGDR_F32;
@@ -250,15 +257,16 @@ bool make_params(const cgdr_args &a, void *ws, Tc05Params &p) {
     p.status = a.status;
     p.polls = polls_of(a);
     p.inject = inject_of(a);
+    p.ext = extents_of(a, true, ws_bytes);
     p.slots = nullptr;
     return true;
 }
 }  // namespace tc05c
 
-cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, cudaStream_t s) {
+cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s) {
     static SmemOnce smem_once;
     tc05c::Tc05Params p;
-    if (!tc05c::make_params(a, ws, p)) return CGDR_ERR_ALIGNMENT;
+    if (!tc05c::make_params(a, ws, ws_bytes, p)) return CGDR_ERR_ALIGNMENT;
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return CGDR_ERR_CUDA;
     if (!smem_limit_once(smem_once, reinterpret_cast<const void *>(prefill_tc05_kernel), tc05c::PREP_SMEM_BYTES))
         return CGDR_ERR_CUDA;

@@ -92,6 +92,7 @@ struct Tc05Params {
     int *status;                         // the caller's optional status word (the same code)
     uint32_t polls;                      // polls of the main-loop waits (drains use kSpin)
     int inject;                          // test hook: the first staging wait targets M_DEAD
+    Extents ext;                         // footprints for the index checks of a debug build
     unsigned char *slots;                // cluster kernel: hand-off ring in the workspace (unused per head)
 };
 
@@ -101,7 +102,7 @@ __device__ __forceinline__ void record_timeout(const Tc05Params &p) {
     if (p.status != nullptr) atomicExch(p.status, (int)CGDR_ERR_TIMEOUT);
 }
 
-bool make_params(const cgdr_args &a, void *ws, Tc05Params &p);   // false if a tensor map cannot be encoded
+bool make_params(const cgdr_args &a, void *ws, size_t ws_bytes, Tc05Params &p);   // false if a tensor map cannot be encoded
 // Whether every input's strides can be described by a tensor map (host arithmetic only).
 bool maps_describable(const cgdr_args &a);
 // Fills the tensor maps of `a` through the driver's encoder; false if it cannot (then the
@@ -202,7 +203,8 @@ __device__ __forceinline__ void stage_rows(const Tc05Params &p, const Head &hd, 
         const int Ln = min(C, p.T - tn);
         const bool ok_row = tid < Ln;
         const int64_t t = tn + (ok_row ? tid : 0);
-        cp_async4(sbase + ST_BETA + 4 * tid, p.beta + hd.b * p.beta_sb + t * p.beta_st + hd.h * p.beta_sh, ok_row);
+        const int64_t e = hd.b * p.beta_sb + t * p.beta_st + hd.h * p.beta_sh;
+        cp_async4(sbase + ST_BETA + 4 * tid, p.beta + e, ok_row && in_bounds(e, p.ext.beta, p.err, p.status));
     }
     cp_async_commit();
 }
@@ -337,9 +339,13 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             if (p.gate == CGDR_GATE_CHANNEL) {
                 be = f32p(sm, ST_BETA)[r];
             } else {
-                be = sigmoid_f(__bfloat162float(p.gb[hd.b * p.b_sb + t * p.b_st + hd.h * p.b_sh]));
-                gs = gdn_gate(p.A_log[hd.h], __bfloat162float(p.ga[hd.b * p.a_sb + t * p.a_st + hd.h * p.a_sh]),
-                              p.dt_bias[hd.h]);
+                const int64_t ea = hd.b * p.a_sb + t * p.a_st + hd.h * p.a_sh, eb = hd.b * p.b_sb + t * p.b_st + hd.h * p.b_sh;
+                const bool ok = in_bounds(ea, p.ext.a, p.err, p.status) && in_bounds(eb, p.ext.b, p.err, p.status) &&
+                                in_bounds(hd.h, p.ext.A_log, p.err, p.status) && in_bounds(hd.h, p.ext.dt_bias, p.err, p.status);
+                if (ok) {
+                    be = sigmoid_f(__bfloat162float(p.gb[eb]));
+                    gs = gdn_gate(p.A_log[hd.h], __bfloat162float(p.ga[ea]), p.dt_bias[hd.h]);
+                }
             }
         }
         sBeta[r] = be;
@@ -637,12 +643,12 @@ __device__ __forceinline__ void store_o(const Tc05Params &p, int64_t obase, uint
         float *op = static_cast<float *>(p.o) + off0;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-            if (c < nv) op[c * p.o_st] = v[c];
+            if (c < nv && in_bounds(off0 + c * p.o_st, p.ext.o, p.err, p.status)) op[c * p.o_st] = v[c];
     } else {
         __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-            if (c < nv) op[c * p.o_st] = __float2bfloat16_rn(v[c]);
+            if (c < nv && in_bounds(off0 + c * p.o_st, p.ext.o, p.err, p.status)) op[c * p.o_st] = __float2bfloat16_rn(v[c]);
     }
 }
 

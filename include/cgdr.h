@@ -71,7 +71,9 @@ typedef enum cgdr_status {
     CGDR_ERR_ALIGNMENT = 3,     /* misaligned pointer, stride or non-unit inner stride */
     CGDR_ERR_WORKSPACE = 4,     /* workspace smaller than cgdr_prefill_workspace_size() */
     CGDR_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
-    CGDR_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up (reported through a status word) */
+    CGDR_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (reported through a status word) */
+    CGDR_ERR_BOUNDS = 7         /* debug build only: a device-side index check failed (through a status
+                                   word); the access was skipped */
 } cgdr_status;
 
 typedef enum cgdr_dtype { CGDR_F32 = 0, CGDR_BF16 = 1 } cgdr_dtype;

@@ -12,6 +12,7 @@ from gated_delta_rule_channelwise_gb300 import build as cbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "cgdr.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -20,31 +21,55 @@ def lib():
     return cg.lib()
 
 
-def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(cgdr_[a-z_]+)\s*\(", text)))
+def declared_functions(headers=None):
+    names = set()
+    for h in headers or HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(cgdr_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_abi():
-    assert declared_functions() == sorted([
+    assert declared_functions([HEADER]) == sorted([
         "cgdr_abi_version", "cgdr_status_string", "cgdr_validate", "cgdr_decode",
         "cgdr_prefill_workspace_size", "cgdr_prefill", "cgdr_workspace_status", "cgdr_prefill_noalloc",
         "cgdr_prefill_path_for"])
+    assert declared_functions([os.path.join(ROOT, "include", "cgdr_debug.h")]) == ["cgdr_debug_decode_shrunk_o"]
+
+
+def _exports(path):
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    return set(re.findall(r"\b[TW] (\w+)$", out, flags=re.M))
 
 
 def test_library_exports_every_declared_symbol(lib):
-    out = subprocess.run(["nm", "-D", "--defined-only", cg.LIB_PATH], capture_output=True, text=True, check=True).stdout
-    exported = set(re.findall(r"\b[TW] (\w+)$", out, flags=re.M))
+    exported = _exports(cg.LIB_PATH)
     for name in declared_functions():
         assert name in exported, name
         assert getattr(lib, name) is not None
 
 
+def test_debug_library_builds_and_exports_every_declared_symbol():
+    """The index-checking build compiles from the same sources and exports the same ABI plus
+    its test entry point; the release library answers that entry point with UNSUPPORTED."""
+    path = cbuild.build(debug=True)
+    exported = _exports(path)
+    for name in declared_functions():
+        assert name in exported, name
+    dlib = ctypes.CDLL(path)
+    dlib.cgdr_abi_version.restype = ctypes.c_int
+    assert dlib.cgdr_abi_version() == cg.lib().cgdr_abi_version()
+    rel = cg.lib()
+    rel.cgdr_debug_decode_shrunk_o.restype = ctypes.c_int
+    rel.cgdr_debug_decode_shrunk_o.argtypes = [ctypes.POINTER(cg.CgdrArgs), ctypes.c_int64, ctypes.c_void_p]
+    A = _args()
+    assert rel.cgdr_debug_decode_shrunk_o(ctypes.byref(A), 4, None) == cg.ERR_UNSUPPORTED
+
+
 def test_abi_version_and_status_strings(lib):
     m = re.search(r"#define CGDR_ABI_VERSION (\d+)", open(HEADER).read())
     assert lib.cgdr_abi_version() == int(m.group(1))
-    for s in range(7):
+    for s in range(8):
         assert cg.status_string(s).startswith("CGDR_")
     assert cg.status_string(99) == "unknown cgdr status"
 
