@@ -541,9 +541,10 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
 def oracle_sample(seconds_budget: float):
     """Time the fp64 CPU oracle, as it stands, on bounded samples of both workloads.
 
-    Decode: every (b, h) unit of a B=64, H=32 batch for one token; prefill: all
-    32 heads for the first `n_tok` tokens of the T=4000 sequence.  Returns
-    (decode GB/s of fp32-state traffic, prefill tokens/s, threads, description).
+    Decode: every (b, h) unit of a B=64, H=32 batch for one token, on all host cores and on
+    one; prefill: all 32 heads for the first `n_tok` tokens of the T=4000 sequence.  Returns
+    (decode GB/s of fp32-state traffic, prefill tokens/s, threads, description, single-thread
+    decode GB/s).
     """
     import oracle
     from gated_delta_rule_channelwise_gb300.synth import WORKLOADS, make_inputs
@@ -553,6 +554,11 @@ def oracle_sample(seconds_budget: float):
     t = time.perf_counter()
     oracle.recurrence(di["q"], di["k"], di["v"], g=di["g"], beta=di["beta"], S0=di["S0"], threads=threads)
     dsec = time.perf_counter() - t
+    # one thread, on an eighth of the units (scaled to the full batch)
+    d1 = make_inputs(wd, T=1, B=8, device="cpu")
+    t = time.perf_counter()
+    oracle.recurrence(d1["q"], d1["k"], d1["v"], g=d1["g"], beta=d1["beta"], S0=d1["S0"], threads=1)
+    dsec1 = (time.perf_counter() - t) * 8
     n_tok = 64
     pi = make_inputs(wp, T=n_tok, device="cpu")
     t = time.perf_counter()
@@ -563,9 +569,9 @@ def oracle_sample(seconds_budget: float):
         if time.perf_counter() - t > seconds_budget / 2 or reps >= 50:
             break
     psec = (time.perf_counter() - t) / reps
-    desc = ("decode: all 2048 (b,h) units of B=64,H=32 for 1 token; prefill: 32 heads x %d tokens of the "
-            "T=4000 sequence, %d repeats" % (n_tok, reps))
-    return DEC_STATE_BYTES / dsec / 1e9, n_tok / psec, threads, desc
+    desc = ("decode: all 2048 (b,h) units of B=64,H=32 for 1 token (single-thread figure: 256 units, "
+            "scaled); prefill: 32 heads x %d tokens of the T=4000 sequence, %d repeats" % (n_tok, reps))
+    return DEC_STATE_BYTES / dsec / 1e9, n_tok / psec, threads, desc, DEC_STATE_BYTES / dsec1 / 1e9
 
 
 def run_reference(args):
@@ -671,9 +677,10 @@ def main():
     out = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if world == 1:
-            dgbs, ptps, cores, desc = oracle_sample(args.cpu_baseline_seconds)
+            dgbs, ptps, cores, desc, dgbs1 = oracle_sample(args.cpu_baseline_seconds)
             out["cpu_baseline"] = {"value": round(dgbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                   "sample": desc, "prefill_tokens_per_s": round(ptps, 2)}
+                                   "sample": desc, "prefill_tokens_per_s": round(ptps, 2),
+                                   "value_one_thread": round(dgbs1, 4)}
         else:
             out["cpu_baseline"] = None
         print(json.dumps(out), flush=True)
