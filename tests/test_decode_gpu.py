@@ -141,3 +141,20 @@ def test_bf16_output_is_the_rounded_fp32_output(dk, dv):
     torch.cuda.synchronize()
     assert torch.equal(s1, s2)
     assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+def test_scalar_gate_equals_broadcast_channel_gate():
+    """Decode: the scalar gate is the channelwise gate with one g broadcast over dk."""
+    import torch.nn.functional as F
+    w = Workload("gbd", B=3, Hk=2, Hv=4, dk=128, dv=64, T=4, dtype="bf16", gate="gdn", seed=321)
+    inp = make_inputs(w, device="cuda")
+    g1 = -torch.exp(inp["A_log"])[None, None, :] * F.softplus(inp["a"].float() + inp["dt_bias"][None, None, :])
+    chan = {k: inp[k] for k in ("q", "k", "v", "S0")}
+    chan["g"] = g1[..., None].expand(-1, -1, -1, w.dk).contiguous()
+    chan["beta"] = torch.sigmoid(inp["b"].float()).contiguous()
+    s1, s2 = inp["S0"].clone(), inp["S0"].clone()
+    o1 = decode_steps(cg, inp, 4, s1)
+    o2 = decode_steps(cg, chan, 4, s2)
+    torch.cuda.synchronize()
+    assert rel_err(o1, o2.double().cpu().numpy()) <= 1e-4
+    assert rel_err(s1, s2.double().cpu().numpy()) <= 1e-4

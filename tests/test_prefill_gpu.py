@@ -288,3 +288,27 @@ def test_packed_gdn_prefill_recurrent():
     _expect_path(inp, cg.PREFILL_RECURRENT)
     o, s = _prefill(inp, 64)
     _check(w, inp, o, s, units=[(0, 0), (0, 1), (1, 17), (1, 31)], tol=TOL[torch.float32])
+
+
+@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT, cg.PREFILL_RECURRENT])
+def test_scalar_gate_equals_broadcast_channel_gate(path):
+    """The scalar GatedDeltaNet gate is the channelwise gate with one g broadcast over dk: the
+    same call with g = -exp(A_log) softplus(a + dt_bias) expanded to every channel and
+    beta = sigmoid(b) gives the same result (up to the rounding of the gate itself, computed
+    by torch here and on the device there), on every prefill kernel."""
+    import torch.nn.functional as F
+    T = 5 if path == cg.PREFILL_RECURRENT else 150
+    w = Workload("gb", B=2, Hk=2, Hv=4, dk=128, dv=128, T=T, dtype="bf16", gate="gdn", seed=123)
+    inp = make_inputs(w, device="cuda")
+    g1 = -torch.exp(inp["A_log"])[None, None, :] * F.softplus(inp["a"].float() + inp["dt_bias"][None, None, :])
+    chan = dict(inp)
+    chan["g"] = g1[..., None].expand(-1, -1, -1, w.dk).contiguous()
+    chan["beta"] = torch.sigmoid(inp["b"].float()).contiguous()
+    for key in ("a", "b", "A_log", "dt_bias"):
+        chan.pop(key)
+    o1, s1 = _prefill(inp, 64, path=path)
+    o2, s2 = _prefill(chan, 64, path=path)
+    eo = rel_err(o1, o2.double().cpu().numpy())
+    es = rel_err(s1, s2.double().cpu().numpy())
+    print("[gate] path %d o %.3e S %.3e" % (path, eo, es))
+    assert eo <= 1e-3 and es <= 1e-3
