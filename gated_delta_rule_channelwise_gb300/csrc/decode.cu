@@ -55,7 +55,6 @@ struct DecodeShape {
     static_assert(RPT * NW * RW == DK, "tile does not split evenly");
 };
 
-__device__ __forceinline__ float4 ld_stream(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
 __device__ __forceinline__ void st_stream(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
 
 template <typename T>

@@ -292,7 +292,7 @@ struct ChunkRegs {
 template <bool kPrefetchQKV>
 __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L, int t_pf,
                                            char *qg, int qg_rows, ChunkRegs &cr) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int ci = tid & 127, cq = tid >> 7;
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
     float *sQt = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
