@@ -288,7 +288,9 @@ def run_ours(args, rank, world, local_rank):
     out = {
         "metric": METRIC, "value": round(dec_gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(sus_step_s * 1e3 + pre_total / K, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "dtype_note": "bf16 q/k/v inputs; fp32 state, gates and accumulation; the prefill's tensor-core "
+                      "operands are TF32",
         "config": bench_config(world),
         "pct_hbm_peak": round(100.0 * dec_gbs / world / hbm, 2),
         "prefill": {"metric": "prefill tokens/s at T=4000, 32 heads", "value": round(pre_tps, 1),
@@ -433,10 +435,12 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
     Every step copies its inputs host -> device and its output device -> host
     inside the timed region.  The copies run on two streams of their own, double
     buffered, so that step i+1's inputs go in and step i's output comes back while
-    the GPU computes (the state is carried on the device from step to step)."""
+    the GPU computes (the state is carried on the device from step to step).  The
+    headline replays a run of such steps from one CUDA graph (the host issues one
+    launch for many steps); the same steps issued call by call from Python are
+    reported beside it."""
     import torch
     K = max(3, min(args.steps, 200))
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
     def packed(tensors, device):
         """One buffer (pinned on the host) holding all the tensors, and views of it in their shapes."""
@@ -451,10 +455,11 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
                  for (k, x), o in zip(tensors.items(), offs)}
         return buf, views
 
-    def pipeline(host_in, out_like, compute, overlap):
-        """A runner of n steps: copy in (s_in) -> compute (stream) -> copy out (s_out), two slots.
-        The inputs travel as one packed copy.  overlap=False runs each step's copies and compute
-        back to back on one stream instead."""
+    def pipeline(host_in, out_like, compute, cs):
+        """A runner of n steps: copy in (s_in) -> compute (cs) -> copy out (s_out), two slots.
+        The inputs travel as one packed copy.  Every event a run waits on is recorded inside the
+        run, so the same runner can be captured into a CUDA graph on cs."""
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         hbuf, hviews = packed(host_in, "cpu")
         for k, x in host_in.items():
             hviews[k].copy_(x)
@@ -462,44 +467,63 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
         dev_out = [torch.empty_like(out_like, device=dev) for _ in range(2)]
         host_out = [torch.empty_like(out_like).pin_memory() for _ in range(2)]
         in_ready, in_free, out_ready, out_free = ([torch.cuda.Event() for _ in range(2)] for _ in range(4))
-        for e in in_free + out_free:
-            e.record(stream)
 
-        def run(n, start):
-            if not overlap:
-                for i in range(n):
-                    j = i & 1
-                    dev_in[j][0].copy_(hbuf, non_blocking=True)
-                    compute(dev_in[j][1], dev_out[j])
-                    host_out[j].copy_(dev_out[j], non_blocking=True)
-                return
-            s_in.wait_event(start)
-            s_out.wait_event(start)
+        def run(n):
+            for e in in_free + out_free:                       # everything before the run is done with both slots
+                e.record(cs)
             for i in range(n):
                 j = i & 1
                 s_in.wait_event(in_free[j])                    # step i-2 has finished reading slot j
                 with torch.cuda.stream(s_in):
                     dev_in[j][0].copy_(hbuf, non_blocking=True)
                 in_ready[j].record(s_in)
-                stream.wait_event(in_ready[j])
-                stream.wait_event(out_free[j])                 # step i-2's output has left slot j
-                compute(dev_in[j][1], dev_out[j])
-                in_free[j].record(stream)
-                out_ready[j].record(stream)
+                cs.wait_event(in_ready[j])
+                cs.wait_event(out_free[j])                     # step i-2's output has left slot j
+                with torch.cuda.stream(cs):
+                    compute(dev_in[j][1], dev_out[j])
+                in_free[j].record(cs)
+                out_ready[j].record(cs)
                 s_out.wait_event(out_ready[j])
                 with torch.cuda.stream(s_out):
                     host_out[j].copy_(dev_out[j], non_blocking=True)
                 out_free[j].record(s_out)
-            stream.wait_event(out_free[(n - 1) & 1])           # the last output is on the host
+            cs.wait_event(out_free[(n - 1) & 1])               # the last output is on the host
         return run
+
+    def graphed(host_in, out_like, compute, n_steps):
+        """The same pipeline captured as one CUDA graph of n_steps steps; returns a replay function."""
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        run = pipeline(host_in, out_like, compute, cap)
+        run(2)                                                 # eager once: per-device set-up outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            run(n_steps)
+        graph.replay()
+        torch.cuda.synchronize()
+        return graph.replay
+
+    def timed(fn, n_calls, steps_per_call):
+        fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n_calls):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / (n_calls * steps_per_call)
 
     # decode: q, k, v, g, beta in, o out
     h = {k: dinp[k][:, 0].contiguous().cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
     o_like = torch.empty(DEC["B"], DEC["H"], DEC["dv"], dtype=torch.float32)
     h2d_dec = sum(x.numel() * x.element_size() for x in h.values())
     d2h_dec = o_like.numel() * o_like.element_size()
-    drun = pipeline(h, o_like, lambda d, o: cg.decode(d["q"], d["k"], d["v"], dstate, o, g=d["g"], beta=d["beta"],
-                                                      stream=stream), True)
+
+    def dcompute(d, o):
+        cg.decode(d["q"], d["k"], d["v"], dstate, o, g=d["g"], beta=d["beta"])
+
     # prefill: q, k, v, g, beta in, o out (zero initial state each step, as in the timed kernel)
     hp = {k: pinp[k].contiguous().cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
     po_like = torch.empty(pinp["v"].shape, dtype=torch.bfloat16)
@@ -513,28 +537,25 @@ def run_e2e(args, cg, dinp, dstate, pinp, dev, stream, world):
 
     def pcompute(d, o):
         ps.zero_()
-        cg.prefill(d["q"], d["k"], d["v"], ps, o, g=d["g"], beta=d["beta"], chunk=64, workspace=ws, stream=stream)
+        cg.prefill(d["q"], d["k"], d["v"], ps, o, g=d["g"], beta=d["beta"], chunk=64, workspace=ws)
 
-    prun = pipeline(hp, po_like, pcompute, True)
-    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-    e0.record(stream)
-    drun(3, e0)
-    prun(3, e0)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    drun(K, e0)
-    e1.record(stream)
-    prun(K, e1)
-    e2.record(stream)
-    torch.cuda.synchronize()
-    dms, pms = e0.elapsed_time(e1) / K, e1.elapsed_time(e2) / K
-    return {"value": round(world * DEC_STATE_BYTES / (dms / 1e3) / 1e9, 2), "unit": "GB/s",
+    drun, prun = pipeline(h, o_like, dcompute, stream), pipeline(hp, po_like, pcompute, stream)
+    drun(3)
+    prun(3)
+    dms, pms = timed(lambda: drun(K), 1, K), timed(lambda: prun(K), 1, K)
+    D_STEPS, P_STEPS = 64, 8
+    graph_dms = timed(graphed(h, o_like, dcompute, D_STEPS), 4, D_STEPS)
+    graph_pms = timed(graphed(hp, po_like, pcompute, P_STEPS), 3, P_STEPS)
+    return {"value": round(world * DEC_STATE_BYTES / (graph_dms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d_dec + h2d_pre, "d2h_bytes_per_step": d2h_dec + d2h_pre,
-            "decode_ms": round(dms, 5), "prefill_ms": round(pms, 5),
-            "prefill_tokens_per_s": round(world * PRE["T"] / (pms / 1e3), 1),
-            "note": "every step copies its inputs in (one packed copy from pinned host memory) and its o "
-                    "out inside the timed region, on two copy streams double-buffered against the compute; "
-                    "the decode state stays resident on the device"}
+            "decode_ms": round(graph_dms, 5), "prefill_ms": round(graph_pms, 5),
+            "prefill_tokens_per_s": round(world * PRE["T"] / (graph_pms / 1e3), 1),
+            "eager_pipelined": {"decode_ms": round(dms, 5), "prefill_ms": round(pms, 5),
+                                "value": round(world * DEC_STATE_BYTES / (dms / 1e3) / 1e9, 2)},
+            "note": f"every step copies its inputs in (one packed copy from pinned host memory) and its o out "
+                    f"inside the timed region, on two copy streams double-buffered against the compute; value: "
+                    f"{D_STEPS} decode / {P_STEPS} prefill steps replayed from one CUDA graph; eager_pipelined: "
+                    f"the same steps issued call by call from Python; the decode state stays resident on the device"}
 
 
 # ------------------------------------------------------------------ oracle timing

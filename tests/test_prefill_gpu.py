@@ -132,6 +132,21 @@ def test_prefill_t4000_full(tc_path):
     _check(w, inp, o, s)
 
 
+def test_prefill_t4000_as_benchmarked_bf16_o():
+    """The configuration the benchmark times -- T = 4000, 32 heads, automatic kernel choice,
+    o in bf16 -- gives exactly the bf16 rounding of the fp32-o result (whose parity with the
+    oracle test_prefill_t4000_full checks) and the same final state."""
+    w = WORKLOADS["prefill_t4000"]
+    inp = make_inputs(w, device="cuda")
+    o32, s32 = _prefill(inp, 64)
+    s16 = inp["S0"].clone()
+    o16 = torch.empty(inp["v"].shape, dtype=torch.bfloat16, device="cuda")
+    cg.prefill(inp["q"], inp["k"], inp["v"], s16, o16, chunk=64, **gate_kwargs(inp))
+    torch.cuda.synchronize()
+    assert torch.equal(s16, s32)
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
 def test_prefill_long_then_decode_sampled(tc_path):
     """B=4, H=32, T=16411 (ragged 27), strong decay; then 64 decode steps from the final state.
     Eight sampled (b, h) units are checked against the oracle over all T + 64 tokens."""
