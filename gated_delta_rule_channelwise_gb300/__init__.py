@@ -28,7 +28,7 @@ import threading
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libcgdr.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = range(8)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS, ERR_RANGE = range(9)
 F32, BF16 = 0, 1
 GATE_CHANNEL, GATE_GDN = 0, 1
 PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT, PREFILL_RECURRENT = range(5)
@@ -159,7 +159,8 @@ def make_args(q, k, v, state, o, *, T, g=None, beta=None, a=None, b=None, A_log=
     ``a, b [B,T,Hv]`` with ``A_log, dt_bias [Hv]`` (GatedDeltaNet gate).  ``path`` is the
     prefill kernel of the call, ``wait_polls`` the polls of a bounded device wait (0: the
     library's default; small values are for failure-path tests) and ``status`` an optional
-    int32 device tensor that receives ``ERR_TIMEOUT`` if a wait gives up.
+    int32 device tensor that receives ``ERR_TIMEOUT`` if a wait gives up, or ``ERR_RANGE`` if a
+    tensor-core prefill met a value beyond the fp16 range in one of its fp16 operands.
     The block is built in one constructor call (field order of ``struct cgdr_args``).
     """
     B, _, Hk, dk = q.shape

@@ -200,6 +200,7 @@ const char *cgdr_status_string(int s) {
         case CGDR_ERR_CUDA: return "CGDR_ERR_CUDA: a CUDA call or kernel launch failed";
         case CGDR_ERR_TIMEOUT: return "CGDR_ERR_TIMEOUT: a bounded device wait gave up";
         case CGDR_ERR_BOUNDS: return "CGDR_ERR_BOUNDS: a debug build's device index check failed";
+        case CGDR_ERR_RANGE: return "CGDR_ERR_RANGE: an fp16 tensor-core operand left the fp16 range";
         default: return "unknown cgdr status";
     }
 }

@@ -13,8 +13,8 @@
 //   ranks 1..3 (preparers) take chunks round robin (chunk c on rank
 //                          1 + c % 3) and run the state-free phases.
 // Hand-off through L2: a preparer sends the tiles it has built in shared
-// memory -- Qg, Kg^T, V^T, Tb, e^gC (inbox A image) and Kend^T, P (inbox B
-// image) -- with bulk stores into one of its three slots of a ring in the
+// memory -- Qg (TF32), Kg^T, V^T, Tb (fp16), e^gC (inbox A image) and Kend^T,
+// P (fp16, inbox B image) -- with bulk stores into one of its three slots of a ring in the
 // workspace, each piece at its place in rank 0's shared-memory tile layout,
 // and arrives on rank 0's ready barrier for that slot; rank 0 pulls each
 // image into its inbox with one bulk load as soon as the inbox is free, and
@@ -38,34 +38,38 @@ using namespace tc05c;
 constexpr int CLUSTER = 4, NPREP = CLUSTER - 1, NSLOTP = 3, NSLOT = NSLOTP * NPREP;   // NSLOTP slots per preparer
 
 // one hand-off slot (bytes): the inbox A image, then the inbox B image
-constexpr int SL_QW = 0;                         // [Qg ; -W] [128 x 128] tile: rows 0..63 Qg (rows 64..127: rank 0)
-constexpr int SL_KG = 65536;                     // Kg^T [128 x 64] tile
-constexpr int SL_VT = 98304;                     // V^T  [128 x 64] tile
-constexpr int SL_TB = 131072;                    // Tb   [64 x 64] tile
-constexpr int SL_DEC = 147456;                   // e^gC [128] fp32
-constexpr uint32_t A_BYTES = 147456 + 512;
-constexpr int SL_KP = (int)A_BYTES;              // [Kend^T ; P] [192 x 64] tile (rows 0..127 Kend^T, 128..191 P)
-constexpr uint32_t B_BYTES = 49152;
+constexpr int SL_QG = 0;                         // Qg   [64 x 128] TF32 tile
+constexpr int SL_KG = 32768;                     // Kg^T [128 x 64] fp16 tile
+constexpr int SL_VT = 49152;                     // V^T  [128 x 64] fp16 tile
+constexpr int SL_TB = 65536;                     // Tb   [64 x 64] fp16 tile
+constexpr int SL_DEC = 73728;                    // e^gC [128] fp32
+constexpr uint32_t A_BYTES = 73728 + 512;
+constexpr int SL_KP = (int)A_BYTES;              // [Kend^T ; P] [192 x 64] fp16 tile (rows 0..127 Kend^T, 128..191 P)
+constexpr uint32_t B_BYTES = 24576;
 constexpr size_t SLOT_BYTES = A_BYTES + B_BYTES;
 constexpr size_t WS_HEADER = 256;                // status word, then the slots
 static_assert(SLOT_BYTES % 16 == 0 && SL_KP % 16 == 0, "bulk copies need 16-byte alignment");
 
 // rank 0 shared memory map (bytes from the 1024-aligned base)
-constexpr int CH_IN_A = 0;                       // inbox A: the slot's first A_BYTES
-constexpr int CH_QW = CH_IN_A + SL_QW, CH_KG = CH_IN_A + SL_KG, CH_VT = CH_IN_A + SL_VT, CH_TB = CH_IN_A + SL_TB;
-constexpr int CH_DEC = CH_IN_A + SL_DEC;
-constexpr int CH_UR = 148480;                    // U^T [128 x 64] tile (TF32-rounded copy)
-constexpr int CH_IN_B = CH_UR + 32768;           // inbox B: the slot's last B_BYTES
+// Inbox A: Qg lands in rows 0..63 of the [Qg; -W] tile (one bulk load per 32-column block, so
+// that S^T [Qg; -W]^T is a single N = 128 product), the rest of the image after that tile.
+constexpr int CH_QW = 0;                         // [Qg ; -W] [128 x 128] TF32 tile (rows 64..127: -W, built here)
+constexpr int CH_A_REST = 65536;                 // the image from SL_KG on
+constexpr int CH_KG = CH_A_REST + SL_KG - SL_KG, CH_VT = CH_A_REST + SL_VT - SL_KG, CH_TB = CH_A_REST + SL_TB - SL_KG;
+constexpr int CH_DEC = CH_A_REST + SL_DEC - SL_KG;
+constexpr uint32_t A_REST_BYTES = A_BYTES - SL_KG;
+constexpr int CH_UR = 107520;                    // U^T [128 x 64] fp16 tile
+constexpr int CH_IN_B = CH_UR + 16384;           // inbox B: the slot's last B_BYTES
 constexpr int CH_KP = CH_IN_B;
-constexpr int CH_MISC = CH_IN_B + 49152;
+constexpr int CH_MISC = CH_IN_B + 24576;
 constexpr int CH_MBAR = CH_MISC, CH_FULL_A = CH_MISC + 8, CH_FULL_B = CH_MISC + 16, CH_TMEM = CH_MISC + 24;
 constexpr int CH_READY = CH_MISC + 32;           // NSLOT barriers, one per slot
 constexpr int CH_DECC = CH_MISC + 128;           // e^gC copied out of inbox A (the next A image may land early)
 constexpr int CH_END = CH_DECC + 512;
 static_assert(CH_READY + 8 * NSLOT <= CH_DECC, "barriers overlap");
-static_assert(CH_IN_A + (int)A_BYTES <= CH_UR, "inbox A overlaps");
-static_assert(CH_UR % 1024 == 0 && CH_IN_B % 1024 == 0 && CH_KG % 1024 == 0 && CH_VT % 1024 == 0 &&
-              CH_TB % 1024 == 0, "tiles must be 1024-aligned");
+static_assert(SL_KG == 32768 && CH_A_REST + (int)A_REST_BYTES <= CH_UR, "inbox A overlaps");
+static_assert(CH_QW % 1024 == 0 && CH_UR % 1024 == 0 && CH_IN_B % 1024 == 0 && CH_KG % 1024 == 0 &&
+              CH_VT % 1024 == 0 && CH_TB % 1024 == 0, "tiles must be 1024-aligned");
 constexpr int CL_SMEM_BYTES = (CH_END > M_END ? CH_END : M_END) + 1024;
 static_assert(CL_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 // rank 0 tensor memory columns: S^T, then O^T, then U^T, so that [O^T | U^T] and
@@ -157,6 +161,10 @@ __device__ __forceinline__ uint32_t slot_parity(int c) { return (uint32_t)((c / 
 // ---------------------------------------------------------------- rank 0: the state carry
 // ia, ib count the bulk loads issued on full_A, full_B (thread 0), so that a
 // failure can wait for the one that may still be landing.
+// Per chunk c, with W^T(c) and U~^T(c) already in tensor memory:
+//   -W(c) into the [Qg; -W] tile; [O^T | U^T] += S^T [Qg; -W]^T (o of chunk c - 1 is stored
+//   meanwhile); S^T decayed, U^T copied to an fp16 tile; [S^T | O^T] += U^T [Kend^T; P]^T,
+//   and right behind it on the tensor core W^T(c + 1), U~^T(c + 1) from the next inbox A.
 __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
                                           int n, const unsigned char *hslots, int &ia, int &ib) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -172,10 +180,14 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     const int64_t ring0 = (int64_t)(hslots - reinterpret_cast<const unsigned char *>(p.err));   // bytes into the workspace
     auto load_a = [&](int c) {
         ++ia;
-        const int64_t off = ring0 + (int64_t)slot_of(c) * SLOT_BYTES + SL_QW;
+        const int64_t off = ring0 + (int64_t)slot_of(c) * SLOT_BYTES + SL_QG;
         if (range_in_bounds(off, A_BYTES, p.ext.ws, p.err, p.status)) {
+            const unsigned char *src = hslots + slot_of(c) * SLOT_BYTES;
             arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
-            bulk_load(sbase + CH_IN_A, hslots + slot_of(c) * SLOT_BYTES + SL_QW, A_BYTES, sbase + CH_FULL_A);
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb)               // Qg: 64-row blocks into rows 0..63 of [Qg; -W]
+                bulk_load(sbase + CH_QW + kb * 16384, src + SL_QG + kb * 8192, 8192, sbase + CH_FULL_A);
+            bulk_load(sbase + CH_A_REST, src + SL_KG, A_REST_BYTES, sbase + CH_FULL_A);
         } else {
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sbase + CH_FULL_A) : "memory");
         }
@@ -191,6 +203,26 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         }
     };
     auto ready = [&](int c) { return sbase + CH_READY + 8 * slot_of(c); };
+    // (thread 0) W^T = Kg^T Tb^T and U~^T = V^T Tb^T of the chunk in inbox A (fp16 operands)
+    auto issue_wu = [&]() {
+        gemm16<64, 64>(tmem + T_W, sbase + CH_KG, sbase + CH_TB, false);
+        gemm16<64, 64>(tmem + T_U, sbase + CH_VT, sbase + CH_TB, false);
+    };
+    auto store_prev_o = [&](const float (&ov)[16], int cp) {
+        const int t0 = cp * C, nv = min(16, p.T - t0 - 16 * wc);
+        const int64_t off0 = obase + (int64_t)(t0 + 16 * wc) * p.o_st + trow;
+        if (p.o_f32) {
+            float *op = static_cast<float *>(p.o) + off0;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (k < nv && in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = ov[k];
+        } else {
+            __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (k < nv && in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = __float2bfloat16_rn(ov[k]);
+        }
+    };
 
     // state -> T_S = S^T: row j = trow, columns i in [32 wc, 32 wc + 32)
     {
@@ -202,72 +234,47 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         }
         tmem_st32(tmem + lane_off + T_S + 32 * wc, v);
     }
-    {
+    if (n > 0) {
         int okw = 1;
-        if (tid == 0 && n > 0) {
+        if (tid == 0) {
             okw = cl_wait(ready(0), slot_parity(0), p.polls);
             if (okw) {
                 fence_global_to_async();
                 load_a(0);
                 load_b(0);
+                okw = cl_wait(sbase + CH_FULL_A, 0u, p.polls);
             }
+            if (okw) issue_wu();
+            commit(mb.mbar);
         }
+        if (!mma_wait(mb)) return false;
         if (__syncthreads_or(!okw)) return false;
     }
     float oprev[16];                       // O^T columns 16 wc .. + 15 of the previous chunk, lane trow
     for (int c = 0; c < n; ++c) {
-        // ---------------------------------------------------------- inbox A: Qg, Kg^T, V^T, Tb, e^gC
+        // ---------------------------------------------------------- [O^T | U^T] += S^T [Qg; -W]^T
         {
-            const bool done = tid != 0 || cl_wait(sbase + CH_FULL_A, (uint32_t)(c & 1), p.polls);
-            if (__syncthreads_or(!done)) return false;
-        }
-        {
+            if (tid < DK) dec[tid] = f32p(sm, CH_DEC)[tid];
+            float w16[16];
+            tmem_ld16(tmem + lane_off + T_W + 16 * wc, w16);                 // -W [r][i] into rows 64..127
+#pragma unroll
+            for (int j = 0; j < 16; ++j) st_tile(sm, CH_QW, 128, 64 + 16 * wc + j, trow, -w16[j]);
             float z[16];
 #pragma unroll
             for (int m = 0; m < 16; ++m) z[m] = 0.f;
             tmem_st16(tmem + lane_off + T_O + 16 * wc, z);                   // O^T starts at 0
-            if (tid < DK) dec[tid] = f32p(sm, CH_DEC)[tid];
-        }
-        fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            fence_after_sync();
-            gemm<64, 64>(tmem + T_W, sbase + CH_KG, sbase + CH_TB, false);   // W^T  = Kg^T Tb^T
-            gemm<64, 64>(tmem + T_U, sbase + CH_VT, sbase + CH_TB, false);   // U~^T = V^T Tb^T
-            commit(mb.mbar);
-        }
-        if (c > 0) {                                                         // previous chunk's o
-            const int64_t off0 = obase + (int64_t)((c - 1) * C + 16 * wc) * p.o_st + trow;
-            if (p.o_f32) {
-                float *op = static_cast<float *>(p.o) + off0;
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    if (in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = oprev[k];
-            } else {
-                __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    if (in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
-            }
-        }
-        if (!mma_wait(mb)) return false;
-        {
-            float w16[16];
-            tmem_ld16(tmem + lane_off + T_W + 16 * wc, w16);                 // -W [r][i] into rows 64.. of [Qg; -W]
-#pragma unroll
-            for (int j = 0; j < 16; ++j) st_tile(sm, CH_QW, 128, 64 + 16 * wc + j, trow, -w16[j]);
         }
         fence_smem_to_async();
         fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            // [O^T | U^T] += S^T [Qg; -W]^T, S^T read from tensor memory
             fence_after_sync();
-            gemm_ts<128, 128>(tmem + T_O, tmem + T_S, sbase + CH_QW, true);
+            gemm_ts<128, 128>(tmem + T_O, tmem + T_S, sbase + CH_QW, true);   // S^T read from tensor memory
             commit(mb.mbar);
         }
+        if (c > 0) store_prev_o(oprev, c - 1);
         if (!mma_wait(mb)) return false;
-        // inbox A is free: pull the next chunk's A image now if it is already there
+        // inbox A is free (its tiles were read, e^gC copied): pull the next image now if it is there
         bool next_a = false;
         if (tid == 0 && c + 1 < n && cl_test(ready(c + 1), slot_parity(c + 1))) {
             fence_global_to_async();
@@ -281,11 +288,12 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] *= dec[i0 + k];
             tmem_st32(tmem + lane_off + T_S + i0, v);
-            float u[16];
+            float u[16], amax = 0.f;
             tmem_ld16(tmem + lane_off + T_U + 16 * wc, u);
 #pragma unroll
-            for (int k = 0; k < 16; k += 4)                                   // U^T [j][s], rounded
-                st_tile4(sm, CH_UR, 128, trow, 16 * wc + k, u[k], u[k + 1], u[k + 2], u[k + 3]);
+            for (int k = 0; k < 16; k += 4)                                   // U^T [j][s], fp16
+                st_h4(sm, CH_UR, 128, trow, 16 * wc + k, u[k], u[k + 1], u[k + 2], u[k + 3], amax);
+            if (amax > kF16Max) record_range(p.err, p.status);
         }
         fence_smem_to_async();
         fence_before_sync();
@@ -294,45 +302,34 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             const bool done = tid != 0 || cl_wait(sbase + CH_FULL_B, (uint32_t)(c & 1), p.polls);
             if (__syncthreads_or(!done)) return false;
         }
+        int okw = 1;
         if (tid == 0) {
             // [S^T | O^T] += U^T [Kend^T; P]^T
             fence_after_sync();
-            gemm<192, 64>(tmem + T_S, sbase + CH_UR, sbase + CH_KP, true);
-            commit(mb.mbar);
+            gemm16<192, 64>(tmem + T_S, sbase + CH_UR, sbase + CH_KP, true);
             // both images of chunk c have landed (their bulk loads completed, which this
             // thread observed): its slot may be rewritten.  Nothing else to order, so no release.
             remote_arrive_relaxed(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) % NSLOTP), owner_of(c)));
+            if (c + 1 < n) {
+                // the next chunk's W^T, U~^T queue behind it on the tensor core
+                if (!next_a) {
+                    okw = cl_wait(ready(c + 1), slot_parity(c + 1), p.polls);
+                    if (okw) {
+                        fence_global_to_async();
+                        load_a(c + 1);
+                    }
+                }
+                if (okw) okw = cl_wait(sbase + CH_FULL_A, (uint32_t)((c + 1) & 1), p.polls);
+                if (okw) issue_wu();
+            }
+            commit(mb.mbar);
         }
         if (!mma_wait(mb)) return false;
         tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);
-        int okw = 1;
-        if (tid == 0 && c + 1 < n) {
-            if (!next_a) {
-                okw = cl_wait(ready(c + 1), slot_parity(c + 1), p.polls);
-                if (okw) {
-                    fence_global_to_async();
-                    load_a(c + 1);
-                }
-            }
-            if (okw) load_b(c + 1);
-        }
+        if (tid == 0 && okw && c + 1 < n) load_b(c + 1);                   // inbox B was read
         if (__syncthreads_or(!okw)) return false;
     }
-    if (n > 0) {                                                             // last chunk's o
-        const int t0 = (n - 1) * C, nv = min(16, p.T - t0 - 16 * wc);
-        const int64_t off0 = obase + (int64_t)(t0 + 16 * wc) * p.o_st + trow;
-        if (p.o_f32) {
-            float *op = static_cast<float *>(p.o) + off0;
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                if (k < nv && in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = oprev[k];
-        } else {
-            __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                if (k < nv && in_bounds(off0 + k * p.o_st, p.ext.o, p.err, p.status)) op[k * p.o_st] = __float2bfloat16_rn(oprev[k]);
-        }
-    }
+    if (n > 0) store_prev_o(oprev, n - 1);                                 // last chunk's o
     float v[32];
     tmem_ld32(tmem + lane_off + T_S + 32 * wc, v);
 #pragma unroll
@@ -383,10 +380,9 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             int okw = 1;
             if (k >= NSLOTP) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1), p.polls);
             if (okw) {
-                // Qg (64-row tile: 8 KB per K block) into rows 0..63 of [Qg; -W]; Kg^T; e^gC
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb) ring_store(p, slot + SL_QW + kb * 16384, sbase + R_B + kb * 8192, 8192);
-                ring_store(p, slot + SL_KG, sbase + R_C, 32768);
+                // Qg, Kg^T, e^gC
+                ring_store(p, slot + SL_QG, sbase + R_B, 32768);
+                ring_store(p, slot + SL_KG, sbase + R_C, 16384);
                 ring_store(p, slot + SL_DEC, sbase + M_DEC, 512);
                 bulk_commit();
             }
@@ -396,14 +392,13 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         if (*slot_ok == 0) return false;
         if (tid == kIO) {
             // P (64-row tile) into rows 128..191 of [Kend^T; P]; V^T
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) ring_store(p, slot + SL_KP + kb * 24576 + 16384, sbase + R_F + kb * 8192, 8192);
-            ring_store(p, slot + SL_VT, sbase + A1_VT, 32768);
+            ring_store(p, slot + SL_KP + 16384, sbase + R_F, 8192);
+            ring_store(p, slot + SL_VT, sbase + A1_VT, 16384);
             bulk_commit();
         }
-        solve_tb(sm);
+        solve_tb(sm, cr.amax);
         if (tid == kIO) {
-            ring_store(p, slot + SL_TB, sbase + R_G, 16384);
+            ring_store(p, slot + SL_TB, sbase + R_G, 8192);
             bulk_commit();
             bulk_wait_read<0>();                                           // R_B, R_C, R_F, A1_VT, R_G read
         }
@@ -418,17 +413,17 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {
                 const int s0 = 16 * cq + jj;
-                st_tile4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
-                         ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc,
-                         ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc);
+                st_h4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
+                      ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc,
+                      ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc, cr.amax);
             }
+            if (cr.amax > kF16Max) record_range(p.err, p.status);
         }
         fence_smem_to_async();
         __syncthreads();
         if (tid == kIO) {
-            // Kend^T (128-row tile: 16 KB per K block) into rows 0..127 of [Kend^T; P]
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) ring_store(p, slot + SL_KP + kb * 24576, sbase + R_C + kb * 16384, 16384);
+            // Kend^T into rows 0..127 of [Kend^T; P]
+            ring_store(p, slot + SL_KP, sbase + R_C, 16384);
             bulk_commit();
         }
         if (tn < p.T) st.stage<STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, tn);        // A2 is free

@@ -1,4 +1,4 @@
-// Chunked prefill on the fifth-generation tensor cores (tcgen05, TF32
+// Chunked prefill on the fifth-generation tensor cores (tcgen05, TF32 and fp16
 // operands, fp32 accumulators in tensor memory), dk = dv = 128, chunk 64:
 // one CTA per (batch, v-head) walks its chunks in order, with the state in
 // tensor memory as S^T [dv x dk] for the whole sequence.
@@ -7,9 +7,9 @@
 // gated delta rule" (executorch PR #21061, Summary); the per-chunk phases
 // that do not touch the state (decay prefix, operand tiles, causal terms,
 // triangular transform) are in prefill_tc05_chunk.cuh and shared with the
-// cluster kernel.  TF32 operands (rounded to nearest) with fp32 accumulation
-// keep the error near 1e-2 of the output RMS or below; the state is carried
-// in fp32.
+// cluster kernel.  TF32 and fp16 operands (rounded to nearest; the same 10
+// mantissa bits) with fp32 accumulation keep the error near 1e-2 of the output
+// RMS or below; the state is carried in fp32.
 #include <mutex>
 
 #include "prefill_tc05_chunk.cuh"
@@ -76,12 +76,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
         if (!(ok = st.wait(sbase, p.polls, p.inject && t0 == 0))) break;
         prep_chunk<true>(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
         if (!(ok = causal_terms<false>(sm, tmem, mb, cr, sm + R_F, 64, 0))) break;
-        solve_tb(sm);
-        // ------------------------------------------------------------ W^T, U~^T
+        solve_tb(sm, cr.amax);
+        // ------------------------------------------------------------ W^T, U~^T (fp16 operands)
         if (tid == 0) {
             fence_after_sync();
-            gemm<64, 64>(tmem + T_D2, sbase + R_C, sbase + R_G, false);    // W^T  = Kg^T Tb^T
-            gemm<64, 64>(tmem + T_D3, sbase + A1_VT, sbase + R_G, false);  // U~^T = V^T Tb^T
+            gemm16<64, 64>(tmem + T_D2, sbase + R_C, sbase + R_G, false);    // W^T  = Kg^T Tb^T
+            gemm16<64, 64>(tmem + T_D3, sbase + A1_VT, sbase + R_G, false);  // U~^T = V^T Tb^T
             commit(mb.mbar);
         }
         if (!(ok = mma_wait(mb))) break;
@@ -117,14 +117,15 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
             tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, v);
 #pragma unroll
             for (int c = 0; c < 16; c += 4)                                                  // U^T [j][s]
-                st_tile4(sm, R_A1, 128, trow, 16 * wc + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
+                st_h4(sm, R_A1, 128, trow, 16 * wc + c, v[c], v[c + 1], v[c + 2], v[c + 3], cr.amax);
             const float sc = cr.wide ? 1.f : __expf(cr.gcv - cr.gm);
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4) {                                             // Kend^T [i][s]
                 const int s0 = 16 * cq + jj;
-                st_tile4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc,
-                         ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc);
+                st_h4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc,
+                      ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc, cr.amax);
             }
+            if (cr.amax > kF16Max) record_range(p.err, p.status);
         }
         fence_smem_to_async();
         fence_before_sync();
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
         // ------------------------------------------------------------ O^T += U^T P^T ; S^T += U^T Kend
         if (tid == 0) {
             fence_after_sync();
-            gemm<64, 64>(tmem + T_D4, sbase + R_A1, sbase + R_F, true);
-            gemm<128, 64>(tmem + T_D0, sbase + R_A1, sbase + R_C, true);
+            gemm16<64, 64>(tmem + T_D4, sbase + R_A1, sbase + R_F, true);
+            gemm16<128, 64>(tmem + T_D0, sbase + R_A1, sbase + R_C, true);
             commit(mb.mbar);
         }
         if (!(ok = mma_wait(mb))) break;

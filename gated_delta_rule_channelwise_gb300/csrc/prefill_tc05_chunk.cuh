@@ -22,9 +22,17 @@
 // magnitude on every channel.  A chunk outside that range forms A and P on
 // the CUDA cores from exponentials of differences instead (exact for any
 // decay).
+//
+// Operand precision.  D1's anchored factors span up to e^80 and the state products read S^T
+// and -W, Qg as TF32 (the first fp32 range, the others kept as they were measured); the other
+// products (D2, the V^T part of D3, and U^T . [P^T | Kend]) take fp16 tiles, which round like
+// TF32 (10 mantissa bits) for values below 65504 in magnitude, move half the bytes and run at
+// twice the rate.  Every fp16 value is checked against that range; a chunk that would overflow
+// it records CGDR_ERR_RANGE.
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "cgdr_internal.cuh"
 #include "tc05.cuh"
@@ -39,12 +47,12 @@ constexpr float kRange = 80.f;           // max |gamma_r - gamma_mid| for the te
 constexpr uint32_t kSpin = kDefaultPolls;   // bounded mbarrier wait (polls) of the drains after a failure
 
 // shared memory map of a CTA that prepares chunks (bytes from a 1024-aligned base)
-constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, V^T | U^T ; wide: q~, k~
+constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, V^T (fp16) | U^T (fp16) ; wide: q~, k~
 constexpr int R_A2 = 65536;              // 32 KB: X2 (kn e^(gm-g)), the source of Kend ; wide: gamma
 constexpr int R_B = 98304;               // 32 KB: Qg = qn e^g            [64 x 128]
-constexpr int R_C = 131072;              // 32 KB: Kg^T [128 x 64] | -W [64 x 128] | Kend^T [128 x 64]
-constexpr int R_F = 163840;              // 16 KB: P  [64 x 64]
-constexpr int R_G = 180224;              // 16 KB: Xs fp32 [64][64] | Tb [64 x 64]
+constexpr int R_C = 131072;              // 32 KB: Kg^T [128 x 64] (fp16) | -W [64 x 128] | Kend^T [128 x 64] (fp16)
+constexpr int R_F = 163840;              // 16 KB: P  [64 x 64] (fp16)
+constexpr int R_G = 180224;              // 16 KB: Xs fp32 [64][64] | Tb [64 x 64] (fp16)
 constexpr int R_MISC = 196608;
 // misc (fp32 unless noted)
 constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BETA + 256;
@@ -130,6 +138,30 @@ __device__ __forceinline__ void st_raw4(char *base, int region, int R, int r, in
 }
 __device__ __forceinline__ float ld_tile(const char *base, int region, int R, int r, int k) {
     return *reinterpret_cast<const float *>(base + region + sw_off(R, r, k));
+}
+// Four consecutive K elements (k0 % 4 == 0) of row r of an fp16 tile, rounded to nearest: one
+// 8-byte store.  amax keeps the largest magnitude stored, for the range check.
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) {
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+__device__ __forceinline__ void st_h4(char *base, int region, int R, int r, int k0, float a, float b, float c,
+                                      float d, float &amax) {
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a), fabsf(b)), fmaxf(fabsf(c), fabsf(d))));
+    *reinterpret_cast<uint2 *>(base + region + sw_off16(R, r, k0)) =
+        make_uint2(h2_bits(__floats2half2_rn(a, b)), h2_bits(__floats2half2_rn(c, d)));
+}
+__device__ __forceinline__ void st_h(char *base, int region, int R, int r, int k, float x, float &amax) {
+    amax = fmaxf(amax, fabsf(x));
+    *reinterpret_cast<__half *>(base + region + sw_off16(R, r, k)) = __float2half_rn(x);
+}
+// Largest magnitude an fp16 operand may take (the largest finite fp16).
+constexpr float kF16Max = 65504.f;
+// Records an fp16 operand out of range (one thread per CTA, or any thread: idempotent).
+__device__ __forceinline__ void record_range(int *err, int *status) {
+    atomicExch(err, (int)CGDR_ERR_RANGE);
+    if (status != nullptr) atomicExch(status, (int)CGDR_ERR_RANGE);
 }
 
 // This CTA's (batch, v-head) and the bases of its input rows.
@@ -281,6 +313,7 @@ struct ChunkRegs {
     float vreg[16];                      // v column ci at those rows
     float gm, gcv;                       // prefix at the anchor row 32 and at the chunk's end
     bool wide;                           // the chunk's decay range is beyond kRange
+    float amax;                          // largest magnitude this thread stored into an fp16 tile
 };
 
 // Row norms, beta, the log-decay prefix and the decay-scaled operand tiles of
@@ -388,6 +421,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
         }
     }
     const float gm = cr.gm;
+    cr.amax = 0.f;
     // v column ci for this thread's 16 rows (staged), read before B is reused for Qg
     {
         const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_V);
@@ -424,7 +458,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
             st_raw(qg, 0, qg_rows, r, ci, qt * eg);           // Qg [r][i] (taken as TF32 by truncation)
             kg4[jj & 3] = kt * eg;
-            if ((jj & 3) == 3) st_raw4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3]);    // Kg^T [i][s]
+            if ((jj & 3) == 3) st_h4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3], cr.amax);   // Kg^T [i][s]
             if (!wide) {
                 const float e2 = __expf(gm - cr.lam[jj]);
                 st_tile(sm, R_A1, 128, r, ci, be4[jj & 3] * kt * e1);   // X1 rows 0..63
@@ -449,7 +483,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
 // V^T into A1_VT.  False if a tensor-core wait gave up.
 // kBulkOut: P and V^T leave by bulk copy, so fence them for the async proxy.
 template <bool kBulkOut>
-__device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, const ChunkRegs &cr, char *pt,
+__device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, ChunkRegs &cr, char *pt,
                                              int pt_rows, int pt_row0) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;
@@ -478,8 +512,8 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
 #pragma unroll
             for (int c = 0; c < 16; c += 4) {
                 const int s = 16 * wc + c;
-                st_tile4(pt, 0, pt_rows, pt_row0 + r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
-                         s + 2 <= r ? v[c + 2] : 0.f, s + 3 <= r ? v[c + 3] : 0.f);
+                st_h4(pt, 0, pt_rows, pt_row0 + r, s, s <= r ? v[c] : 0.f, s + 1 <= r ? v[c + 1] : 0.f,
+                      s + 2 <= r ? v[c + 2] : 0.f, s + 3 <= r ? v[c + 3] : 0.f, cr.amax);
             }
         }
     } else {
@@ -516,14 +550,13 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
         for (int e = 0; e < 8; ++e) {
             const int idx = tid + NT * e, r = idx >> 6, s = idx & 63;
             sA[r * LDA + s] = ra[e];
-            st_tile(pt, 0, pt_rows, pt_row0 + r, s, rp[e]);
+            st_h(pt, 0, pt_rows, pt_row0 + r, s, rp[e], cr.amax);
         }
     }
-    // V^T [j][s] (exact: bf16 values are TF32 values)
+    // V^T [j][s] (exact in fp16 for bf16 values of magnitude 2^-14 .. 65504)
 #pragma unroll
     for (int jj = 0; jj < 16; jj += 4)
-        *reinterpret_cast<float4 *>(sm + A1_VT + sw_off(128, ci, 16 * cq + jj)) =
-            make_float4(cr.vreg[jj], cr.vreg[jj + 1], cr.vreg[jj + 2], cr.vreg[jj + 3]);
+        st_h4(sm, A1_VT, 128, ci, 16 * cq + jj, cr.vreg[jj], cr.vreg[jj + 1], cr.vreg[jj + 2], cr.vreg[jj + 3], cr.amax);
     if (kBulkOut) fence_smem_to_async();
     __syncthreads();
     return true;
@@ -534,13 +567,13 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
 // eight different rows hits eight different bank groups.
 __device__ __forceinline__ int xs_off(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
 
-// Tb = (I + A)^-1 Diag(beta) into R_G as a TF32 tile, by 16 x 16 blocks:
+// Tb = (I + A)^-1 Diag(beta) into R_G as an fp16 tile, by 16 x 16 blocks:
 // X_RR = (I + A_RR)^-1 by forward substitution (four blocks at once), then
 // Z_Rm = X_RR A_Rm for the six pairs m < R, then X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS
 // one block diagonal at a time.  Each thread of the product steps owns four
 // consecutive columns of one row (float4 loads).  Ends with Tb fenced for the
 // tensor core.
-__device__ __forceinline__ void solve_tb(char *sm) {
+__device__ __forceinline__ void solve_tb(char *sm, float &amax) {
     const int tid = threadIdx.x;
     const float *sA = f32p(sm, A1_A32), *sBeta = f32p(sm, M_BETA);
     float *sZ = f32p(sm, A1_Z), *sXs = f32p(sm, R_G);
@@ -622,7 +655,7 @@ __device__ __forceinline__ void solve_tb(char *sm) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
-            st_tile4(sm, R_G, 64, r, s2, tv[e].x, tv[e].y, tv[e].z, tv[e].w);
+            st_h4(sm, R_G, 64, r, s2, tv[e].x, tv[e].y, tv[e].z, tv[e].w, amax);
         }
     }
     fence_smem_to_async();

@@ -1,7 +1,7 @@
 // Blackwell (sm_100 family) fifth-generation tensor core helpers: tcgen05.mma
 // with operands in shared memory and the accumulator in tensor memory (TMEM).
 //
-// Operand tiles are fp32 values rounded to TF32, stored K-major with the
+// TF32 operand tiles are fp32 values rounded to TF32, stored K-major with the
 // 128-byte swizzle: a tile of R rows and K columns is split into K/32 blocks
 // of 32 fp32 (128 bytes per row); each block is R x 128 bytes, contiguous,
 // 1024-byte aligned; inside a row the sixteen-byte chunk c sits at chunk
@@ -83,6 +83,42 @@ __device__ __forceinline__ void gemm_ts(uint32_t d_tmem, uint32_t a_tmem, uint32
     for (int ks = 0; ks < K / 8; ++ks) {
         const uint64_t b = bd + (uint64_t)((ks >> 2) * (N * 128 / 16) + (ks & 3) * 2);
         mma_tf32_ts(d_tmem, a_tmem + 8 * ks, b, idesc, (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
+// fp16 operand tiles.  fp16 carries the same 10 explicit mantissa bits as TF32, so for values
+// well inside its range (|x| < 65504) it rounds no worse than TF32 in absolute terms, at half
+// the bytes and twice the tensor-core rate.  Same K-major 128-byte swizzle: a block holds 64
+// halves per row, and one instruction consumes K = 16 (32 bytes), so the descriptor steps are
+// those of the TF32 tiles.
+__host__ __device__ __forceinline__ uint32_t sw_off16(int R, int r, int k) {
+    const int kb = k >> 6, c = (k & 63) >> 3;
+    return (uint32_t)(kb * R * 128 + r * 128 + ((c ^ (r & 7)) << 4) + ((k & 7) << 1));
+}
+
+// Instruction descriptor: D fp32, A and B fp16 (both K-major), M = 128.
+__host__ __device__ constexpr uint32_t idesc_f16(int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// D[128 x N] (+)= A[128 x K] * B[N x K]^T with fp16 tiles (128 and N rows).
+template <int N, int K>
+__device__ __forceinline__ void gemm16(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, bool accumulate) {
+    constexpr uint32_t idesc = idesc_f16(N);
+    const uint64_t ad = smem_desc(a_smem), bd = smem_desc(b_smem);
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks) {
+        constexpr int kAStep = 128 * 128 / 16, kBStep = N * 128 / 16;
+        const uint64_t a = ad + (uint64_t)((ks >> 2) * kAStep + (ks & 3) * 2);
+        const uint64_t b = bd + (uint64_t)((ks >> 2) * kBStep + (ks & 3) * 2);
+        mma_f16(d_tmem, a, b, idesc, (accumulate || ks > 0) ? 1u : 0u);
     }
 }
 

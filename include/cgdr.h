@@ -72,8 +72,13 @@ typedef enum cgdr_status {
     CGDR_ERR_WORKSPACE = 4,     /* workspace smaller than cgdr_prefill_workspace_size() */
     CGDR_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
     CGDR_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (reported through a status word) */
-    CGDR_ERR_BOUNDS = 7         /* debug build only: a device-side index check failed (through a status
+    CGDR_ERR_BOUNDS = 7,        /* debug build only: a device-side index check failed (through a status
                                    word); the access was skipped */
+    CGDR_ERR_RANGE = 8          /* a tensor-core prefill met a value of magnitude above 65504 in one of
+                                   its fp16 operands (v, the triangular transform, U, or a
+                                   decay-scaled key or query when g > 0 grows them); reported through
+                                   the status words, the outputs are then invalid: run that call with
+                                   CGDR_PREFILL_SIMT */
 } cgdr_status;
 
 typedef enum cgdr_dtype { CGDR_F32 = 0, CGDR_BF16 = 1 } cgdr_dtype;
@@ -109,7 +114,8 @@ typedef struct cgdr_args {
     float *state;                                       /* [B,Hv,dk,dv] in/out */
     void *o;           int64_t o_sb, o_st, o_sh;        /* [B,T,Hv,dv] out, o_dtype */
     int32_t *status;   /* optional DEVICE int32: a kernel whose bounded wait gave up stores
-                          CGDR_ERR_TIMEOUT here (its outputs are then invalid).  The library never
+                          CGDR_ERR_TIMEOUT here, a tensor-core prefill whose fp16 operand left
+                          the fp16 range CGDR_ERR_RANGE (its outputs are then invalid).  The library never
                           clears it: zero it before the calls it should cover.  NULL: not reported
                           (the prefill workspace keeps its own status word either way) */
 } cgdr_args;
@@ -146,8 +152,8 @@ cgdr_status cgdr_decode(const cgdr_args *args, void *stream);
 /*
  * Bytes of device workspace cgdr_prefill needs for `args` (may be 0): 0 for
  * the CUDA-core kernel, 256 for the per-head tensor-core kernel (a status
- * word), and 256 + B * Hv * 1774080 for the cluster kernel (the status word,
- * then nine 197120-byte hand-off slots per (batch, v-head)).  Depends on the
+ * word), and 256 + B * Hv * 889344 for the cluster kernel (the status word,
+ * then nine 98816-byte hand-off slots per (batch, v-head)).  Depends on the
  * kernel cgdr_prefill_path_for reports.  The workspace plays the part of the
  * single scratch arena of "Add parallel chunked prefill for channelwise gated
  * delta rule" (Summary), sliced per (batch, head) unit.  Returns 0 for
@@ -166,12 +172,14 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
  * Paths: 1 <= T <= 8 runs the token recurrence itself (the decode kernel
  * stepping through the tokens, each state tile read once and written once;
  * the chunk length plays no part); otherwise bf16 inputs with dk = dv = 128
- * and chunk 64 run one of the two tensor-core kernels (tcgen05, TF32
- * operands, fp32 accumulation and state), and every other case an fp32
+ * and chunk 64 run one of the two tensor-core kernels (tcgen05; TF32 operands
+ * for the anchored causal terms and the state products, fp16 operands for the
+ * others, fp32 accumulation and state), and every other case an fp32
  * CUDA-core kernel; args->prefill_path can force a kernel for this call.
  * Workspace: the tensor-core path needs cgdr_prefill_workspace_size() bytes
  * (16-byte aligned); its first int32 is set to CGDR_ERR_TIMEOUT if a bounded
- * device wait gave up (see cgdr_workspace_status).  `workspace` may be NULL
+ * device wait gave up, or to CGDR_ERR_RANGE if an fp16 operand left the fp16
+ * range (see cgdr_workspace_status).  `workspace` may be NULL
  * when the size is 0.  Returns CGDR_ERR_WORKSPACE if it is too small.
  */
 cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspace_bytes, void *stream);
@@ -210,8 +218,9 @@ int cgdr_prefill_path_for(const cgdr_args *args);
 
 /*
  * Waits for `stream`, then reports the device-side status a cgdr_prefill
- * call left in `workspace`: CGDR_OK, or CGDR_ERR_TIMEOUT if one of its
- * bounded waits on the tensor core gave up (its outputs are then invalid).
+ * call left in `workspace`: CGDR_OK, CGDR_ERR_TIMEOUT if one of its bounded
+ * waits on the tensor core gave up, or CGDR_ERR_RANGE if an fp16 operand left
+ * the fp16 range (in both cases its outputs are invalid).
  * Returns CGDR_ERR_CUDA if the copy or the synchronisation fails.
  */
 cgdr_status cgdr_workspace_status(const void *workspace, void *stream);
@@ -240,8 +249,9 @@ cgdr_status cgdr_workspace_status(const void *workspace, void *stream);
  * the last call's contents; the call clears what must start at zero before
  * its kernel runs.  Calls whose kernels overlap on the GPU (other streams,
  * other host threads) race on the array: serialise them.  A device-side
- * wait that gives up is recorded in the static area, which the caller cannot
- * read, and in args->status when that is given.
+ * wait that gives up, or an fp16 operand out of range, is recorded in the
+ * static area, which the caller cannot read, and in args->status when that
+ * is given.
  *
  * Arguments and results are those of cgdr_prefill, except that a choice of
  * the cluster kernel (automatic or forced) runs the per-head tensor-core

@@ -69,7 +69,7 @@ def test_debug_library_builds_and_exports_every_declared_symbol():
 def test_abi_version_and_status_strings(lib):
     m = re.search(r"#define CGDR_ABI_VERSION (\d+)", open(HEADER).read())
     assert lib.cgdr_abi_version() == int(m.group(1))
-    for s in range(8):
+    for s in range(9):
         assert cg.status_string(s).startswith("CGDR_")
     assert cg.status_string(99) == "unknown cgdr status"
 
@@ -215,7 +215,7 @@ def test_prefill_path_choice(lib):
     A = _args(T=100, prefill_path=cg.PREFILL_PER_HEAD)
     assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 256
     A = _args(T=100, prefill_path=cg.PREFILL_CLUSTER)
-    need = 256 + A.B * A.Hv * 9 * 197120
+    need = 256 + A.B * A.Hv * 9 * 98816
     assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == need
     assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
     assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(1 << 30), need - 16, None) == cg.ERR_WORKSPACE
@@ -237,7 +237,7 @@ def test_calls_from_two_threads_do_not_interfere(lib):
                 return
 
     ts = [threading.Thread(target=worker, args=(cg.PREFILL_PER_HEAD, 256)),
-          threading.Thread(target=worker, args=(cg.PREFILL_CLUSTER, 256 + 2 * 4 * 9 * 197120)),
+          threading.Thread(target=worker, args=(cg.PREFILL_CLUSTER, 256 + 2 * 4 * 9 * 98816)),
           threading.Thread(target=worker, args=(cg.PREFILL_SIMT, 0))]
     for t in ts:
         t.start()

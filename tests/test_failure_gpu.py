@@ -110,3 +110,44 @@ def test_prefill_per_head_wait_gives_up(gate):
     o_ref, S_ref = oracle_run(inp)
     assert rel_err(o, o_ref) <= TOL[torch.bfloat16]
     assert rel_err(state, S_ref) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER])
+def test_fp16_operand_range(path):
+    """The tensor-core kernels carry some products in fp16 operands.  Inputs well inside the
+    fp16 range report CGDR_OK; a v of magnitude 1e5 (a valid bf16 value beyond the largest
+    fp16, 65504) reports CGDR_ERR_RANGE through both status words, and the fp32 CUDA-core
+    kernel -- the remedy the header names -- runs the same call to the oracle's result."""
+    w, inp = _inputs(200, H=2, seed=12)
+    ref_ws = None
+    for big in (False, True):
+        v = inp["v"].clone()
+        if big:
+            v[0, 100, 1, 7] = 1.0e5
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(cg.prefill_workspace_size(inp["q"], inp["k"], v, inp["S0"],
+                                                   torch.empty(v.shape, device="cuda"), path=path, chunk=64,
+                                                   **gate_kwargs(inp)) + 256, dtype=torch.uint8, device="cuda")
+        state = inp["S0"].clone()
+        cg.prefill(inp["q"], inp["k"], v, state, chunk=64, path=path, workspace=ws, status=st, **gate_kwargs(inp))
+        torch.cuda.synchronize()
+        want = cg.ERR_RANGE if big else cg.OK
+        assert int(st.item()) == want and cg.workspace_status(ws) == want
+        if big:
+            state = inp["S0"].clone()
+            o = cg.prefill(inp["q"], inp["k"], v, state, chunk=64, path=cg.PREFILL_SIMT, **gate_kwargs(inp))
+            o_ref, S_ref = oracle_run(dict(inp, v=v))
+            assert rel_err(o, o_ref) <= TOL[torch.bfloat16] and rel_err(state, S_ref) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER])
+def test_growing_gate_range(path):
+    """A positive log-decay (a gate that grows the state) scales keys by e^(sum of g); 64 tokens of
+    g = +0.5 reach e^32, beyond fp16: CGDR_ERR_RANGE, not a silent overflow."""
+    w, inp = _inputs(128, H=1, seed=13)
+    g = torch.full_like(inp["g"], 0.5)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    state = inp["S0"].clone()
+    cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=path, status=st, g=g, beta=inp["beta"])
+    torch.cuda.synchronize()
+    assert int(st.item()) == cg.ERR_RANGE
