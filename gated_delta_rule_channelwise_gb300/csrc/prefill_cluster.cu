@@ -13,8 +13,8 @@
 //   ranks 1..3 (preparers) take chunks round robin (chunk c on rank
 //                          1 + c % 3) and run the state-free phases.
 // Hand-off through L2: a preparer sends the tiles it has built in shared
-// memory -- Qg (TF32), Kg^T, V^T, Tb (fp16), e^gC (inbox A image) and Kend^T,
-// P (fp16, inbox B image) -- with bulk stores into one of its three slots of a ring in the
+// memory -- Qg, Kg^T, V^T, Tb, e^gC (inbox A image) and Kend^T, P (inbox B
+// image), fp16 tiles -- with bulk stores into one of its three slots of a ring in the
 // workspace, each piece at its place in rank 0's shared-memory tile layout,
 // and arrives on rank 0's ready barrier for that slot; rank 0 pulls each
 // image into its inbox with one bulk load as soon as the inbox is free, and
@@ -38,12 +38,12 @@ using namespace tc05c;
 constexpr int CLUSTER = 4, NPREP = CLUSTER - 1, NSLOTP = 3, NSLOT = NSLOTP * NPREP;   // NSLOTP slots per preparer
 
 // one hand-off slot (bytes): the inbox A image, then the inbox B image
-constexpr int SL_QG = 0;                         // Qg   [64 x 128] TF32 tile
-constexpr int SL_KG = 32768;                     // Kg^T [128 x 64] fp16 tile
-constexpr int SL_VT = 49152;                     // V^T  [128 x 64] fp16 tile
-constexpr int SL_TB = 65536;                     // Tb   [64 x 64] fp16 tile
-constexpr int SL_DEC = 73728;                    // e^gC [128] fp32
-constexpr uint32_t A_BYTES = 73728 + 512;
+constexpr int SL_QG = 0;                         // Qg   [64 x 128] fp16 tile
+constexpr int SL_KG = 16384;                     // Kg^T [128 x 64] fp16 tile
+constexpr int SL_VT = 32768;                     // V^T  [128 x 64] fp16 tile
+constexpr int SL_TB = 49152;                     // Tb   [64 x 64] fp16 tile
+constexpr int SL_DEC = 57344;                    // e^gC [128] fp32
+constexpr uint32_t A_BYTES = 57344 + 512;
 constexpr int SL_KP = (int)A_BYTES;              // [Kend^T ; P] [192 x 64] fp16 tile (rows 0..127 Kend^T, 128..191 P)
 constexpr uint32_t B_BYTES = 24576;
 constexpr size_t SLOT_BYTES = A_BYTES + B_BYTES;
@@ -51,30 +51,30 @@ constexpr size_t WS_HEADER = 256;                // status word, then the slots
 static_assert(SLOT_BYTES % 16 == 0 && SL_KP % 16 == 0, "bulk copies need 16-byte alignment");
 
 // rank 0 shared memory map (bytes from the 1024-aligned base)
-// Inbox A: Qg lands in rows 0..63 of the [Qg; -W] tile (one bulk load per 32-column block, so
+// Inbox A: Qg lands in rows 0..63 of the [Qg; -W] tile (one bulk load per 64-column block, so
 // that S^T [Qg; -W]^T is a single N = 128 product), the rest of the image after that tile.
-constexpr int CH_QW = 0;                         // [Qg ; -W] [128 x 128] TF32 tile (rows 64..127: -W, built here)
-constexpr int CH_A_REST = 65536;                 // the image from SL_KG on
+constexpr int CH_QW = 0;                         // [Qg ; -W] [128 x 128] fp16 tile (rows 64..127: -W, built here)
+constexpr int CH_A_REST = 32768;                 // the image from SL_KG on
 constexpr int CH_KG = CH_A_REST + SL_KG - SL_KG, CH_VT = CH_A_REST + SL_VT - SL_KG, CH_TB = CH_A_REST + SL_TB - SL_KG;
 constexpr int CH_DEC = CH_A_REST + SL_DEC - SL_KG;
 constexpr uint32_t A_REST_BYTES = A_BYTES - SL_KG;
-constexpr int CH_UR = 107520;                    // U^T [128 x 64] fp16 tile
+constexpr int CH_UR = 74752;                     // U^T [128 x 64] fp16 tile
 constexpr int CH_IN_B = CH_UR + 16384;           // inbox B: the slot's last B_BYTES
 constexpr int CH_KP = CH_IN_B;
 constexpr int CH_MISC = CH_IN_B + 24576;
 constexpr int CH_MBAR = CH_MISC, CH_FULL_A = CH_MISC + 8, CH_FULL_B = CH_MISC + 16, CH_TMEM = CH_MISC + 24;
 constexpr int CH_READY = CH_MISC + 32;           // NSLOT barriers, one per slot
-constexpr int CH_DECC = CH_MISC + 128;           // e^gC copied out of inbox A (the next A image may land early)
-constexpr int CH_END = CH_DECC + 512;
-static_assert(CH_READY + 8 * NSLOT <= CH_DECC, "barriers overlap");
-static_assert(SL_KG == 32768 && CH_A_REST + (int)A_REST_BYTES <= CH_UR, "inbox A overlaps");
+constexpr int CH_OST = CH_MISC + 1024;           // o of one chunk [64 tokens][128] in o's dtype (TMA store source)
+constexpr int CH_END = CH_OST + 32768;
+static_assert(CH_READY + 8 * NSLOT <= CH_MISC + 128, "barriers overlap");
+static_assert(SL_KG == 16384 && CH_A_REST + (int)A_REST_BYTES <= CH_UR, "inbox A overlaps");
 static_assert(CH_QW % 1024 == 0 && CH_UR % 1024 == 0 && CH_IN_B % 1024 == 0 && CH_KG % 1024 == 0 &&
               CH_VT % 1024 == 0 && CH_TB % 1024 == 0, "tiles must be 1024-aligned");
 constexpr int CL_SMEM_BYTES = (CH_END > M_END ? CH_END : M_END) + 1024;
 static_assert(CL_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 // rank 0 tensor memory columns: S^T, then O^T, then U^T, so that [O^T | U^T] and
-// [S^T | O^T] are each one accumulator of a single MMA; W^T after them
-constexpr uint32_t T_S = 0, T_O = 128, T_U = 192, T_W = 256;
+// [S^T | O^T] are each one accumulator of a single MMA; W^T and the fp16 copy of S^T after them
+constexpr uint32_t T_S = 0, T_O = 128, T_U = 192, T_W = 256, T_S16 = 320;
 
 // ---------------------------------------------------------------- cluster and bulk-copy primitives
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -141,6 +141,11 @@ __device__ __forceinline__ void ring_store(const Tc05Params &p, char *dst, uint3
     if (range_in_bounds(off, bytes, p.ext.ws, p.err, p.status)) bulk_store(dst, src, bytes);
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// TMA tensor store of the box at (0, token t0, head, batch) of map tm from this CTA's shared memory.
+__device__ __forceinline__ void tma_store_tile(const CUtensorMap *tm, uint32_t src, int t0, int head, int b) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(t0), "r"(head), "r"(b), "r"(src) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_store_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -159,12 +164,14 @@ __device__ __forceinline__ int slot_of(int c) { return NSLOTP * (c % NPREP) + (c
 __device__ __forceinline__ uint32_t slot_parity(int c) { return (uint32_t)((c / NPREP / NSLOTP) & 1); }
 
 // ---------------------------------------------------------------- rank 0: the state carry
+constexpr int kOIO = 32;                         // rank 0: issues and waits for the TMA stores of o
 // ia, ib count the bulk loads issued on full_A, full_B (thread 0), so that a
 // failure can wait for the one that may still be landing.
 // Per chunk c, with W^T(c) and U~^T(c) already in tensor memory:
-//   -W(c) into the [Qg; -W] tile; [O^T | U^T] += S^T [Qg; -W]^T (o of chunk c - 1 is stored
-//   meanwhile); S^T decayed, U^T copied to an fp16 tile; [S^T | O^T] += U^T [Kend^T; P]^T,
-//   and right behind it on the tensor core W^T(c + 1), U~^T(c + 1) from the next inbox A.
+//   S^T copied to fp16 (S16) and decayed; -W(c) into the [Qg; -W] tile; [O^T | U^T] +=
+//   S16 [Qg; -W]^T (o of chunk c - 1 is stored meanwhile); U^T copied to an fp16 tile;
+//   [S^T | O^T] += U^T [Kend^T; P]^T, and right behind it on the tensor core W^T(c + 1),
+//   U~^T(c + 1) from the next inbox A.
 __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
                                           int n, const unsigned char *hslots, int &ia, int &ib) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -175,7 +182,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     const int64_t sbase_e = ((int64_t)hd.b * p.Hv + hd.h) * DK * DV;   // the head's state tile (elements)
     float *state = p.state + sbase_e;
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
-    float *dec = f32p(sm, CH_DECC);
+    const float *dec = f32p(sm, CH_DEC);            // e^gC of the chunk in inbox A
     // (debug build) a ring access outside the workspace is skipped; its barrier phase still completes
     const int64_t ring0 = (int64_t)(hslots - reinterpret_cast<const unsigned char *>(p.err));   // bytes into the workspace
     auto load_a = [&](int c) {
@@ -185,7 +192,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             const unsigned char *src = hslots + slot_of(c) * SLOT_BYTES;
             arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb)               // Qg: 64-row blocks into rows 0..63 of [Qg; -W]
+            for (int kb = 0; kb < 2; ++kb)               // Qg: 64-row blocks into rows 0..63 of [Qg; -W]
                 bulk_load(sbase + CH_QW + kb * 16384, src + SL_QG + kb * 8192, 8192, sbase + CH_FULL_A);
             bulk_load(sbase + CH_A_REST, src + SL_KG, A_REST_BYTES, sbase + CH_FULL_A);
         } else {
@@ -207,6 +214,20 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     auto issue_wu = [&]() {
         gemm16<64, 64>(tmem + T_W, sbase + CH_KG, sbase + CH_TB, false);
         gemm16<64, 64>(tmem + T_U, sbase + CH_VT, sbase + CH_TB, false);
+    };
+    // o of chunk cp (this thread's 16 tokens of column trow) into the staging tile, fenced for the
+    // TMA store that thread kOIO issues after the next barrier; without an o map, thread stores
+    auto stage_o = [&](const float (&ov)[16]) {
+        if (p.o_f32) {
+            float *t = f32p(sm, CH_OST);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) t[(16 * wc + k) * DV + trow] = ov[k];
+        } else {
+            __nv_bfloat16 *t = reinterpret_cast<__nv_bfloat16 *>(sm + CH_OST);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) t[(16 * wc + k) * DV + trow] = __float2bfloat16_rn(ov[k]);
+        }
+        fence_smem_to_async();
     };
     auto store_prev_o = [&](const float (&ov)[16], int cp) {
         const int t0 = cp * C, nv = min(16, p.T - t0 - 16 * wc);
@@ -250,15 +271,21 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         if (!mma_wait(mb)) return false;
         if (__syncthreads_or(!okw)) return false;
     }
-    float oprev[16];                       // O^T columns 16 wc .. + 15 of the previous chunk, lane trow
+    float oprev[16];                       // O^T columns 16 wc .. + 15 of a chunk, lane trow
     for (int c = 0; c < n; ++c) {
-        // ---------------------------------------------------------- [O^T | U^T] += S^T [Qg; -W]^T
+        // ---------------------------------------------------------- [O^T | U^T] += S16 [Qg; -W]^T
         {
-            if (tid < DK) dec[tid] = f32p(sm, CH_DEC)[tid];
+            // S16 <- S^T as fp16 pairs; S^T <- S^T Diag(e^gC) (the carry accumulates onto it)
+            float amax = s16_and_decay(tmem + lane_off + T_S, tmem + lane_off + T_S16, 32 * wc, dec);
             float w16[16];
             tmem_ld16(tmem + lane_off + T_W + 16 * wc, w16);                 // -W [r][i] into rows 64..127
 #pragma unroll
-            for (int j = 0; j < 16; ++j) st_tile(sm, CH_QW, 128, 64 + 16 * wc + j, trow, -w16[j]);
+            for (int j = 0; j < 16; ++j) st_h(sm, CH_QW, 128, 64 + 16 * wc + j, trow, -w16[j], amax);
+            if (amax > kF16Max) record_range(p.err, p.status);
+        }
+        if (c > 0) tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);       // o of chunk c - 1
+        if (p.o_tma && tid == kOIO) bulk_wait_read<0>();                     // the staging tile is free
+        {
             float z[16];
 #pragma unroll
             for (int m = 0; m < 16; ++m) z[m] = 0.f;
@@ -269,12 +296,19 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         __syncthreads();
         if (tid == 0) {
             fence_after_sync();
-            gemm_ts<128, 128>(tmem + T_O, tmem + T_S, sbase + CH_QW, true);   // S^T read from tensor memory
+            gemm16_ts<128, 128>(tmem + T_O, tmem + T_S16, sbase + CH_QW, true);
             commit(mb.mbar);
         }
-        if (c > 0) store_prev_o(oprev, c - 1);
+        if (c > 0) {
+            if (p.o_tma) stage_o(oprev);
+            else store_prev_o(oprev, c - 1);
+        }
         if (!mma_wait(mb)) return false;
-        // inbox A is free (its tiles were read, e^gC copied): pull the next image now if it is there
+        if (p.o_tma && c > 0 && tid == kOIO) {
+            tma_store_tile(&p.tm.o, sbase + CH_OST, (c - 1) * C, hd.h, hd.b);
+            bulk_commit();
+        }
+        // inbox A is free (its tiles and e^gC were read): pull the next image now if it is there
         bool next_a = false;
         if (tid == 0 && c + 1 < n && cl_test(ready(c + 1), slot_parity(c + 1))) {
             fence_global_to_async();
@@ -282,12 +316,6 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             next_a = true;
         }
         {
-            float v[32];
-            const int i0 = 32 * wc;
-            tmem_ld32(tmem + lane_off + T_S + i0, v);                        // S^T <- S^T Diag(e^gC)
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] *= dec[i0 + k];
-            tmem_st32(tmem + lane_off + T_S + i0, v);
             float u[16], amax = 0.f;
             tmem_ld16(tmem + lane_off + T_U + 16 * wc, u);
 #pragma unroll
@@ -325,11 +353,25 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             commit(mb.mbar);
         }
         if (!mma_wait(mb)) return false;
-        tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);
         if (tid == 0 && okw && c + 1 < n) load_b(c + 1);                   // inbox B was read
         if (__syncthreads_or(!okw)) return false;
     }
-    if (n > 0) store_prev_o(oprev, n - 1);                                 // last chunk's o
+    if (n > 0) {                                                             // last chunk's o
+        tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);
+        if (p.o_tma) {
+            if (tid == kOIO) bulk_wait_read<0>();
+            __syncthreads();
+            stage_o(oprev);
+            __syncthreads();
+            if (tid == kOIO) {
+                tma_store_tile(&p.tm.o, sbase + CH_OST, (n - 1) * C, hd.h, hd.b);
+                bulk_commit();
+            }
+        } else {
+            store_prev_o(oprev, n - 1);
+        }
+    }
+    if (p.o_tma && tid == kOIO) bulk_store_wait();                        // every o store complete
     float v[32];
     tmem_ld32(tmem + lane_off + T_S + 32 * wc, v);
 #pragma unroll
@@ -352,7 +394,6 @@ constexpr int kIO = 448;
 __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
                                          int n, int rank, unsigned char *hslots, StageTrack &st) {
     const int tid = threadIdx.x;
-    const int ci = tid & 127, cq = tid >> 7;
     const uint32_t sbase = smem_u32(sm);
     volatile int *slot_ok = reinterpret_cast<volatile int *>(sm + M_FLAG);
     const int c_first = rank - 1;
@@ -373,7 +414,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         char *slot = slot_ptr(c);
         if (!st.wait(sbase, p.polls, p.inject && k == 0)) return false;
         // operand tiles; prefetch the next own chunk's g rows into L2 (they are staged last)
-        prep_chunk<false>(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
+        prep_chunk<false, true>(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
         if (tid == kIO) {
             if (k > 0) announce(c - NPREP);
             // the slot's previous chunk (own chunk k - NSLOTP) has been pulled by rank 0
@@ -381,7 +422,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             if (k >= NSLOTP) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1), p.polls);
             if (okw) {
                 // Qg, Kg^T, e^gC
-                ring_store(p, slot + SL_QG, sbase + R_B, 32768);
+                ring_store(p, slot + SL_QG, sbase + R_B, 16384);
                 ring_store(p, slot + SL_KG, sbase + R_C, 16384);
                 ring_store(p, slot + SL_DEC, sbase + M_DEC, 512);
                 bulk_commit();
@@ -393,40 +434,19 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
         if (tid == kIO) {
             // P (64-row tile) into rows 128..191 of [Kend^T; P]; V^T
             ring_store(p, slot + SL_KP + 16384, sbase + R_F, 8192);
-            ring_store(p, slot + SL_VT, sbase + A1_VT, 16384);
+            ring_store(p, slot + SL_VT, sbase + RC_VT, 16384);
             bulk_commit();
         }
-        solve_tb(sm, cr.amax);
+        solve_tb<true>(sm, cr);                                           // and Kend^T into A1_KE
+        if (cr.amax > kF16Max) record_range(p.err, p.status);
         if (tid == kIO) {
             ring_store(p, slot + SL_TB, sbase + R_G, 8192);
+            ring_store(p, slot + SL_KP, sbase + A1_KE, 16384);             // Kend^T: rows 0..127 of [Kend^T; P]
             bulk_commit();
-            bulk_wait_read<0>();                                           // R_B, R_C, R_F, A1_VT, R_G read
+            bulk_wait_read<0>();                                           // R_B, R_C, R_F, R_G, A1_KE read
         }
         __syncthreads();
-        if (tn < p.T) {
-            st.stage<STG_Q | STG_V | STG_ONCE>(p, hd, sbase, tn);
-            st.stage<STG_K | STG_ONCE>(p, hd, sbase, tn);
-        }
-        {
-            // Kend^T [i][s] = X2 [s][i] e^(gC - gm) (wide chunk: the Kend source as is) into R_C
-            const float sc = cr.wide ? 1.f : __expf(cr.gcv - cr.gm);
-#pragma unroll
-            for (int jj = 0; jj < 16; jj += 4) {
-                const int s0 = 16 * cq + jj;
-                st_h4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc,
-                      ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc,
-                      ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc, cr.amax);
-            }
-            if (cr.amax > kF16Max) record_range(p.err, p.status);
-        }
-        fence_smem_to_async();
-        __syncthreads();
-        if (tid == kIO) {
-            // Kend^T into rows 0..127 of [Kend^T; P]
-            ring_store(p, slot + SL_KP, sbase + R_C, 16384);
-            bulk_commit();
-        }
-        if (tn < p.T) st.stage<STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, tn);        // A2 is free
+        if (tn < p.T) st.stage<STG_Q | STG_V | STG_K | STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, tn);
     }
     if (k > 0 && tid == kIO) announce(c_first + NPREP * (k - 1));        // the last own chunk
     return true;
@@ -478,7 +498,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
         if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1), kSpin);
         if (!chain) st.drain(sbase);
     }
-    if (!chain && tid == kIO) bulk_store_wait();   // no bulk store may still read this CTA's shared memory
+    if (tid == (chain ? kOIO : kIO)) bulk_store_wait();   // no bulk store may still read this CTA's shared memory
     cp_async_wait_all();
     fence_before_sync();
     __syncthreads();

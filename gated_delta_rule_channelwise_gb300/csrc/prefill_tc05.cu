@@ -31,7 +31,6 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     const Head hd = head_of(p, blockIdx.y, blockIdx.x);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;                 // TMEM lane quarter, column quarter
-    const int ci = tid & 127, cq = tid >> 7;                 // channel (or column), row quarter (16 rows)
     const int64_t sbase_e = ((int64_t)hd.b * p.Hv + hd.h) * DK * DV;   // the head's state tile (elements)
     float *state = p.state + sbase_e;
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
@@ -74,14 +73,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     for (int t0 = 0; t0 < p.T && ok; t0 += C) {
         const int L = min(C, p.T - t0);
         if (!(ok = st.wait(sbase, p.polls, p.inject && t0 == 0))) break;
-        prep_chunk<true>(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
+        prep_chunk<true, false>(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
         if (!(ok = causal_terms<false>(sm, tmem, mb, cr, sm + R_F, 64, 0))) break;
-        solve_tb(sm, cr.amax);
+        solve_tb<false>(sm, cr);
         // ------------------------------------------------------------ W^T, U~^T (fp16 operands)
         if (tid == 0) {
             fence_after_sync();
             gemm16<64, 64>(tmem + T_D2, sbase + R_C, sbase + R_G, false);    // W^T  = Kg^T Tb^T
-            gemm16<64, 64>(tmem + T_D3, sbase + A1_VT, sbase + R_G, false);  // U~^T = V^T Tb^T
+            gemm16<64, 64>(tmem + T_D3, sbase + RC_VT, sbase + R_G, false);  // U~^T = V^T Tb^T
             commit(mb.mbar);
         }
         if (!(ok = mma_wait(mb))) break;
@@ -113,18 +112,14 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
 #pragma unroll
             for (int c = 0; c < 32; ++c) sv[c] *= sDec[i0 + c];
             tmem_st32(tmem + lane_off + T_D0 + i0, sv);
+        }
+        build_kend(sm, cr);                                                                  // Kend^T
+        {
             float v[16];
             tmem_ld16(tmem + lane_off + T_D3 + 16 * wc, v);
 #pragma unroll
             for (int c = 0; c < 16; c += 4)                                                  // U^T [j][s]
                 st_h4(sm, R_A1, 128, trow, 16 * wc + c, v[c], v[c + 1], v[c + 2], v[c + 3], cr.amax);
-            const float sc = cr.wide ? 1.f : __expf(cr.gcv - cr.gm);
-#pragma unroll
-            for (int jj = 0; jj < 16; jj += 4) {                                             // Kend^T [i][s]
-                const int s0 = 16 * cq + jj;
-                st_h4(sm, R_C, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc,
-                      ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc, cr.amax);
-            }
             if (cr.amax > kF16Max) record_range(p.err, p.status);
         }
         fence_smem_to_async();
@@ -134,11 +129,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
         if (tid == 0) {
             fence_after_sync();
             gemm16<64, 64>(tmem + T_D4, sbase + R_A1, sbase + R_F, true);
-            gemm16<128, 64>(tmem + T_D0, sbase + R_A1, sbase + R_C, true);
+            gemm16<128, 64>(tmem + T_D0, sbase + R_A1, sbase + A1_KE, true);
             commit(mb.mbar);
         }
+        if (t0 + C < p.T) st.stage<STG_G>(p, hd, sbase, t0 + C);           // A2 is free (Kend^T was read out of it)
         if (!(ok = mma_wait(mb))) break;
-        if (t0 + C < p.T) st.stage<STG_Q | STG_G | STG_LAST>(p, hd, sbase, t0 + C);   // F and A2 are free
+        if (t0 + C < p.T) st.stage<STG_Q | STG_LAST>(p, hd, sbase, t0 + C);   // F is free
         store_o(p, obase, tmem + T_D4, t0, L);
         fence_before_sync();
         __syncthreads();
@@ -260,6 +256,10 @@ bool make_params(const cgdr_args &a, void *ws, size_t ws_bytes, Tc05Params &p) {
     p.inject = inject_of(a);
     p.ext = extents_of(a, true, ws_bytes);
     p.slots = nullptr;
+    // o by TMA tensor stores where a map can describe it (a 16-byte aligned base and strides)
+    p.o_tma = describable(p.o_f32 ? 4 : 2, a.dv, a, a.Hv, a.o_st, a.o_sh, a.o_sb) &&
+              encode4(p.tm.o, p.o_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      p.o_f32 ? 4 : 2, a.o, a.dv, a.T, a.Hv, a.B, a.o_st, a.o_sh, a.o_sb);
     return true;
 }
 }  // namespace tc05c

@@ -23,12 +23,14 @@
 // the CUDA cores from exponentials of differences instead (exact for any
 // decay).
 //
-// Operand precision.  D1's anchored factors span up to e^80 and the state products read S^T
-// and -W, Qg as TF32 (the first fp32 range, the others kept as they were measured); the other
-// products (D2, the V^T part of D3, and U^T . [P^T | Kend]) take fp16 tiles, which round like
-// TF32 (10 mantissa bits) for values below 65504 in magnitude, move half the bytes and run at
-// twice the rate.  Every fp16 value is checked against that range; a chunk that would overflow
-// it records CGDR_ERR_RANGE.
+// Operand precision.  D1's anchored factors span up to e^80, so D1 takes TF32 tiles.  W, U~ and
+// the U^T products take fp16 tiles, which round like TF32 (10 mantissa bits) for values below
+// 65504 in magnitude, move half the bytes and run at twice the rate.  The state products
+// S^T [Qg; -W]^T read S^T as TF32 straight from the fp32 state in the per-head kernel; the
+// cluster kernel's state CTA, whose chain is the serial part, keeps an fp16 copy of S^T in
+// tensor memory and runs them in fp16 too (Qg in fp16, prep_chunk<.., true>).  Every fp16
+// value is checked against the fp16 range; a chunk that would overflow it records
+// CGDR_ERR_RANGE.
 #pragma once
 
 #include <cuda.h>
@@ -47,10 +49,10 @@ constexpr float kRange = 80.f;           // max |gamma_r - gamma_mid| for the te
 constexpr uint32_t kSpin = kDefaultPolls;   // bounded mbarrier wait (polls) of the drains after a failure
 
 // shared memory map of a CTA that prepares chunks (bytes from a 1024-aligned base)
-constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, V^T (fp16) | U^T (fp16) ; wide: q~, k~
+constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, Kend^T (fp16) | U^T (fp16) ; wide: q~, k~
 constexpr int R_A2 = 65536;              // 32 KB: X2 (kn e^(gm-g)), the source of Kend ; wide: gamma
-constexpr int R_B = 98304;               // 32 KB: Qg = qn e^g            [64 x 128]
-constexpr int R_C = 131072;              // 32 KB: Kg^T [128 x 64] (fp16) | -W [64 x 128] | Kend^T [128 x 64] (fp16)
+constexpr int R_B = 98304;               // 32 KB: Qg = qn e^g [64 x 128] (TF32, or fp16 for the cluster kernel)
+constexpr int R_C = 131072;              // 32 KB: Kg^T [128 x 64], V^T [128 x 64] | -W [64 x 128] (fp16)
 constexpr int R_F = 163840;              // 16 KB: P  [64 x 64] (fp16)
 constexpr int R_G = 180224;              // 16 KB: Xs fp32 [64][64] | Tb [64 x 64] (fp16)
 constexpr int R_MISC = 196608;
@@ -65,8 +67,9 @@ constexpr int M_END = M_DEAD + 8;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
 constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned)
 constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
-constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_VT = R_A1 + 32768;
-static_assert(A1_Z + 6 * 16 * LDZ * 4 <= A1_VT, "A1 overflow");
+constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_KE = R_A1 + 32768;   // Kend^T built during the solve
+constexpr int RC_VT = R_C + 16384;       // V^T beside Kg^T
+static_assert(A1_Z + 6 * 16 * LDZ * 4 <= A1_KE, "A1 overflow");
 // Staged raw inputs of a chunk (TMA tiles; beta by cp.async), loaded while an earlier chunk finishes:
 // q rows -> F, k rows -> G (bf16 [64][128]); g rows -> A2 (fp32 [64][128]);
 // v rows -> B (bf16 [64][128]); beta -> B + 16 KB (fp32 [64]).
@@ -74,12 +77,13 @@ constexpr int ST_Q = R_F, ST_K = R_G, ST_G = R_A2, ST_V = R_B, ST_BETA = R_B + 1
 static_assert(PREP_SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 
 // tensor memory columns
-constexpr uint32_t T_D0 = 0, T_D1 = 128, T_D2 = 192, T_D3 = 256, T_D4 = 320, T_D4B = 384, T_COLS = 512;
+constexpr uint32_t T_D0 = 0, T_D1 = 128, T_D2 = 192, T_D3 = 256, T_D4 = 320, T_COLS = 512;
 
-// TMA tensor maps of the inputs: 4-D (channel, token, head, batch) with the caller's
-// strides, box = 128 channels x 64 tokens; rows past T read as zeros.
+// TMA tensor maps of the inputs and of o: 4-D (channel, token, head, batch) with the caller's
+// strides, box = 128 channels x 64 tokens; input rows past T read as zeros, o rows past T are
+// not written.
 struct Tc05Maps {
-    CUtensorMap q, k, v, g;
+    CUtensorMap q, k, v, g, o;
 };
 
 struct Tc05Params {
@@ -102,6 +106,7 @@ struct Tc05Params {
     int inject;                          // test hook: the first staging wait targets M_DEAD
     Extents ext;                         // footprints for the index checks of a debug build
     unsigned char *slots;                // cluster kernel: hand-off ring in the workspace (unused per head)
+    int o_tma;                           // tm.o describes o (else o is written by thread stores)
 };
 
 // Records a wait that gave up (one thread per CTA).
@@ -126,15 +131,11 @@ __device__ __forceinline__ void st_tile4(char *base, int region, int R, int r, i
                                          float d) {
     *reinterpret_cast<float4 *>(base + region + sw_off(R, r, k0)) = make_float4(tf32r(a), tf32r(b), tf32r(c), tf32r(d));
 }
-// Unrounded stores: the tensor core then reads the value as TF32 by dropping the low
-// mantissa bits.  Used only for the Qg and Kg^T operands, whose truncation leaves the
-// result unchanged to the printed digits in emulation (the other operands need rounding).
+// Unrounded store: the tensor core reads the value as TF32 by dropping the low mantissa bits
+// (the Qg operand, whose truncation leaves the result unchanged to the printed digits in
+// emulation).
 __device__ __forceinline__ void st_raw(char *base, int region, int R, int r, int k, float x) {
     *reinterpret_cast<float *>(base + region + sw_off(R, r, k)) = x;
-}
-__device__ __forceinline__ void st_raw4(char *base, int region, int R, int r, int k0, float a, float b, float c,
-                                        float d) {
-    *reinterpret_cast<float4 *>(base + region + sw_off(R, r, k0)) = make_float4(a, b, c, d);
 }
 __device__ __forceinline__ float ld_tile(const char *base, int region, int R, int r, int k) {
     return *reinterpret_cast<const float *>(base + region + sw_off(R, r, k));
@@ -155,6 +156,29 @@ __device__ __forceinline__ void st_h4(char *base, int region, int R, int r, int 
 __device__ __forceinline__ void st_h(char *base, int region, int R, int r, int k, float x, float &amax) {
     amax = fmaxf(amax, fabsf(x));
     *reinterpret_cast<__half *>(base + region + sw_off16(R, r, k)) = __float2half_rn(x);
+}
+// One pass over this thread's 32 columns [i0, i0 + 32) of S^T in tensor memory (lane quarter
+// at lane_off): the fp16 copy into columns s16 + i0 / 2 .. (the A operand of the state
+// products), then S^T <- S^T Diag(dec) in place.  Two 16-column halves keep few registers live.
+// Returns the largest magnitude seen (for the fp16 range check).
+__device__ __forceinline__ float s16_and_decay(uint32_t t_s, uint32_t s16, int i0, const float *dec) {
+    float amax = 0.f;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        const int j0 = i0 + 16 * half;
+        float sv[16], h[8];
+        tmem_ld16(t_s + j0, sv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            amax = fmaxf(amax, fmaxf(fabsf(sv[2 * k]), fabsf(sv[2 * k + 1])));
+            h[k] = __uint_as_float(h2_bits(__floats2half2_rn(sv[2 * k], sv[2 * k + 1])));
+        }
+        tmem_st8(s16 + j0 / 2, h);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) sv[k] *= dec[j0 + k];
+        tmem_st16(t_s + j0, sv);
+    }
+    return amax;
 }
 // Largest magnitude an fp16 operand may take (the largest finite fp16).
 constexpr float kF16Max = 65504.f;
@@ -321,8 +345,9 @@ struct ChunkRegs {
 // rows at t_pf into L2.  The Qg tile goes to rows 0..63 of the qg_rows-row tile
 // at qg (shared or global memory, same tile image).  Ends with the operand
 // tiles fenced for the tensor core.
-// kPrefetchQKV = false prefetches only the g rows (for callers that stage q, k, v early).
-template <bool kPrefetchQKV>
+// kPrefetchQKV = false prefetches only the g rows (for callers that stage q, k, v early);
+// kQgF16: Qg as an fp16 tile (else TF32).
+template <bool kPrefetchQKV, bool kQgF16>
 __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L, int t_pf,
                                            char *qg, int qg_rows, ChunkRegs &cr) {
     const int tid = threadIdx.x;
@@ -456,7 +481,8 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             float eg, e1 = 0.f;
             if (!wide) e1 = __expf(cr.lam[jj] - gm);
             eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
-            st_raw(qg, 0, qg_rows, r, ci, qt * eg);           // Qg [r][i] (taken as TF32 by truncation)
+            if (kQgF16) st_h(qg, 0, qg_rows, r, ci, qt * eg, cr.amax);   // Qg [r][i]
+            else st_raw(qg, 0, qg_rows, r, ci, qt * eg);            // (taken as TF32 by truncation)
             kg4[jj & 3] = kt * eg;
             if ((jj & 3) == 3) st_h4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3], cr.amax);   // Kg^T [i][s]
             if (!wide) {
@@ -480,7 +506,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
 // The causal terms: A (fp32, strictly lower, beta-folded) into A1_A32, P (lower
 // with diagonal) into rows pt_row0 .. pt_row0 + 63 of the pt_rows-row tile at pt
 // (shared or global memory), the Kend source into R_A2 for a wide chunk, and
-// V^T into A1_VT.  False if a tensor-core wait gave up.
+// V^T into RC_VT.  False if a tensor-core wait gave up.
 // kBulkOut: P and V^T leave by bulk copy, so fence them for the async proxy.
 template <bool kBulkOut>
 __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb, ChunkRegs &cr, char *pt,
@@ -492,12 +518,19 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const int trow = 32 * wq + lane;
     float *sA = f32p(sm, A1_A32), *sBeta = f32p(sm, M_BETA);
+    // V^T [j][s] into R_C's second half (exact in fp16 for bf16 values of magnitude 2^-14 .. 65504)
+    auto store_vt = [&]() {
+#pragma unroll
+        for (int jj = 0; jj < 16; jj += 4)
+            st_h4(sm, RC_VT, 128, ci, 16 * cq + jj, cr.vreg[jj], cr.vreg[jj + 1], cr.vreg[jj + 2], cr.vreg[jj + 3], cr.amax);
+    };
     if (!cr.wide) {
         if (tid == 0) {
             fence_after_sync();
             gemm<64, 128>(tmem + T_D1, sbase + R_A1, sbase + R_A2, false);
             commit(mb.mbar);
         }
+        store_vt();                          // while the product runs (it reads A1 and A2 only)
         if (!mma_wait(mb)) return false;
         float v[16];
         tmem_ld16(tmem + lane_off + T_D1 + 16 * wc, v);
@@ -552,14 +585,24 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
             sA[r * LDA + s] = ra[e];
             st_h(pt, 0, pt_rows, pt_row0 + r, s, rp[e], cr.amax);
         }
+        store_vt();
     }
-    // V^T [j][s] (exact in fp16 for bf16 values of magnitude 2^-14 .. 65504)
-#pragma unroll
-    for (int jj = 0; jj < 16; jj += 4)
-        st_h4(sm, A1_VT, 128, ci, 16 * cq + jj, cr.vreg[jj], cr.vreg[jj + 1], cr.vreg[jj + 2], cr.vreg[jj + 3], cr.amax);
     if (kBulkOut) fence_smem_to_async();
     __syncthreads();
     return true;
+}
+
+// Kend^T [i][s] = X2 [s][i] e^(gC - gm) into A1_KE as an fp16 tile, by all threads: thread
+// (channel ci, rows 16 cq .. + 15).  A wide chunk's X2 region holds the Kend source itself.
+__device__ __forceinline__ void build_kend(char *sm, ChunkRegs &cr) {
+    const int tid = threadIdx.x, ci = tid & 127, cq = tid >> 7;
+    const float sc = cr.wide ? 1.f : __expf(cr.gcv - cr.gm);
+#pragma unroll
+    for (int jj = 0; jj < 16; jj += 4) {
+        const int s0 = 16 * cq + jj;
+        st_h4(sm, A1_KE, 128, ci, s0, ld_tile(sm, R_A2, 64, s0, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 1, ci) * sc,
+              ld_tile(sm, R_A2, 64, s0 + 2, ci) * sc, ld_tile(sm, R_A2, 64, s0 + 3, ci) * sc, cr.amax);
+    }
 }
 
 // Element (r, c) of the 64 x 64 fp32 X = (I + A)^-1 held in R_G: rows of 64
@@ -567,16 +610,31 @@ __device__ __forceinline__ bool causal_terms(char *sm, uint32_t tmem, MmaBar &mb
 // eight different rows hits eight different bank groups.
 __device__ __forceinline__ int xs_off(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
 
-// Tb = (I + A)^-1 Diag(beta) into R_G as an fp16 tile, by 16 x 16 blocks:
+// Tb = (I + A)^-1 Diag(beta) into R_G as an fp16 tile, by 16 x 16 blocks (and with kKend, while
+// 64 threads run the diagonal substitution, Kend^T = (kn e^(gC - g))^T into A1_KE as an fp16
+// tile; see build_kend):
 // X_RR = (I + A_RR)^-1 by forward substitution (four blocks at once), then
 // Z_Rm = X_RR A_Rm for the six pairs m < R, then X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS
 // one block diagonal at a time.  Each thread of the product steps owns four
 // consecutive columns of one row (float4 loads).  Ends with Tb fenced for the
 // tensor core.
-__device__ __forceinline__ void solve_tb(char *sm, float &amax) {
+template <bool kKend>
+__device__ __forceinline__ void solve_tb(char *sm, ChunkRegs &cr) {
     const int tid = threadIdx.x;
+    float &amax = cr.amax;
     const float *sA = f32p(sm, A1_A32), *sBeta = f32p(sm, M_BETA);
     float *sZ = f32p(sm, A1_Z), *sXs = f32p(sm, R_G);
+    if (kKend && tid >= 64 && tid < 448) {
+        // Kend^T [i][s] = X2 [s][i] e^(gC_i - gm_i) (a wide chunk's X2 region holds the Kend
+        // source itself): thread (channel i, row quads q0, q0 + 3, ...)
+        const int i = (tid - 64) & 127, q0 = (tid - 64) >> 7;
+        const float sc = cr.wide ? 1.f : __expf(f32p(sm, M_GC)[i] - f32p(sm, M_GM)[i]);
+        for (int q = q0; q < 16; q += 3) {
+            const int s0 = 4 * q;
+            st_h4(sm, A1_KE, 128, i, s0, ld_tile(sm, R_A2, 64, s0, i) * sc, ld_tile(sm, R_A2, 64, s0 + 1, i) * sc,
+                  ld_tile(sm, R_A2, 64, s0 + 2, i) * sc, ld_tile(sm, R_A2, 64, s0 + 3, i) * sc, amax);
+        }
+    }
     if (tid < 64) {
         const int Rb = tid >> 4, jc = tid & 15;
         float x[16];

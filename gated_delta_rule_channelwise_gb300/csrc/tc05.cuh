@@ -122,6 +122,26 @@ __device__ __forceinline__ void gemm16(uint32_t d_tmem, uint32_t a_smem, uint32_
     }
 }
 
+// The same with A read from tensor memory: A[m][k] = the fp16 pair in TMEM[lane m][column
+// a_tmem + k / 2] (element k in the low half for even k), K = 16 per instruction (8 columns).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+template <int N, int K>
+__device__ __forceinline__ void gemm16_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
+    constexpr uint32_t idesc = idesc_f16(N);
+    const uint64_t bd = smem_desc(b_smem);
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint64_t b = bd + (uint64_t)((ks >> 2) * (N * 128 / 16) + (ks & 3) * 2);
+        mma_f16_ts(d_tmem, a_tmem + 8 * ks, b, idesc, (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
 __device__ __forceinline__ void commit(uint32_t mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar));
 }
@@ -199,6 +219,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
           "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
           "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
           "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])));
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane (warp-wide store).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n"
+        ::"r"(taddr),
+          "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+          "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])));
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 

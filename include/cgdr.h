@@ -152,8 +152,8 @@ cgdr_status cgdr_decode(const cgdr_args *args, void *stream);
 /*
  * Bytes of device workspace cgdr_prefill needs for `args` (may be 0): 0 for
  * the CUDA-core kernel, 256 for the per-head tensor-core kernel (a status
- * word), and 256 + B * Hv * 889344 for the cluster kernel (the status word,
- * then nine 98816-byte hand-off slots per (batch, v-head)).  Depends on the
+ * word), and 256 + B * Hv * 741888 for the cluster kernel (the status word,
+ * then nine 82432-byte hand-off slots per (batch, v-head)).  Depends on the
  * kernel cgdr_prefill_path_for reports.  The workspace plays the part of the
  * single scratch arena of "Add parallel chunked prefill for channelwise gated
  * delta rule" (Summary), sliced per (batch, head) unit.  Returns 0 for

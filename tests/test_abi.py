@@ -215,7 +215,7 @@ def test_prefill_path_choice(lib):
     A = _args(T=100, prefill_path=cg.PREFILL_PER_HEAD)
     assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == 256
     A = _args(T=100, prefill_path=cg.PREFILL_CLUSTER)
-    need = 256 + A.B * A.Hv * 9 * 98816
+    need = 256 + A.B * A.Hv * 9 * 82432
     assert lib.cgdr_prefill_workspace_size(ctypes.byref(A)) == need
     assert lib.cgdr_prefill(ctypes.byref(A), None, 0, None) == cg.ERR_WORKSPACE
     assert lib.cgdr_prefill(ctypes.byref(A), ctypes.c_void_p(1 << 30), need - 16, None) == cg.ERR_WORKSPACE
@@ -237,7 +237,7 @@ def test_calls_from_two_threads_do_not_interfere(lib):
                 return
 
     ts = [threading.Thread(target=worker, args=(cg.PREFILL_PER_HEAD, 256)),
-          threading.Thread(target=worker, args=(cg.PREFILL_CLUSTER, 256 + 2 * 4 * 9 * 98816)),
+          threading.Thread(target=worker, args=(cg.PREFILL_CLUSTER, 256 + 2 * 4 * 9 * 82432)),
           threading.Thread(target=worker, args=(cg.PREFILL_SIMT, 0))]
     for t in ts:
         t.start()

@@ -222,7 +222,7 @@ def test_tensor_core_path_reports_ok_status(tc_path):
     state = inp["S0"].clone()
     n = cg.prefill_workspace_size(inp["q"], inp["k"], inp["v"], state, torch.empty(inp["v"].shape, device="cuda"),
                                   path=tc_path, **gate_kwargs(inp))
-    assert n == (256 if tc_path == cg.PREFILL_PER_HEAD else 256 + 9 * 98816)   # + hand-off slots
+    assert n == (256 if tc_path == cg.PREFILL_PER_HEAD else 256 + 9 * 82432)   # + hand-off slots
     ws = torch.full((n,), 0x7F, dtype=torch.uint8, device="cuda")
     cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=tc_path, workspace=ws, **gate_kwargs(inp))
     assert cg.workspace_status(ws) == cg.OK
