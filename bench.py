@@ -56,9 +56,10 @@ PRE_BYTES_F32O = prefill_bytes(PRE["B"], PRE["T"], PRE["H"], 4)                 
 # prefill tensor flops per token-head: 10*C*d (intra-chunk) + 6*dk*dv (carry)
 PRE_FLOPS = PRE["B"] * PRE["T"] * PRE["H"] * (10 * PRE["chunk"] * 128 + 6 * 128 * 128)
 L2_FLUSH_BYTES = 256 << 20
-# kernel name and the sources that define it, per prefill path (1 = per head, 2 = cluster)
+# kernel name and the sources that define it, per prefill path (1 = per head, 2 = cluster, 5 = cooperative)
 PREFILL_KERNELS = {1: ("prefill_tc05_kernel", ["prefill_tc05.cu", "prefill_tc05_chunk.cuh", "tc05.cuh"]),
-                   2: ("prefill_cluster_kernel", ["prefill_cluster.cu", "prefill_tc05_chunk.cuh", "tc05.cuh"])}
+                   2: ("prefill_cluster_kernel", ["prefill_cluster.cu", "prefill_tc05_chunk.cuh", "tc05.cuh"]),
+                   5: ("prefill_coop_kernel", ["prefill_cluster.cu", "prefill_tc05_chunk.cuh", "tc05.cuh"])}
 DECODE_KERNEL = ("decode_kernel", ["decode.cu", "cgdr_internal.cuh"])
 
 
@@ -396,6 +397,7 @@ def run_secondary(cg, dev, stream, flush_l2):
     o = torch.empty(inp["v"].shape, dtype=torch.bfloat16, device=dev)
     o32 = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
     out["prefill_t4000_by_kernel"] = {"o": "bf16",
+                                      "ms_per_launch_coop_kernel": time_prefill(inp, st, o, cg.PREFILL_COOP),
                                       "ms_per_launch_cluster_kernel": time_prefill(inp, st, o, cg.PREFILL_CLUSTER),
                                       "ms_per_launch_per_head_kernel": time_prefill(inp, st, o, cg.PREFILL_PER_HEAD),
                                       "ms_per_launch_o_fp32": time_prefill(inp, st, o32, cg.PREFILL_AUTO),
@@ -416,13 +418,15 @@ def run_secondary(cg, dev, stream, flush_l2):
         pth = cg.prefill_path_for(inp["q"], inp["k"], inp["v"], st, o, chunk=64, **gate_kwargs(inp))
         t_auto = time_prefill(inp, st, o, cg.PREFILL_AUTO)
         sweep[key] = {"kernel": {cg.PREFILL_PER_HEAD: "per_head", cg.PREFILL_CLUSTER: "cluster",
-                                 cg.PREFILL_SIMT: "simt", cg.PREFILL_RECURRENT: "recurrent"}.get(pth, str(pth)),
+                                 cg.PREFILL_SIMT: "simt", cg.PREFILL_RECURRENT: "recurrent",
+                                 cg.PREFILL_COOP: "coop"}.get(pth, str(pth)),
                       "ms": t_auto, "tokens_per_s": round(B * T / (t_auto / 1e3), 1)}
         if pth == cg.PREFILL_RECURRENT:
             sweep[key]["ms_chunked_per_head"] = time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)
         elif B > 1:
             sweep[key]["ms_per_head"] = time_prefill(inp, st, o, cg.PREFILL_PER_HEAD)
             sweep[key]["ms_cluster"] = time_prefill(inp, st, o, cg.PREFILL_CLUSTER)
+            sweep[key]["ms_coop"] = time_prefill(inp, st, o, cg.PREFILL_COOP)
         del inp, st, o
     out["prefill_sweep"] = sweep
     torch.cuda.empty_cache()
@@ -648,7 +652,8 @@ def run_case(name):
     from gated_delta_rule_channelwise_gb300.synth import Workload, gate_kwargs, make_inputs
     cbuild.build()
     if name.startswith("prefill_t1024"):
-        path = cg.PREFILL_PER_HEAD if name == "prefill_t1024_per_head" else cg.PREFILL_AUTO
+        path = {"prefill_t1024_per_head": cg.PREFILL_PER_HEAD,
+                "prefill_t1024_cluster": cg.PREFILL_CLUSTER}.get(name, cg.PREFILL_AUTO)
         w = Workload("p", B=1, Hk=32, Hv=32, dk=128, dv=128, T=1024, dtype="bf16", gate="channel", seed=1)
         inp = make_inputs(w, device="cuda")
         o = torch.empty(inp["v"].shape, dtype=torch.bfloat16, device="cuda")
@@ -673,7 +678,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the B=1 decode and T=16411 prefill timings")
-    ap.add_argument("--case", choices=["prefill_t1024", "prefill_t1024_per_head", "decode_b16"],
+    ap.add_argument("--case", choices=["prefill_t1024", "prefill_t1024_per_head", "prefill_t1024_cluster", "decode_b16"],
                     help="run one small case twice (for a profiler) and exit")
     args = ap.parse_args()
     if args.case:

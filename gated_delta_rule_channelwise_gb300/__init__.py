@@ -31,7 +31,7 @@ LIB_PATH = os.path.join(_PKG, "libcgdr.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS, ERR_RANGE = range(9)
 F32, BF16 = 0, 1
 GATE_CHANNEL, GATE_GDN = 0, 1
-PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT, PREFILL_RECURRENT = range(5)
+PREFILL_AUTO, PREFILL_PER_HEAD, PREFILL_CLUSTER, PREFILL_SIMT, PREFILL_RECURRENT, PREFILL_COOP = range(6)
 
 
 class CgdrArgs(ctypes.Structure):

@@ -27,7 +27,7 @@ cgdr_status check(const cgdr_args *a, bool prefill) {
     if (a->gate != CGDR_GATE_CHANNEL && a->gate != CGDR_GATE_GDN) return CGDR_ERR_UNSUPPORTED;
     if (prefill && !(a->chunk == 0 || a->chunk == 16 || a->chunk == 32 || a->chunk == 64))
         return CGDR_ERR_UNSUPPORTED;
-    if (prefill && (a->prefill_path < CGDR_PREFILL_AUTO || a->prefill_path > CGDR_PREFILL_RECURRENT))
+    if (prefill && (a->prefill_path < CGDR_PREFILL_AUTO || a->prefill_path > CGDR_PREFILL_COOP))
         return CGDR_ERR_INVALID_ARG;
     if (a->B == 0 || a->T == 0) return CGDR_OK;  // nothing to do: no pointer is touched
     if (!aligned(a->status, 4)) return CGDR_ERR_ALIGNMENT;
@@ -150,25 +150,36 @@ int prefill_path(const cgdr_args &a, bool allow_cluster) {
     if (few && (choice == CGDR_PREFILL_AUTO || choice == CGDR_PREFILL_RECURRENT)) return CGDR_PREFILL_RECURRENT;
     if (choice == CGDR_PREFILL_SIMT || !prefill_tc05_supported(a)) return CGDR_PREFILL_SIMT;
     int path = choice == CGDR_PREFILL_RECURRENT ? CGDR_PREFILL_AUTO : choice;
+    const int64_t units = (int64_t)a.B * a.Hv;
+    if (path == CGDR_PREFILL_COOP && prefill_coop_grid() <= units) path = CGDR_PREFILL_AUTO;
     if (path == CGDR_PREFILL_AUTO) {
-        // Whichever finishes first in waves of resident work: a four-CTA cluster carries a head
-        // about 3.3 times faster per chunk than one CTA (7.2 K against 24 K cycles measured on
-        // GB300), but four times fewer clusters than CTAs are resident at once.
-        const int64_t units = (int64_t)a.B * a.Hv;
+        // Whichever needs the least time, from cycles per chunk of one head measured on GB300
+        // (clock64 phase stamps, T = 4000): one CTA per head 23 K, resident one per SM; a
+        // four-CTA cluster 6.3 K (its three preparers need 18.9 K per chunk each), 36 clusters
+        // resident; the cooperative grid max(5.3 K for the state CTA, 18.9 K x heads /
+        // preparers), all heads at once.
         const int cap = prefill_cluster_capacity();
         const int sms = device_sms();
+        const int grid = prefill_coop_grid();
+        int64_t best = sms > 0 ? (units + sms - 1) / sms * 230 : 0;                 // per head (x 100 cycles)
         path = CGDR_PREFILL_PER_HEAD;
-        if (cap > 0 && sms > 0) {
-            const int64_t waves_cluster = (units + cap - 1) / cap, waves_head = (units + sms - 1) / sms;
-            if (10 * waves_cluster <= 33 * waves_head) path = CGDR_PREFILL_CLUSTER;
+        if (cap > 0 && (units + cap - 1) / cap * 63 < best) {
+            best = (units + cap - 1) / cap * 63;
+            path = CGDR_PREFILL_CLUSTER;
+        }
+        if (grid > units) {
+            const int64_t prep = (189 * units + (grid - units) - 1) / (grid - units);
+            const int64_t coop = prep > 53 ? prep : 53;
+            if (coop < best) path = CGDR_PREFILL_COOP;
         }
     }
-    if (path == CGDR_PREFILL_CLUSTER && !allow_cluster) path = CGDR_PREFILL_PER_HEAD;
+    if ((path == CGDR_PREFILL_CLUSTER || path == CGDR_PREFILL_COOP) && !allow_cluster) path = CGDR_PREFILL_PER_HEAD;
     return path;
 }
 
 size_t prefill_workspace_for(const cgdr_args &a, int path) {
     if (path == CGDR_PREFILL_CLUSTER) return prefill_cluster_workspace(a);
+    if (path == CGDR_PREFILL_COOP) return prefill_coop_workspace(a);
     if (path == CGDR_PREFILL_PER_HEAD) return prefill_tc05_workspace(a);
     return 0;
 }
@@ -179,6 +190,7 @@ cgdr_status prefill_dispatch(const cgdr_args &a, int path, void *ws, size_t ws_b
     const size_t need = prefill_workspace_for(a, path);
     if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 16) != 0) return CGDR_ERR_WORKSPACE;
     const cgdr_status st = path == CGDR_PREFILL_CLUSTER ? launch_prefill_cluster(a, ws, ws_bytes, s)
+                           : path == CGDR_PREFILL_COOP  ? launch_prefill_coop(a, ws, ws_bytes, s)
                                                         : launch_prefill_tc05(a, ws, ws_bytes, s);
     // the driver's tensor-map encoder refused a tensor that the host check accepted: CUDA-core kernel
     return st == CGDR_ERR_ALIGNMENT ? launch_prefill_simt(a, s) : st;

@@ -51,8 +51,12 @@ size_t prefill_tc05_workspace(const cgdr_args &a);
 cgdr_status launch_prefill_tc05(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
 int prefill_cluster_capacity();
 size_t prefill_cluster_workspace(const cgdr_args &a);
-// The prefill kernel for `a` given a.prefill_path (CGDR_PREFILL_PER_HEAD, _CLUSTER, _SIMT or
-// _RECURRENT); allow_cluster = false maps the cluster kernel to the per-head one.
+int prefill_coop_grid();
+size_t prefill_coop_workspace(const cgdr_args &a);
+cgdr_status launch_prefill_coop(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
+// The prefill kernel for `a` given a.prefill_path (CGDR_PREFILL_PER_HEAD, _CLUSTER, _COOP, _SIMT
+// or _RECURRENT); allow_cluster = false maps the kernels with a hand-off ring (cluster,
+// cooperative) to the per-head one.
 int prefill_path(const cgdr_args &a, bool allow_cluster);
 size_t prefill_workspace_for(const cgdr_args &a, int path);
 // Runs the kernel `path` (as prefill_path returned it) with the given workspace.

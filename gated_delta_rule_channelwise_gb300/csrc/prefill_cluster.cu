@@ -163,6 +163,87 @@ __device__ __forceinline__ int slot_of(int c) { return NSLOTP * (c % NPREP) + (c
 // Parity of the phase, on a per-slot barrier, that belongs to chunk c.
 __device__ __forceinline__ uint32_t slot_parity(int c) { return (uint32_t)((c / NPREP / NSLOTP) & 1); }
 
+// Global-memory flags of the cooperative kernel (one int each, gpu scope).
+__device__ __forceinline__ int ld_acquire_gpu(const int *f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int *f, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(int *f, int v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+// The hand-off between the CTAs that prepare a head's chunks and the CTA that carries its
+// state: where chunk c's slot is, and how "chunk c is in its slot" (preparer -> state CTA,
+// after the slot's bulk stores completed) and "chunk c's slot may be rewritten" (state CTA ->
+// preparer, after both of its bulk loads landed) are signalled.  Every wait is bounded.
+template <bool kCoop>
+struct Link;
+
+// Four-CTA cluster: NSLOTP slots per preparer, one mbarrier per slot on each side, arrives
+// across the cluster's shared memories.
+template <>
+struct Link<false> {
+    unsigned char *slots;                          // the head's NSLOT slots
+    __device__ unsigned char *slot(int c) const { return slots + slot_of(c) * SLOT_BYTES; }
+    // state CTA, thread 0
+    __device__ bool ready_test(uint32_t sbase, int c) const {
+        return cl_test(sbase + CH_READY + 8 * slot_of(c), slot_parity(c));
+    }
+    __device__ bool ready_wait(uint32_t sbase, int c, uint32_t polls) const {
+        return cl_wait(sbase + CH_READY + 8 * slot_of(c), slot_parity(c), polls);
+    }
+    // Nothing of this thread's own memory operations to order, so no release.
+    __device__ void release(uint32_t sbase, int c) const {
+        remote_arrive_relaxed(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) % NSLOTP), owner_of(c)));
+    }
+    // preparer, thread kIO: chunk c is this preparer's own chunk kown
+    __device__ bool free_wait(uint32_t sbase, int, int kown, uint32_t polls) const {
+        return kown < NSLOTP ||
+               cl_wait(sbase + M_SLOTFREE + 8 * (kown % NSLOTP), (uint32_t)((kown / NSLOTP - 1) & 1), polls);
+    }
+    __device__ void announce(uint32_t sbase, int c) const {
+        bulk_store_wait();
+        remote_arrive(mapa_rank(sbase + CH_READY + 8 * slot_of(c), 0));
+    }
+};
+
+// Cooperative grid: NSLOT_COOP slots per head, chunk c in slot c % NSLOT_COOP, and per slot two
+// sequence numbers in the workspace: ready = 1 + the last chunk stored there, freed = 1 + the
+// last chunk read out of it.
+constexpr int NSLOT_COOP = 8;
+template <>
+struct Link<true> {
+    unsigned char *slots;                          // the head's NSLOT_COOP slots
+    int *ready, *freed;                            // the head's flags, NSLOT_COOP each
+    __device__ unsigned char *slot(int c) const { return slots + (c % NSLOT_COOP) * SLOT_BYTES; }
+    __device__ bool ready_test(uint32_t, int c) const { return ld_acquire_gpu(ready + c % NSLOT_COOP) > c; }
+    __device__ bool ready_wait(uint32_t, int c, uint32_t polls) const {
+        for (uint32_t it = 0; it < polls; ++it)
+            if (ready_test(0u, c)) return true;
+        return false;
+    }
+    // (both bulk loads of chunk c completed before; the preparer acquires this flag)
+    __device__ void release(uint32_t, int c) const { st_relaxed_gpu(freed + c % NSLOT_COOP, c + 1); }
+    __device__ bool free_wait(uint32_t, int c, int, uint32_t polls) const {
+        if (c < NSLOT_COOP) return true;
+        for (uint32_t it = 0; it < polls; ++it)
+            if (ld_acquire_gpu(freed + c % NSLOT_COOP) > c - NSLOT_COOP) {
+                fence_global_to_async();             // the slot's next writes are bulk (async-proxy) stores
+                return true;
+            }
+        return false;
+    }
+    __device__ void announce(uint32_t, int c) const {
+        bulk_store_wait();
+        fence_global_to_async();
+        st_release_gpu(ready + c % NSLOT_COOP, c + 1);
+    }
+};
+
 // ---------------------------------------------------------------- rank 0: the state carry
 constexpr int kOIO = 32;                         // rank 0: issues and waits for the TMA stores of o
 // ia, ib count the bulk loads issued on full_A, full_B (thread 0), so that a
@@ -172,8 +253,9 @@ constexpr int kOIO = 32;                         // rank 0: issues and waits for
 //   S16 [Qg; -W]^T (o of chunk c - 1 is stored meanwhile); U^T copied to an fp16 tile;
 //   [S^T | O^T] += U^T [Kend^T; P]^T, and right behind it on the tensor core W^T(c + 1),
 //   U~^T(c + 1) from the next inbox A.
+template <bool kCoop>
 __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
-                                          int n, const unsigned char *hslots, int &ia, int &ib) {
+                                          int n, const Link<kCoop> &lk, int &ia, int &ib) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, wc = warp >> 2;
     const uint32_t sbase = smem_u32(sm);
@@ -184,12 +266,12 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     const int64_t obase = hd.b * p.o_sb + hd.h * p.o_sh;
     const float *dec = f32p(sm, CH_DEC);            // e^gC of the chunk in inbox A
     // (debug build) a ring access outside the workspace is skipped; its barrier phase still completes
-    const int64_t ring0 = (int64_t)(hslots - reinterpret_cast<const unsigned char *>(p.err));   // bytes into the workspace
+    auto ws_off = [&](int c) { return (int64_t)(lk.slot(c) - reinterpret_cast<const unsigned char *>(p.err)); };
     auto load_a = [&](int c) {
         ++ia;
-        const int64_t off = ring0 + (int64_t)slot_of(c) * SLOT_BYTES + SL_QG;
+        const int64_t off = ws_off(c) + SL_QG;
         if (range_in_bounds(off, A_BYTES, p.ext.ws, p.err, p.status)) {
-            const unsigned char *src = hslots + slot_of(c) * SLOT_BYTES;
+            const unsigned char *src = lk.slot(c);
             arrive_expect_tx(sbase + CH_FULL_A, A_BYTES);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb)               // Qg: 64-row blocks into rows 0..63 of [Qg; -W]
@@ -201,15 +283,14 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     };
     auto load_b = [&](int c) {
         ++ib;
-        const int64_t off = ring0 + (int64_t)slot_of(c) * SLOT_BYTES + SL_KP;
+        const int64_t off = ws_off(c) + SL_KP;
         if (range_in_bounds(off, B_BYTES, p.ext.ws, p.err, p.status)) {
             arrive_expect_tx(sbase + CH_FULL_B, B_BYTES);
-            bulk_load(sbase + CH_IN_B, hslots + slot_of(c) * SLOT_BYTES + SL_KP, B_BYTES, sbase + CH_FULL_B);
+            bulk_load(sbase + CH_IN_B, lk.slot(c) + SL_KP, B_BYTES, sbase + CH_FULL_B);
         } else {
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sbase + CH_FULL_B) : "memory");
         }
     };
-    auto ready = [&](int c) { return sbase + CH_READY + 8 * slot_of(c); };
     // (thread 0) W^T = Kg^T Tb^T and U~^T = V^T Tb^T of the chunk in inbox A (fp16 operands)
     auto issue_wu = [&]() {
         gemm16<64, 64>(tmem + T_W, sbase + CH_KG, sbase + CH_TB, false);
@@ -258,7 +339,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     if (n > 0) {
         int okw = 1;
         if (tid == 0) {
-            okw = cl_wait(ready(0), slot_parity(0), p.polls);
+            okw = lk.ready_wait(sbase, 0, p.polls);
             if (okw) {
                 fence_global_to_async();
                 load_a(0);
@@ -310,7 +391,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         }
         // inbox A is free (its tiles and e^gC were read): pull the next image now if it is there
         bool next_a = false;
-        if (tid == 0 && c + 1 < n && cl_test(ready(c + 1), slot_parity(c + 1))) {
+        if (tid == 0 && c + 1 < n && lk.ready_test(sbase, c + 1)) {
             fence_global_to_async();
             load_a(c + 1);
             next_a = true;
@@ -336,12 +417,12 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             fence_after_sync();
             gemm16<192, 64>(tmem + T_S, sbase + CH_UR, sbase + CH_KP, true);
             // both images of chunk c have landed (their bulk loads completed, which this
-            // thread observed): its slot may be rewritten.  Nothing else to order, so no release.
-            remote_arrive_relaxed(mapa_rank(sbase + M_SLOTFREE + 8 * ((c / NPREP) % NSLOTP), owner_of(c)));
+            // thread observed): its slot may be rewritten
+            lk.release(sbase, c);
             if (c + 1 < n) {
                 // the next chunk's W^T, U~^T queue behind it on the tensor core
                 if (!next_a) {
-                    okw = cl_wait(ready(c + 1), slot_parity(c + 1), p.polls);
+                    okw = lk.ready_wait(sbase, c + 1, p.polls);
                     if (okw) {
                         fence_global_to_async();
                         load_a(c + 1);
@@ -382,44 +463,46 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
     return true;
 }
 
-// ---------------------------------------------------------------- ranks 1..3: state-free phases
-// Own chunk k (chunk c = rank - 1 + 3 k) goes to slot k % NSLOTP of this preparer.  Every
-// output leaves by bulk store from the shared-memory tile it was built in, as soon as the
-// tile is complete; the staging of the next own chunk's rows follows as the tiles' reads
-// finish.  Thread 0 issues the tensor-core work and the TMA staging; thread kIO (a warp with
-// no part in the triangular solve's serial steps) issues the bulk stores, waits for their
-// reads, and announces chunk k to rank 0 after the operand phase of own chunk k + 1 (or
-// after the loop), when its stores have long completed.
+// ---------------------------------------------------------------- preparers: state-free phases
+// A preparer takes its jobs (head, chunk) in order.  Every output leaves by bulk store from the
+// shared-memory tile it was built in, as soon as the tile is complete; the staging of the next
+// job's rows follows once the tiles have been read.  Thread 0 issues the tensor-core work and
+// the TMA staging; thread kIO (a warp with no part in the triangular solve's serial steps)
+// issues the bulk stores, waits for their reads, and announces job k after the operand phase of
+// job k + 1 (or after the loop), when its stores have long completed.
 constexpr int kIO = 448;
-__device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, char *sm, uint32_t tmem, MmaBar &mb,
-                                         int n, int rank, unsigned char *hslots, StageTrack &st) {
+
+template <bool kCoop>
+struct Job {
+    Head hd;
+    int c;                                       // chunk
+    int kown;                                    // the job's index among this preparer's jobs
+    Link<kCoop> lk;
+};
+
+// jobs(k, job): job k of this preparer, false past the last.
+template <bool kCoop, class Jobs>
+__device__ __forceinline__ bool run_prep(const Tc05Params &p, char *sm, uint32_t tmem, MmaBar &mb, StageTrack &st,
+                                         Jobs jobs) {
     const int tid = threadIdx.x;
     const uint32_t sbase = smem_u32(sm);
     volatile int *slot_ok = reinterpret_cast<volatile int *>(sm + M_FLAG);
-    const int c_first = rank - 1;
-    if (c_first < n) {
-        st.stage<STG_V | STG_K | STG_ONCE>(p, hd, sbase, c_first * C);
-        st.stage<STG_Q | STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, c_first * C);
-    }
-    auto slot_ptr = [&](int cc) { return reinterpret_cast<char *>(hslots + slot_of(cc) * SLOT_BYTES); };
-    // (thread kIO) chunk cc's stores have completed, to bulk loads too: tell rank 0
-    auto announce = [&](int cc) {
-        bulk_store_wait();
-        remote_arrive(mapa_rank(sbase + CH_READY + 8 * slot_of(cc), 0));
-    };
+    Job<kCoop> cur, nxt, prev;
+    if (!jobs(0, cur)) return true;
+    st.stage<STG_V | STG_K | STG_ONCE>(p, cur.hd, sbase, cur.c * C);
+    st.stage<STG_Q | STG_G | STG_ONCE | STG_LAST>(p, cur.hd, sbase, cur.c * C);
     ChunkRegs cr;
-    int k = 0;                                                           // own chunk index
-    for (int c = c_first; c < n; c += NPREP, ++k) {
-        const int t0 = c * C, L = min(C, p.T - t0), tn = t0 + NPREP * C;
-        char *slot = slot_ptr(c);
+    for (int k = 0;; ++k) {
+        const bool more = jobs(k + 1, nxt);
+        const int t0 = cur.c * C, L = min(C, p.T - t0);
+        char *slot = reinterpret_cast<char *>(cur.lk.slot(cur.c));
         if (!st.wait(sbase, p.polls, p.inject && k == 0)) return false;
-        // operand tiles; prefetch the next own chunk's g rows into L2 (they are staged last)
-        prep_chunk<false, true>(p, hd, sm, t0, L, tn, sm + R_B, 64, cr);
+        // operand tiles; prefetch the next job's g rows into L2 (they are staged last)
+        prep_chunk<false, true>(p, cur.hd, sm, t0, L, more ? nxt.hd : cur.hd, more ? nxt.c * C : p.T, sm + R_B, 64, cr);
         if (tid == kIO) {
-            if (k > 0) announce(c - NPREP);
-            // the slot's previous chunk (own chunk k - NSLOTP) has been pulled by rank 0
-            int okw = 1;
-            if (k >= NSLOTP) okw = cl_wait(sbase + M_SLOTFREE + 8 * (k % NSLOTP), (uint32_t)((k / NSLOTP - 1) & 1), p.polls);
+            if (k > 0) prev.lk.announce(sbase, prev.c);
+            // the slot's previous chunk has been pulled by the state CTA
+            const int okw = cur.lk.free_wait(sbase, cur.c, cur.kown, p.polls);
             if (okw) {
                 // Qg, Kg^T, e^gC
                 ring_store(p, slot + SL_QG, sbase + R_B, 16384);
@@ -446,10 +529,24 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, const Head &hd, ch
             bulk_wait_read<0>();                                           // R_B, R_C, R_F, R_G, A1_KE read
         }
         __syncthreads();
-        if (tn < p.T) st.stage<STG_Q | STG_V | STG_K | STG_G | STG_ONCE | STG_LAST>(p, hd, sbase, tn);
+        prev = cur;
+        if (!more) break;
+        st.stage<STG_Q | STG_V | STG_K | STG_G | STG_ONCE | STG_LAST>(p, nxt.hd, sbase, nxt.c * C);
+        cur = nxt;
     }
-    if (k > 0 && tid == kIO) announce(c_first + NPREP * (k - 1));        // the last own chunk
+    if (tid == kIO) prev.lk.announce(sbase, prev.c);                      // the last job
     return true;
+}
+
+// After a wait gave up (thread 0): record it, give the tensor core and the last bulk load on
+// each inbox (at most one can be outstanding) a bounded chance to finish.
+__device__ __forceinline__ void drain_after_failure(const Tc05Params &p, uint32_t sbase, MmaBar &mb, bool chain,
+                                                    int ia, int ib, StageTrack &st) {
+    record_timeout(p);
+    mbar_wait(mb.mbar, mb.phase ^ 1u, kSpin);
+    if (ia > 0) cl_wait(sbase + CH_FULL_A, (uint32_t)((ia - 1) & 1), kSpin);
+    if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1), kSpin);
+    if (!chain) st.drain(sbase);
 }
 
 __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
@@ -460,7 +557,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
     const int rank = (int)cluster_ctarank();
     const bool chain = rank == 0;
     const Head hd = head_of(p, blockIdx.y, blockIdx.x / CLUSTER);
-    unsigned char *hslots = p.slots + ((size_t)hd.b * p.Hv + hd.h) * NSLOT * SLOT_BYTES;
+    const Link<false> lk{p.slots + ((size_t)hd.b * p.Hv + hd.h) * NSLOT * SLOT_BYTES};
     const int tid = threadIdx.x, warp = tid >> 5;
     const int n = (p.T + C - 1) / C;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + (chain ? CH_TMEM : M_TMEM));
@@ -487,17 +584,20 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
 
     int ia = 0, ib = 0;
     StageTrack st;
-    const bool ok = chain ? run_chain(p, hd, sm, tmem, mb, n, hslots, ia, ib)
-                          : run_prep(p, hd, sm, tmem, mb, n, rank, hslots, st);
-    if (!ok && tid == 0) {
-        // a wait gave up: record it, give the tensor core and the last bulk load on
-        // each inbox (at most one can be outstanding) a bounded chance to finish
-        record_timeout(p);
-        mbar_wait(mb.mbar, mb.phase ^ 1u, kSpin);
-        if (ia > 0) cl_wait(sbase + CH_FULL_A, (uint32_t)((ia - 1) & 1), kSpin);
-        if (ib > 0) cl_wait(sbase + CH_FULL_B, (uint32_t)((ib - 1) & 1), kSpin);
-        if (!chain) st.drain(sbase);
+    bool ok;
+    if (chain) {
+        ok = run_chain<false>(p, hd, sm, tmem, mb, n, lk, ia, ib);
+    } else {
+        // own chunk k: chunk rank - 1 + 3 k of this head
+        ok = run_prep<false>(p, sm, tmem, mb, st, [&](int k, Job<false> &j) {
+            j.c = rank - 1 + NPREP * k;
+            j.kown = k;
+            j.hd = hd;
+            j.lk = lk;
+            return j.c < n;
+        });
     }
+    if (!ok && tid == 0) drain_after_failure(p, sbase, mb, chain, ia, ib, st);
     if (tid == (chain ? kOIO : kIO)) bulk_store_wait();   // no bulk store may still read this CTA's shared memory
     cp_async_wait_all();
     fence_before_sync();
@@ -506,8 +606,74 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(NT, 1)
     cluster_barrier();                         // no CTA leaves while another may still address it
 }
 
+// The same work as a cooperative grid with one CTA per SM: CTA u < B * Hv carries the state of
+// (batch, v-head) u, every other CTA prepares chunks for all heads, job j = (chunk j / (B Hv),
+// unit j % (B Hv)) on preparer j % (number of preparers).  All CTAs are resident together (a
+// cooperative launch), so the flag waits between them always make progress.
+__global__ void __launch_bounds__(NT, 1) prefill_coop_kernel(const __grid_constant__ Tc05Params p) {
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sbase = smem_u32(sm);
+    const int units = p.B * p.Hv;
+    const bool chain = (int)blockIdx.x < units;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int n = (p.T + C - 1) / C;
+    auto link_of = [&](int u) {
+        return Link<true>{p.slots + (size_t)u * NSLOT_COOP * SLOT_BYTES, p.flags + 2 * NSLOT_COOP * u,
+                          p.flags + 2 * NSLOT_COOP * u + NSLOT_COOP};
+    };
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + (chain ? CH_TMEM : M_TMEM));
+    MmaBar mb{sbase + (chain ? CH_MBAR : M_MBAR), 0u, p.polls};
+    if (tid == 0) {
+        mbar_init(mb.mbar, 1);
+        if (chain) {
+            mbar_init(sbase + CH_FULL_A, 1);
+            mbar_init(sbase + CH_FULL_B, 1);
+        } else {
+            mbar_init(sbase + M_STAGE, 1);
+            mbar_init(sbase + M_DEAD, 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), T_COLS);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    int ia = 0, ib = 0;
+    StageTrack st;
+    bool ok;
+    if (chain) {
+        const int u = (int)blockIdx.x;
+        ok = run_chain<true>(p, head_of(p, u / p.Hv, u % p.Hv), sm, tmem, mb, n, link_of(u), ia, ib);
+    } else {
+        const int pid = (int)blockIdx.x - units, nprep = (int)gridDim.x - units;
+        const int64_t jobs_total = (int64_t)units * n;
+        ok = run_prep<true>(p, sm, tmem, mb, st, [&](int k, Job<true> &j) {
+            const int64_t jj = pid + (int64_t)nprep * k;
+            if (jj >= jobs_total) return false;
+            const int u = (int)(jj % units);
+            j.c = (int)(jj / units);
+            j.kown = k;
+            j.hd = head_of(p, u / p.Hv, u % p.Hv);
+            j.lk = link_of(u);
+            return true;
+        });
+    }
+    if (!ok && tid == 0) drain_after_failure(p, sbase, mb, chain, ia, ib, st);
+    if (tid == (chain ? kOIO : kIO)) bulk_store_wait();
+    cp_async_wait_all();
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, T_COLS);
+}
+
 std::mutex g_cluster_mutex;
 int g_cluster_fit[kMaxDevices];                         // per device: clusters resident at once, + 1 (0 = not queried)
+int g_coop_grid[kMaxDevices];                           // per device: CTAs of a cooperative grid, + 1 (0 = not queried)
+
+size_t coop_flag_bytes(const cgdr_args &a) { return ((size_t)a.B * a.Hv * 2 * NSLOT_COOP * sizeof(int) + 255) / 256 * 256; }
 
 }  // namespace
 
@@ -530,6 +696,48 @@ int prefill_cluster_capacity() {
         g_cluster_fit[dev] = fit + 1;
     }
     return g_cluster_fit[dev] - 1;
+}
+
+// CTAs of a cooperative grid of the cooperative kernel on the current device (every CTA resident
+// at once; 0 if the device cannot launch it).
+int prefill_coop_grid() {
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    std::lock_guard<std::mutex> lock(g_cluster_mutex);
+    if (g_coop_grid[dev] == 0) {
+        int grid = 0, coop = 0, per_sm = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            cudaFuncSetAttribute(prefill_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CL_SMEM_BYTES) ==
+                cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_coop_kernel, NT, CL_SMEM_BYTES) == cudaSuccess)
+            grid = per_sm * sms;
+        cudaGetLastError();
+        g_coop_grid[dev] = grid + 1;
+    }
+    return g_coop_grid[dev] - 1;
+}
+
+size_t prefill_coop_workspace(const cgdr_args &a) {
+    return WS_HEADER + coop_flag_bytes(a) + (size_t)a.B * a.Hv * NSLOT_COOP * SLOT_BYTES;
+}
+
+cgdr_status launch_prefill_coop(const cgdr_args &a, void *ws, size_t ws_bytes, cudaStream_t s) {
+    const int grid = prefill_coop_grid();
+    if (grid <= a.B * a.Hv) return CGDR_ERR_UNSUPPORTED;
+    Tc05Params p;
+    if (!make_params(a, ws, ws_bytes, p)) return CGDR_ERR_ALIGNMENT;
+    p.flags = reinterpret_cast<int *>(static_cast<unsigned char *>(ws) + WS_HEADER);
+    p.slots = static_cast<unsigned char *>(ws) + WS_HEADER + coop_flag_bytes(a);
+    // the status word and every sequence number start at 0
+    if (cudaMemsetAsync(ws, 0, WS_HEADER + coop_flag_bytes(a), s) != cudaSuccess) return CGDR_ERR_CUDA;
+    void *args[] = {&p};
+    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(prefill_coop_kernel), dim3(grid), dim3(NT), args,
+                                    CL_SMEM_BYTES, s) != cudaSuccess) {
+        cudaGetLastError();
+        return CGDR_ERR_CUDA;
+    }
+    return CGDR_OK;
 }
 
 size_t prefill_cluster_workspace(const cgdr_args &a) {

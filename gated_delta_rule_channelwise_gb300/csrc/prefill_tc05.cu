@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_tc05_kernel(const __grid_consta
     for (int t0 = 0; t0 < p.T && ok; t0 += C) {
         const int L = min(C, p.T - t0);
         if (!(ok = st.wait(sbase, p.polls, p.inject && t0 == 0))) break;
-        prep_chunk<true, false>(p, hd, sm, t0, L, t0 + C, sm + R_B, 64, cr);
+        prep_chunk<true, false>(p, hd, sm, t0, L, hd, t0 + C, sm + R_B, 64, cr);
         if (!(ok = causal_terms<false>(sm, tmem, mb, cr, sm + R_F, 64, 0))) break;
         solve_tb<false>(sm, cr);
         // ------------------------------------------------------------ W^T, U~^T (fp16 operands)
@@ -231,7 +231,7 @@ bool make_maps(const cgdr_args &a, Tc05Maps &tm) {
 
 bool make_params(const cgdr_args &a, void *ws, size_t ws_bytes, Tc05Params &p) {
     if (!make_maps(a, p.tm)) return false;
-    p.T = a.T; p.Hk = a.Hk; p.Hv = a.Hv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate;
+    p.B = a.B; p.T = a.T; p.Hk = a.Hk; p.Hv = a.Hv; p.l2norm = a.l2norm_qk != 0; p.gate = a.gate;
     p.o_f32 = a.o_dtype == CGDR_F32;
     p.q_scale = qscale_of(a); p.eps = eps_of(a);
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -256,6 +256,7 @@ bool make_params(const cgdr_args &a, void *ws, size_t ws_bytes, Tc05Params &p) {
     p.inject = inject_of(a);
     p.ext = extents_of(a, true, ws_bytes);
     p.slots = nullptr;
+    p.flags = nullptr;
     // o by TMA tensor stores where a map can describe it (a 16-byte aligned base and strides)
     p.o_tma = describable(p.o_f32 ? 4 : 2, a.dv, a, a.Hv, a.o_st, a.o_sh, a.o_sb) &&
               encode4(p.tm.o, p.o_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,

@@ -88,7 +88,7 @@ struct Tc05Maps {
 
 struct Tc05Params {
     Tc05Maps tm;                         // first: 64-byte aligned
-    int T, Hk, Hv, l2norm, gate, o_f32;
+    int B, T, Hk, Hv, l2norm, gate, o_f32;
     float q_scale, eps;
     const __nv_bfloat16 *q, *k, *v;
     int64_t q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh;
@@ -105,7 +105,8 @@ struct Tc05Params {
     uint32_t polls;                      // polls of the main-loop waits (drains use kSpin)
     int inject;                          // test hook: the first staging wait targets M_DEAD
     Extents ext;                         // footprints for the index checks of a debug build
-    unsigned char *slots;                // cluster kernel: hand-off ring in the workspace (unused per head)
+    unsigned char *slots;                // cluster kernels: hand-off ring in the workspace (unused per head)
+    int *flags;                          // cooperative kernel: the ring's sequence numbers
     int o_tma;                           // tm.o describes o (else o is written by thread stores)
 };
 
@@ -342,27 +343,27 @@ struct ChunkRegs {
 
 // Row norms, beta, the log-decay prefix and the decay-scaled operand tiles of
 // the chunk at t0 (L valid rows) from its staged raw rows; also prefetches the
-// rows at t_pf into L2.  The Qg tile goes to rows 0..63 of the qg_rows-row tile
+// rows of head hd_pf at t_pf into L2.  The Qg tile goes to rows 0..63 of the qg_rows-row tile
 // at qg (shared or global memory, same tile image).  Ends with the operand
 // tiles fenced for the tensor core.
 // kPrefetchQKV = false prefetches only the g rows (for callers that stage q, k, v early);
 // kQgF16: Qg as an fp16 tile (else TF32).
 template <bool kPrefetchQKV, bool kQgF16>
-__device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L, int t_pf,
-                                           char *qg, int qg_rows, ChunkRegs &cr) {
+__device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, char *sm, int t0, int L,
+                                           const Head &hd_pf, int t_pf, char *qg, int qg_rows, ChunkRegs &cr) {
     const int tid = threadIdx.x;
     const int ci = tid & 127, cq = tid >> 7;
     float *sRq = f32p(sm, M_RQ), *sRk = f32p(sm, M_RK), *sBeta = f32p(sm, M_BETA), *sGs = f32p(sm, M_GS);
     float *sQt = f32p(sm, M_H0), *sGm = f32p(sm, M_GM), *sGc = f32p(sm, M_GC), *sDec = f32p(sm, M_DEC);
     if (t_pf < p.T && tid == 0) {
         // L2 prefetch of the rows at t_pf, one TMA prefetch per tile
-        const int hk = hd.h / (p.Hv / p.Hk);
+        const int hk = hd_pf.h / (p.Hv / p.Hk);
         if (kPrefetchQKV) {
-            tma_prefetch(&p.tm.q, t_pf, hk, hd.b);
-            tma_prefetch(&p.tm.k, t_pf, hk, hd.b);
-            tma_prefetch(&p.tm.v, t_pf, hd.h, hd.b);
+            tma_prefetch(&p.tm.q, t_pf, hk, hd_pf.b);
+            tma_prefetch(&p.tm.k, t_pf, hk, hd_pf.b);
+            tma_prefetch(&p.tm.v, t_pf, hd_pf.h, hd_pf.b);
         }
-        if (p.gate == CGDR_GATE_CHANNEL) tma_prefetch(&p.tm.g, t_pf, hd.h, hd.b);
+        if (p.gate == CGDR_GATE_CHANNEL) tma_prefetch(&p.tm.g, t_pf, hd_pf.h, hd_pf.b);
     }
     // row norms from the staged raw q/k rows: four threads per row (q rows on warps 0-7, k rows
     // on warps 8-15), each summing 32 channels from four 16-byte pieces taken in a row-rotated

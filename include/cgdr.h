@@ -152,8 +152,11 @@ cgdr_status cgdr_decode(const cgdr_args *args, void *stream);
 /*
  * Bytes of device workspace cgdr_prefill needs for `args` (may be 0): 0 for
  * the CUDA-core kernel, 256 for the per-head tensor-core kernel (a status
- * word), and 256 + B * Hv * 741888 for the cluster kernel (the status word,
- * then nine 82432-byte hand-off slots per (batch, v-head)).  Depends on the
+ * word), 256 + B * Hv * 741888 for the cluster kernel (the status word,
+ * then nine 82432-byte hand-off slots per (batch, v-head)), and
+ * 256 + ceil256(64 * B * Hv) + B * Hv * 659456 for the cooperative kernel (the
+ * status word, 16 sequence numbers per (batch, v-head), then eight 82432-byte
+ * slots per (batch, v-head)).  Depends on the
  * kernel cgdr_prefill_path_for reports.  The workspace plays the part of the
  * single scratch arena of "Add parallel chunked prefill for channelwise gated
  * delta rule" (Summary), sliced per (batch, head) unit.  Returns 0 for
@@ -193,26 +196,30 @@ cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspac
  * (Summary); running them on different SMs has no counterpart there.
  */
 typedef enum cgdr_prefill_path {
-    CGDR_PREFILL_AUTO = 0,      /* per call: RECURRENT when 1 <= T <= 8; else CLUSTER or PER_HEAD,
-                                   whichever needs less time in waves of resident work (a cluster
-                                   carries a head ~3.3x faster per chunk, but 4x fewer are
-                                   resident); SIMT for shapes the tensor-core kernels do not cover */
+    CGDR_PREFILL_AUTO = 0,      /* per call: RECURRENT when 1 <= T <= 8; else COOP, CLUSTER or
+                                   PER_HEAD, whichever needs the least time by the cycles per chunk
+                                   each was measured at and how many heads each runs at once; SIMT
+                                   for shapes the tensor-core kernels do not cover */
     CGDR_PREFILL_PER_HEAD = 1,  /* tensor cores, one CTA per (batch, v-head) */
     CGDR_PREFILL_CLUSTER = 2,   /* tensor cores, a cluster of four CTAs per (batch, v-head):
                                    one carries the state, three prepare chunks for it */
     CGDR_PREFILL_SIMT = 3,      /* fp32 CUDA cores, chunked */
-    CGDR_PREFILL_RECURRENT = 4  /* 1 <= T <= 8: the token recurrence, fp32 CUDA cores, no
+    CGDR_PREFILL_RECURRENT = 4, /* 1 <= T <= 8: the token recurrence, fp32 CUDA cores, no
                                    workspace; for a longer T it means AUTO */
+    CGDR_PREFILL_COOP = 5       /* tensor cores, one cooperative grid of one CTA per SM: a CTA per
+                                   (batch, v-head) carries the state, every other CTA prepares
+                                   chunks for all heads (needs more SMs than heads; else AUTO) */
 } cgdr_prefill_path;
 
 /*
  * The kernel cgdr_prefill would run for `args` on the current device, given
  * args->prefill_path: CGDR_PREFILL_PER_HEAD, CGDR_PREFILL_CLUSTER,
- * CGDR_PREFILL_SIMT or CGDR_PREFILL_RECURRENT; CGDR_PREFILL_AUTO (0) if `args`
- * is invalid or there is nothing to do (B == 0 or T == 0).  A forced
- * tensor-core kernel applies only to the shapes it covers (else SIMT);
- * RECURRENT applies only to 1 <= T <= 8 (else the automatic choice).  Queries
- * the SM count and the cluster capacity once per device.
+ * CGDR_PREFILL_COOP, CGDR_PREFILL_SIMT or CGDR_PREFILL_RECURRENT;
+ * CGDR_PREFILL_AUTO (0) if `args` is invalid or there is nothing to do (B == 0
+ * or T == 0).  A forced tensor-core kernel applies only to the shapes it covers
+ * (else SIMT); COOP only with more resident CTAs than heads, and RECURRENT
+ * only to 1 <= T <= 8 (else the automatic choice).  Queries the SM count, the
+ * cluster capacity and the cooperative grid size once per device.
  */
 int cgdr_prefill_path_for(const cgdr_args *args);
 

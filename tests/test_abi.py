@@ -135,7 +135,7 @@ def test_validation_accepts_good_args(lib):
     (dict(v_st=12), True, cg.ERR_ALIGNMENT),
     (dict(g_sb=2), False, cg.ERR_ALIGNMENT),
     (dict(o_sb=-8), False, cg.ERR_ALIGNMENT),
-    (dict(prefill_path=5), True, cg.ERR_INVALID_ARG),
+    (dict(prefill_path=6), True, cg.ERR_INVALID_ARG),
     (dict(prefill_path=-1), True, cg.ERR_INVALID_ARG),
     (dict(status=(9 << 20) + 2), False, cg.ERR_ALIGNMENT),
 ])
@@ -191,7 +191,7 @@ def test_prefill_path_choice(lib):
     tensor-core kernel applies only to the shapes it covers (bf16, dk = dv = 128, chunk 64);
     out-of-range choices are rejected."""
     path_for = lambda A: lib.cgdr_prefill_path_for(ctypes.byref(A))
-    for bad in (5, -1, 9):
+    for bad in (6, -1, 9):
         assert path_for(_args(T=100, prefill_path=bad)) == cg.PREFILL_AUTO       # invalid arguments
     for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
         assert path_for(_args(T=100, prefill_path=path)) == path
@@ -204,10 +204,14 @@ def test_prefill_path_choice(lib):
         for kw in ({}, dict(dtype=cg.F32, q_sb=8 * 128, q_st=2 * 128, q_sh=128), dict(dk=32, dv=64)):
             assert path_for(_args(T=T, **kw)) == cg.PREFILL_RECURRENT
         assert lib.cgdr_prefill_workspace_size(ctypes.byref(_args(T=T))) == 0
-    assert path_for(_args(T=9)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
+    assert path_for(_args(T=9)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_COOP)
     assert path_for(_args(T=2, prefill_path=cg.PREFILL_PER_HEAD)) == cg.PREFILL_PER_HEAD
     assert path_for(_args(T=3, prefill_path=cg.PREFILL_RECURRENT)) == cg.PREFILL_RECURRENT
-    assert path_for(_args(T=100, prefill_path=cg.PREFILL_RECURRENT)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)
+    assert path_for(_args(T=100, prefill_path=cg.PREFILL_RECURRENT)) in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER,
+                                                                         cg.PREFILL_COOP)
+    # the cooperative kernel needs more resident CTAs than heads; without a device it falls back
+    assert path_for(_args(T=100, prefill_path=cg.PREFILL_COOP)) in (cg.PREFILL_COOP, cg.PREFILL_PER_HEAD,
+                                                                    cg.PREFILL_CLUSTER)
     assert path_for(_args(T=0)) == cg.PREFILL_AUTO
     assert path_for(_args(T=100, dk=96)) == cg.PREFILL_AUTO
     assert lib.cgdr_prefill_path_for(None) == cg.PREFILL_AUTO

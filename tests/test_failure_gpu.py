@@ -89,30 +89,33 @@ def test_decode_wait_gives_up():
     assert rel_err(good_state, S_ref) <= TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_COOP])
 @pytest.mark.parametrize("gate", ["channel", "gdn"])
-def test_prefill_per_head_wait_gives_up(gate):
-    """The per-head tensor-core prefill on one chunk of one head: the staging wait for the
-    chunk's rows gives up (test hook) while those rows are still being copied in; both status
-    words read CGDR_ERR_TIMEOUT, the state is untouched, and a normal call afterwards on the
-    same context and workspace matches the oracle."""
+def test_prefill_wait_gives_up(gate, path):
+    """A tensor-core prefill on one chunk of one head: the staging wait for the chunk's rows
+    gives up (test hook) while those rows are still being copied in, and with it (cluster and
+    cooperative kernels) the state CTA's wait for the chunk's hand-off; both status words read
+    CGDR_ERR_TIMEOUT, the state is untouched, and a normal call afterwards on the same context
+    and workspace matches the oracle."""
     w, inp = _inputs(64, gate=gate, seed=12)
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    n = cg.prefill_workspace_size(inp["q"], inp["k"], inp["v"], inp["S0"], torch.empty(inp["v"].shape, device="cuda"),
+                                  path=path, chunk=64, **gate_kwargs(inp))
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     state = inp["S0"].clone()
-    cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=cg.PREFILL_PER_HEAD, workspace=ws, status=st,
+    cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=path, workspace=ws, status=st,
                wait_polls=-4, **gate_kwargs(inp))
     assert cg.workspace_status(ws) == cg.ERR_TIMEOUT
     assert int(st.item()) == cg.ERR_TIMEOUT
     assert torch.equal(state, inp["S0"])
-    o = cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=cg.PREFILL_PER_HEAD, workspace=ws,
-                   **gate_kwargs(inp))
+    o = cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=path, workspace=ws, **gate_kwargs(inp))
     assert cg.workspace_status(ws) == cg.OK
     o_ref, S_ref = oracle_run(inp)
     assert rel_err(o, o_ref) <= TOL[torch.bfloat16]
     assert rel_err(state, S_ref) <= TOL[torch.bfloat16]
 
 
-@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER])
+@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_COOP])
 def test_fp16_operand_range(path):
     """The tensor-core kernels carry some products in fp16 operands.  Inputs well inside the
     fp16 range report CGDR_OK; a v of magnitude 1e5 (a valid bf16 value beyond the largest
@@ -140,7 +143,7 @@ def test_fp16_operand_range(path):
             assert rel_err(o, o_ref) <= TOL[torch.bfloat16] and rel_err(state, S_ref) <= TOL[torch.bfloat16]
 
 
-@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER])
+@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_COOP])
 def test_growing_gate_range(path):
     """A positive log-decay (a gate that grows the state) scales keys by e^(sum of g); 64 tokens of
     g = +0.5 reach e^32, beyond fp16: CGDR_ERR_RANGE, not a silent overflow."""

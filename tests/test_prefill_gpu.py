@@ -23,7 +23,18 @@ def _built():
     cg.lib()
 
 
-TC_PATHS = [pytest.param(cg.PREFILL_PER_HEAD, id="per_head"), pytest.param(cg.PREFILL_CLUSTER, id="cluster")]
+TC_PATHS = [pytest.param(cg.PREFILL_PER_HEAD, id="per_head"), pytest.param(cg.PREFILL_CLUSTER, id="cluster"),
+            pytest.param(cg.PREFILL_COOP, id="coop")]
+
+
+def _ws_bytes(path, units):
+    """Workspace of each tensor-core kernel: the status word, then (cluster) nine 82432-byte
+    hand-off slots per (batch, v-head), or (cooperative) 16 sequence numbers and eight slots."""
+    if path == cg.PREFILL_PER_HEAD:
+        return 256
+    if path == cg.PREFILL_CLUSTER:
+        return 256 + units * 9 * 82432
+    return 256 + (64 * units + 255) // 256 * 256 + units * 8 * 82432
 
 
 @pytest.fixture(params=TC_PATHS)
@@ -87,7 +98,7 @@ def test_fp32_chunk_sizes_and_tails(chunk, T, dk, dv, simt_path):
 @pytest.mark.parametrize("dv", [32, 64, 128])
 @pytest.mark.parametrize("gate", ["channel", "gdn"])
 def test_tensor_core_path_tails(T, dv, gate, tc_path):
-    if dv != 128 and tc_path == cg.PREFILL_CLUSTER:
+    if dv != 128 and tc_path != cg.PREFILL_PER_HEAD:
         pytest.skip("dv < 128 runs the CUDA-core kernel whatever the choice")
     w = Workload("tc", B=2, Hk=1, Hv=2, dk=128, dv=dv, T=T, dtype="bf16", gate=gate, seed=T * 3 + dv)
     inp = make_inputs(w, device="cuda")
@@ -222,7 +233,7 @@ def test_tensor_core_path_reports_ok_status(tc_path):
     state = inp["S0"].clone()
     n = cg.prefill_workspace_size(inp["q"], inp["k"], inp["v"], state, torch.empty(inp["v"].shape, device="cuda"),
                                   path=tc_path, **gate_kwargs(inp))
-    assert n == (256 if tc_path == cg.PREFILL_PER_HEAD else 256 + 9 * 82432)   # + hand-off slots
+    assert n == _ws_bytes(tc_path, 1)
     ws = torch.full((n,), 0x7F, dtype=torch.uint8, device="cuda")
     cg.prefill(inp["q"], inp["k"], inp["v"], state, chunk=64, path=tc_path, workspace=ws, **gate_kwargs(inp))
     assert cg.workspace_status(ws) == cg.OK
@@ -239,17 +250,19 @@ def test_mixed_wide_and_narrow_chunks(tc_path):
     _check(w, inp, o, s)
 
 
-def test_both_tensor_core_kernels_agree():
-    """The per-head and the cluster kernel run the same chunk algorithm (both read the state
-    operand from tensor memory); only the grouping of their MMAs differs, so they agree far
-    inside the oracle tolerance (on GB300 they agree exactly)."""
+def test_tensor_core_kernels_agree():
+    """The three tensor-core kernels run the same chunk algorithm; the cluster and the
+    cooperative kernel also run the very same per-chunk code (only the hand-off between their
+    CTAs differs), so those two agree bit for bit, and with the per-head kernel (TF32 state
+    products where they use fp16) far inside the oracle tolerance."""
     w = Workload("agree", B=1, Hk=2, Hv=4, dk=128, dv=128, T=700, dtype="bf16", gate="channel", seed=55)
     inp = make_inputs(w, device="cuda")
-    outs = [_prefill(inp, 64, path=path) for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER)]
-    (o1, s1), (o2, s2) = outs
+    (o1, s1), (o2, s2), (o3, s3) = [_prefill(inp, 64, path=path)
+                                    for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_COOP)]
     eo, es = rel_err(o2, o1.double().cpu().numpy()), rel_err(s2, s1.double().cpu().numpy())
     print("[kernels] o %.3e S %.3e" % (eo, es))
     assert eo <= 5e-3 and es <= 5e-3
+    assert torch.equal(o3, o2) and torch.equal(s3, s2)
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
@@ -277,7 +290,7 @@ def test_recurrent_matches_chunked_kernels():
     w = Workload("rec8", B=2, Hk=2, Hv=2, dk=128, dv=128, T=8, dtype="bf16", gate="channel", seed=77)
     inp = make_inputs(w, device="cuda")
     o_r, s_r = _prefill(inp, 64)
-    for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_SIMT):
+    for path in (cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_COOP, cg.PREFILL_SIMT):
         _expect_path(inp, path, path)
         o_c, s_c = _prefill(inp, 64, path=path)
         assert rel_err(o_c, o_r.double().cpu().numpy()) <= 2e-2
