@@ -66,7 +66,7 @@ constexpr int CH_MBAR = CH_MISC, CH_FULL_A = CH_MISC + 8, CH_FULL_B = CH_MISC + 
 constexpr int CH_READY = CH_MISC + 32;           // NSLOT barriers, one per slot
 constexpr int CH_OST = CH_MISC + 1024;           // o of one chunk [64 tokens][128] in o's dtype (TMA store source)
 constexpr int CH_END = CH_OST + 32768;
-static_assert(CH_READY + 8 * NSLOT <= CH_MISC + 128, "barriers overlap");
+static_assert(CH_READY + 8 * NSLOT <= CH_OST, "misc words overlap");
 static_assert(SL_KG == 16384 && CH_A_REST + (int)A_REST_BYTES <= CH_UR, "inbox A overlaps");
 static_assert(CH_QW % 1024 == 0 && CH_UR % 1024 == 0 && CH_IN_B % 1024 == 0 && CH_KG % 1024 == 0 &&
               CH_VT % 1024 == 0 && CH_TB % 1024 == 0, "tiles must be 1024-aligned");
@@ -468,8 +468,8 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
 // shared-memory tile it was built in, as soon as the tile is complete; the staging of the next
 // job's rows follows once the tiles have been read.  Thread 0 issues the tensor-core work and
 // the TMA staging; thread kIO (a warp with no part in the triangular solve's serial steps)
-// issues the bulk stores, waits for their reads, and announces job k after the operand phase of
-// job k + 1 (or after the loop), when its stores have long completed.
+// issues the bulk stores, waits for their reads, and announces job k > 0 after the operand phase
+// of job k + 1 (or after the loop), when its stores have long completed (job 0 at once).
 constexpr int kIO = 448;
 
 template <bool kCoop>
@@ -492,6 +492,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, char *sm, uint32_t
     st.stage<STG_V | STG_K | STG_ONCE>(p, cur.hd, sbase, cur.c * C);
     st.stage<STG_Q | STG_G | STG_ONCE | STG_LAST>(p, cur.hd, sbase, cur.c * C);
     ChunkRegs cr;
+    bool pending = false;                        // (thread kIO) prev has not been announced yet
     for (int k = 0;; ++k) {
         const bool more = jobs(k + 1, nxt);
         const int t0 = cur.c * C, L = min(C, p.T - t0);
@@ -500,7 +501,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, char *sm, uint32_t
         // operand tiles; prefetch the next job's g rows into L2 (they are staged last)
         prep_chunk<false, true>(p, cur.hd, sm, t0, L, more ? nxt.hd : cur.hd, more ? nxt.c * C : p.T, sm + R_B, 64, cr);
         if (tid == kIO) {
-            if (k > 0) prev.lk.announce(sbase, prev.c);
+            if (pending) prev.lk.announce(sbase, prev.c);
             // the slot's previous chunk has been pulled by the state CTA
             const int okw = cur.lk.free_wait(sbase, cur.c, cur.kown, p.polls);
             if (okw) {
@@ -527,6 +528,10 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, char *sm, uint32_t
             ring_store(p, slot + SL_KP, sbase + A1_KE, 16384);             // Kend^T: rows 0..127 of [Kend^T; P]
             bulk_commit();
             bulk_wait_read<0>();                                           // R_B, R_C, R_F, R_G, A1_KE read
+            // the first job is announced at once (its state CTA has nothing else to work on);
+            // later ones after the next job's operand phase, when their stores have long completed
+            pending = k > 0;
+            if (k == 0) cur.lk.announce(sbase, cur.c);
         }
         __syncthreads();
         prev = cur;
@@ -534,7 +539,7 @@ __device__ __forceinline__ bool run_prep(const Tc05Params &p, char *sm, uint32_t
         st.stage<STG_Q | STG_V | STG_K | STG_G | STG_ONCE | STG_LAST>(p, nxt.hd, sbase, nxt.c * C);
         cur = nxt;
     }
-    if (tid == kIO) prev.lk.announce(sbase, prev.c);                      // the last job
+    if (tid == kIO && pending) prev.lk.announce(sbase, prev.c);           // the last job
     return true;
 }
 
