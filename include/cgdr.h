@@ -175,9 +175,10 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
  * Paths: 1 <= T <= 8 runs the token recurrence itself (the decode kernel
  * stepping through the tokens, each state tile read once and written once;
  * the chunk length plays no part); otherwise bf16 inputs with dk = dv = 128
- * and chunk 64 run one of the two tensor-core kernels (tcgen05; TF32 operands
- * for the anchored causal terms and the state products, fp16 operands for the
- * others, fp32 accumulation and state), and every other case an fp32
+ * and chunk 64 run one of the three tensor-core kernels (tcgen05; TF32
+ * operands for the anchored causal terms, fp16 operands for the other products
+ * -- the per-head kernel keeps its state products in TF32 --, fp32
+ * accumulation and state), and every other case an fp32
  * CUDA-core kernel; args->prefill_path can force a kernel for this call.
  * Workspace: the tensor-core path needs cgdr_prefill_workspace_size() bytes
  * (16-byte aligned); its first int32 is set to CGDR_ERR_TIMEOUT if a bounded
@@ -188,9 +189,10 @@ size_t cgdr_prefill_workspace_size(const cgdr_args *args);
 cgdr_status cgdr_prefill(const cgdr_args *args, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * The kernels behind cgdr_prefill.  The two tensor-core kernels cover bf16
- * inputs with dk = dv = 128 and chunk 64 and agree up to rounding order; the
- * CUDA-core kernel covers every supported shape.  The split of the chunk's
+ * The kernels behind cgdr_prefill.  The three tensor-core kernels cover bf16
+ * inputs with dk = dv = 128 and chunk 64 and agree up to rounding (the
+ * cluster and cooperative kernels bit for bit); the CUDA-core kernel covers
+ * every supported shape.  The split of the chunk's
  * work into a state-free part and the state carry follows the chunkwise form
  * of "Add parallel chunked prefill for channelwise gated delta rule"
  * (Summary); running them on different SMs has no counterpart there.
