@@ -306,7 +306,11 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
         } else {
             __nv_bfloat16 *t = reinterpret_cast<__nv_bfloat16 *>(sm + CH_OST);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) t[(16 * wc + k) * DV + trow] = __float2bfloat16_rn(ov[k]);
+            for (int k = 0; k < 16; k += 2) {                  // tokens in pairs: one conversion each
+                const __nv_bfloat162 h = __floats2bfloat162_rn(ov[k], ov[k + 1]);
+                t[(16 * wc + k) * DV + trow] = __low2bfloat16(h);
+                t[(16 * wc + k + 1) * DV + trow] = __high2bfloat16(h);
+            }
         }
         fence_smem_to_async();
     };
@@ -361,7 +365,7 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             float w16[16];
             tmem_ld16(tmem + lane_off + T_W + 16 * wc, w16);                 // -W [r][i] into rows 64..127
 #pragma unroll
-            for (int j = 0; j < 16; ++j) st_h(sm, CH_QW, 128, 64 + 16 * wc + j, trow, -w16[j], amax);
+            for (int j = 0; j < 16; j += 2) st_h_rows(sm, CH_QW, 128, 64 + 16 * wc + j, trow, -w16[j], -w16[j + 1], amax);
             if (amax > kF16Max) record_range(p.err, p.status);
         }
         if (c > 0) tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);       // o of chunk c - 1

@@ -158,6 +158,15 @@ __device__ __forceinline__ void st_h(char *base, int region, int R, int r, int k
     amax = fmaxf(amax, fabsf(x));
     *reinterpret_cast<__half *>(base + region + sw_off16(R, r, k)) = __float2half_rn(x);
 }
+// Elements (r, k) = a and (r + 1, k) = b of an fp16 tile, converted together (one paired
+// conversion instead of two).
+__device__ __forceinline__ void st_h_rows(char *base, int region, int R, int r, int k, float a, float b,
+                                          float &amax) {
+    amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+    const __half2 h = __floats2half2_rn(a, b);
+    *reinterpret_cast<__half *>(base + region + sw_off16(R, r, k)) = __low2half(h);
+    *reinterpret_cast<__half *>(base + region + sw_off16(R, r + 1, k)) = __high2half(h);
+}
 // One pass over this thread's 32 columns [i0, i0 + 32) of S^T in tensor memory (lane quarter
 // at lane_off): the fp16 copy into columns s16 + i0 / 2 .. (the A operand of the state
 // products), then S^T <- S^T Diag(dec) in place.  Two 16-column halves keep few registers live.
@@ -465,7 +474,7 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
         const float emv = gm > -80.f ? __expf(gm) : 0.f;
         const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_Q);
         const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_K);
-        float kg4[4], rk4[4], rq4[4], be4[4];
+        float kg4[4], rk4[4], rq4[4], be4[4], qprev = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int r = 16 * cq + jj;
@@ -482,8 +491,12 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             float eg, e1 = 0.f;
             if (!wide) e1 = __expf(cr.lam[jj] - gm);
             eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
-            if (kQgF16) st_h(qg, 0, qg_rows, r, ci, qt * eg, cr.amax);   // Qg [r][i]
-            else st_raw(qg, 0, qg_rows, r, ci, qt * eg);            // (taken as TF32 by truncation)
+            if (kQgF16) {                                           // Qg [r][i], rows in pairs
+                if (jj & 1) st_h_rows(qg, 0, qg_rows, r - 1, ci, qprev, qt * eg, cr.amax);
+                else qprev = qt * eg;
+            } else {
+                st_raw(qg, 0, qg_rows, r, ci, qt * eg);             // (taken as TF32 by truncation)
+            }
             kg4[jj & 3] = kt * eg;
             if ((jj & 3) == 3) st_h4(sm, R_C, 128, ci, r - 3, kg4[0], kg4[1], kg4[2], kg4[3], cr.amax);   // Kg^T [i][s]
             if (!wide) {
@@ -739,8 +752,12 @@ __device__ __forceinline__ void store_o(const Tc05Params &p, int64_t obase, uint
     } else {
         __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(p.o) + off0;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-            if (c < nv && in_bounds(off0 + c * p.o_st, p.ext.o, p.err, p.status)) op[c * p.o_st] = __float2bfloat16_rn(v[c]);
+        for (int c = 0; c < 16; c += 2) {                      // tokens in pairs: one conversion each
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[c], v[c + 1]);
+            if (c < nv && in_bounds(off0 + c * p.o_st, p.ext.o, p.err, p.status)) op[c * p.o_st] = __low2bfloat16(h);
+            if (c + 1 < nv && in_bounds(off0 + (c + 1) * p.o_st, p.ext.o, p.err, p.status))
+                op[(c + 1) * p.o_st] = __high2bfloat16(h);
+        }
     }
 }
 
