@@ -49,12 +49,12 @@ constexpr float kRange = 80.f;           // max |gamma_r - gamma_mid| for the te
 constexpr uint32_t kSpin = kDefaultPolls;   // bounded mbarrier wait (polls) of the drains after a failure
 
 // shared memory map of a CTA that prepares chunks (bytes from a 1024-aligned base)
-constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, Kend^T (fp16) | U^T (fp16) ; wide: q~, k~
+constexpr int R_A1 = 0;                  // 64 KB: X1 | A32 + scratch, Kend^T (fp16), X fp32 | U^T (fp16) ; wide: q~, k~
 constexpr int R_A2 = 65536;              // 32 KB: X2 (kn e^(gm-g)), the source of Kend ; wide: gamma
 constexpr int R_B = 98304;               // 32 KB: Qg = qn e^g [64 x 128] (TF32, or fp16 for the cluster kernel)
 constexpr int R_C = 131072;              // 32 KB: Kg^T [128 x 64], V^T [128 x 64] | -W [64 x 128] (fp16)
 constexpr int R_F = 163840;              // 16 KB: P  [64 x 64] (fp16)
-constexpr int R_G = 180224;              // 16 KB: Xs fp32 [64][64] | Tb [64 x 64] (fp16)
+constexpr int R_G = 180224;              // 16 KB: Tb [64 x 64] (fp16)
 constexpr int R_MISC = 196608;
 // misc (fp32 unless noted)
 constexpr int M_RQ = R_MISC, M_RK = M_RQ + 256, M_BETA = M_RK + 256, M_GS = M_BETA + 256;
@@ -66,10 +66,11 @@ constexpr int M_DEAD = M_FLAG + 8;        // a barrier nothing arrives on (targe
 constexpr int M_END = M_DEAD + 8;
 constexpr int PREP_SMEM_BYTES = M_END + 1024;            // + alignment slack
 constexpr int LDA = 68;                  // fp32 A rows (padded, 16-byte aligned)
-constexpr int LDZ = 20;                  // fp32 rows of the six 16 x 16 Z blocks (padded)
+constexpr int LDZ = 20;                  // fp32 rows of the ten 16 x 16 Z blocks of the solve (padded)
 constexpr int A1_A32 = R_A1, A1_Z = R_A1 + 64 * LDA * 4, A1_KE = R_A1 + 32768;   // Kend^T built during the solve
 constexpr int RC_VT = R_C + 16384;       // V^T beside Kg^T
-static_assert(A1_Z + 6 * 16 * LDZ * 4 <= A1_KE, "A1 overflow");
+constexpr int A1_XS = R_A1 + 49152;     // fp32 X = (I + A)^-1 during the solve (16 KB)
+static_assert(A1_Z + 10 * 16 * LDZ * 4 <= A1_KE && A1_KE + 16384 <= A1_XS && A1_XS + 16384 <= R_A2, "A1 overflow");
 // Staged raw inputs of a chunk (TMA tiles; beta by cp.async), loaded while an earlier chunk finishes:
 // q rows -> F, k rows -> G (bf16 [64][128]); g rows -> A2 (fp32 [64][128]);
 // v rows -> B (bf16 [64][128]); beta -> B + 16 KB (fp32 [64]).
@@ -619,25 +620,76 @@ __device__ __forceinline__ void build_kend(char *sm, ChunkRegs &cr) {
     }
 }
 
-// Element (r, c) of the 64 x 64 fp32 X = (I + A)^-1 held in R_G: rows of 64
-// floats with the 16-byte chunks XOR-swizzled by r % 8, so that a float4 of
-// eight different rows hits eight different bank groups.
+// Element (r, c) of the 64 x 64 fp32 X = (I + A)^-1 held in A1_XS during the solve: rows of 64
+// floats with the 16-byte chunks XOR-swizzled by r % 8, so that a float4 of eight different
+// rows hits eight different bank groups.
 __device__ __forceinline__ int xs_off(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
+
+// Operands of the 16 x 16 block products of the solve: the float4 at (r, c), c a multiple of 4,
+// of a block of X (A1_XS), of A (A1_A32) or of one of the Z blocks (A1_Z).
+struct XsBlk {
+    const float *p;
+    int r0, c0;
+    __device__ __forceinline__ float4 operator()(int r, int c) const {
+        return *reinterpret_cast<const float4 *>(p + xs_off(r0 + r, c0 + c));
+    }
+};
+struct ABlk {
+    const float *p;
+    int r0, c0;
+    __device__ __forceinline__ float4 operator()(int r, int c) const {
+        return *reinterpret_cast<const float4 *>(p + (r0 + r) * LDA + c0 + c);
+    }
+};
+struct ZBlk {
+    const float *p;
+    int blk;
+    __device__ __forceinline__ float4 operator()(int r, int c) const {
+        return *reinterpret_cast<const float4 *>(p + (blk * 16 + r) * LDZ + c);
+    }
+};
+
+// acc += L R for 16 x 16 blocks, one warp per block: the lane owns rows rp and rp + 8
+// (rp = lane % 8) and columns c4 .. c4 + 3 (c4 = 4 (lane / 8)).  Each quarter-warp reads one
+// float4 of R per step (one address per four lanes) and eight rows of L in distinct bank groups.
+template <class L, class R>
+__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const L &lf, const R &rt, int rp, int c4) {
+#pragma unroll
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+        const float4 l0 = lf(rp, k4), l1 = lf(rp + 8, k4);
+        const float lv[2][4] = {{l0.x, l0.y, l0.z, l0.w}, {l1.x, l1.y, l1.z, l1.w}};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float4 b = rt(k4 + kk, c4);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                acc[i][0] = fmaf(lv[i][kk], b.x, acc[i][0]);
+                acc[i][1] = fmaf(lv[i][kk], b.y, acc[i][1]);
+                acc[i][2] = fmaf(lv[i][kk], b.z, acc[i][2]);
+                acc[i][3] = fmaf(lv[i][kk], b.w, acc[i][3]);
+            }
+        }
+    }
+}
 
 // Tb = (I + A)^-1 Diag(beta) into R_G as an fp16 tile, by 16 x 16 blocks (and with kKend, while
 // 64 threads run the diagonal substitution, Kend^T = (kn e^(gC - g))^T into A1_KE as an fp16
-// tile; see build_kend):
-// X_RR = (I + A_RR)^-1 by forward substitution (four blocks at once), then
-// Z_Rm = X_RR A_Rm for the six pairs m < R, then X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS
-// one block diagonal at a time.  Each thread of the product steps owns four
-// consecutive columns of one row (float4 loads).  Ends with Tb fenced for the
-// tensor core.
+// tile; see build_kend).  With X_RR = (I + A_RR)^-1 and Z_Rm = X_RR A_Rm, block row R of
+// (I + A) X = I gives X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS for R > S.  After the diagonal blocks
+// (forward substitution, one thread per column), three block-product phases, one warp per
+// 16 x 16 product:
+//   Z_Rm for the six pairs m < R (and the zero blocks above the diagonal of Tb);
+//   X_10, X_21, X_32 from the diagonal blocks, and Z'_30 = Z_30 - Z_32 Z_20, Z'_31 = Z_31 - Z_32 Z_21;
+//   X_20, X_31, and X_30 = -(Z'_30 X_00 + Z'_31 X_10) (X_20 substituted into the row-3 sum),
+//   the two products of each block on two warps.
+// Every block of Tb is stored (scaled by beta, in fp16) by the warp that forms it; X stays in
+// fp32 in A1_XS for the later phases.  Ends with Tb fenced for the tensor core.
 template <bool kKend>
 __device__ __forceinline__ void solve_tb(char *sm, ChunkRegs &cr) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float &amax = cr.amax;
     const float *sA = f32p(sm, A1_A32), *sBeta = f32p(sm, M_BETA);
-    float *sZ = f32p(sm, A1_Z), *sXs = f32p(sm, R_G);
+    float *sZ = f32p(sm, A1_Z), *sXs = f32p(sm, A1_XS);
     if (kKend && tid >= 64 && tid < 448) {
         // Kend^T [i][s] = X2 [s][i] e^(gC_i - gm_i) (a wide chunk's X2 region holds the Kend
         // source itself): thread (channel i, row quads q0, q0 + 3, ...)
@@ -650,6 +702,7 @@ __device__ __forceinline__ void solve_tb(char *sm, ChunkRegs &cr) {
         }
     }
     if (tid < 64) {
+        // X_RR column jc (zero above the diagonal, as the recurrence gives), and Tb's diagonal block
         const int Rb = tid >> 4, jc = tid & 15;
         float x[16];
 #pragma unroll
@@ -659,75 +712,98 @@ __device__ __forceinline__ void solve_tb(char *sm, ChunkRegs &cr) {
             for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-sA[(16 * Rb + r) * LDA + 16 * Rb + s2], x[s2], acc);
             x[r] = acc;
         }
+        const float bj = sBeta[16 * Rb + jc];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sXs[xs_off(16 * Rb + r, 16 * Rb + jc)] = x[r];
+        for (int r = 0; r < 16; ++r) {
+            sXs[xs_off(16 * Rb + r, 16 * Rb + jc)] = x[r];
+            st_h(sm, R_G, 64, 16 * Rb + r, 16 * Rb + jc, x[r] * bj, amax);
+        }
     }
     __syncthreads();
-    // Z_Rm = X_RR A_Rm: 6 pairs x 16 rows x 4 column quads (pair index R(R-1)/2 + m)
-    if (tid < 384) {
-        const int pi = tid >> 6, rho = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-        const int Rb = pi == 0 ? 1 : (pi < 3 ? 2 : 3), mb = pi - Rb * (Rb - 1) / 2;
-        const int xr = 16 * Rb + rho;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
+    const int rp = lane & 7, c4 = 4 * (lane >> 3);
+    float acc[2][4];
+    auto zero = [&]() {
 #pragma unroll
-        for (int u4 = 0; u4 < 16; u4 += 4) {
-            const float4 xv = *reinterpret_cast<const float4 *>(sXs + xs_off(xr, 16 * Rb + u4));
-            const float xs4[4] = {xv.x, xv.y, xv.z, xv.w};
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int uu = 0; uu < 4; ++uu) {
-                const float4 av = *reinterpret_cast<const float4 *>(sA + (16 * Rb + u4 + uu) * LDA + 16 * mb + c4);
-                a[0] = fmaf(xs4[uu], av.x, a[0]);
-                a[1] = fmaf(xs4[uu], av.y, a[1]);
-                a[2] = fmaf(xs4[uu], av.z, a[2]);
-                a[3] = fmaf(xs4[uu], av.w, a[3]);
-            }
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    };
+    auto put_z = [&](int blk, float sg) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<float4 *>(sZ + (blk * 16 + rp + 8 * i) * LDZ + c4) =
+                make_float4(sg * acc[i][0], sg * acc[i][1], sg * acc[i][2], sg * acc[i][3]);
+    };
+    auto put_x = [&](int Rb, int Sb) {                 // X_RS = -acc, kept for the next phase
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<float4 *>(sXs + xs_off(16 * Rb + rp + 8 * i, 16 * Sb + c4)) =
+                make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
+    };
+    auto put_tb = [&](int Rb, int Sb) {                // Tb_RS = -acc Diag(beta_S)
+        const float4 be = *reinterpret_cast<const float4 *>(sBeta + 16 * Sb + c4);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            st_h4(sm, R_G, 64, 16 * Rb + rp + 8 * i, 16 * Sb + c4, -acc[i][0] * be.x, -acc[i][1] * be.y,
+                  -acc[i][2] * be.z, -acc[i][3] * be.w, amax);
+    };
+    auto neg_z = [&](int blk) {                        // acc = -Z_blk
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float4 z = ZBlk{sZ, blk}(rp + 8 * i, c4);
+            acc[i][0] = -z.x; acc[i][1] = -z.y; acc[i][2] = -z.z; acc[i][3] = -z.w;
         }
-        *reinterpret_cast<float4 *>(sZ + (pi * 16 + rho) * LDZ + c4) = make_float4(a[0], a[1], a[2], a[3]);
+    };
+    // Z block index of pair (R, m): R (R - 1) / 2 + m; block 6 holds Z'_31, blocks 7..9 the
+    // second products of the last phase
+    if (warp < 6) {
+        const int Rb = warp == 0 ? 1 : (warp < 3 ? 2 : 3), mb = warp - Rb * (Rb - 1) / 2;
+        zero();
+        blk_mma(acc, XsBlk{sXs, 16 * Rb, 16 * Rb}, ABlk{sA, 16 * Rb, 16 * mb}, rp, c4);
+        put_z(warp, 1.f);
+    } else if (warp < 12) {
+        // block (R, S), R < S, of Tb is zero: lane = (row, 8-column half), one 16-byte store
+        const int u = warp - 6, Rb = u < 3 ? 0 : (u < 5 ? 1 : 2), Sb = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3);
+        *reinterpret_cast<uint4 *>(sm + R_G + sw_off16(64, 16 * Rb + (lane >> 1), 16 * Sb + 8 * (lane & 1))) =
+            make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
-    // X_RS = -sum_{m=S}^{R-1} Z_Rm X_mS, one block diagonal d = R - S at a time
-#pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        if (tid < (4 - d) * 64) {
-            const int blk = tid >> 6, Rb = d + blk, Sb = Rb - d, rho = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < d; ++j) {
-                const int mm = Sb + j;
-                const float *z = sZ + ((Rb * (Rb - 1) / 2 + mm) * 16 + rho) * LDZ;
-#pragma unroll
-                for (int u4 = 0; u4 < 16; u4 += 4) {
-                    const float4 zv = *reinterpret_cast<const float4 *>(z + u4);
-                    const float zs4[4] = {zv.x, zv.y, zv.z, zv.w};
-#pragma unroll
-                    for (int uu = 0; uu < 4; ++uu) {
-                        const float4 xv = *reinterpret_cast<const float4 *>(sXs + xs_off(16 * mm + u4 + uu, 16 * Sb + c4));
-                        a[0] = fmaf(zs4[uu], xv.x, a[0]);
-                        a[1] = fmaf(zs4[uu], xv.y, a[1]);
-                        a[2] = fmaf(zs4[uu], xv.z, a[2]);
-                        a[3] = fmaf(zs4[uu], xv.w, a[3]);
-                    }
-                }
-            }
-            *reinterpret_cast<float4 *>(sXs + xs_off(16 * Rb + rho, 16 * Sb + c4)) = make_float4(-a[0], -a[1], -a[2], -a[3]);
-        }
-        __syncthreads();
+    if (warp < 3) {                                    // X_{d+1,d} = -Z_{d+1,d} X_dd
+        const int d = warp, zb = d == 0 ? 0 : (d == 1 ? 2 : 5);
+        zero();
+        blk_mma(acc, ZBlk{sZ, zb}, XsBlk{sXs, 16 * d, 16 * d}, rp, c4);
+        if (d < 2) put_x(d + 1, d);
+        put_tb(d + 1, d);
+    } else if (warp < 5) {                             // Z'_30 (in place of Z_30), Z'_31 (block 6)
+        const int m = warp - 3;
+        neg_z(3 + m);
+        blk_mma(acc, ZBlk{sZ, 5}, ZBlk{sZ, 1 + m}, rp, c4);
+        put_z(m == 0 ? 3 : 6, -1.f);
     }
-    {
-        // thread t converts elements [4t, 4t+4) and [2048 + 4t, 2048 + 4t + 4) of X: Tb = X Diag(beta), lower part
-        float4 tv[2];
+    __syncthreads();
+    if (warp < 6) {
+        // X_20 = -(Z_20 X_00 + Z_21 X_10), X_31 = -(Z_31 X_11 + Z_32 X_21), X_30 = -(Z'_30 X_00 + Z'_31 X_10):
+        // block j = warp % 3; warp j forms the first product, warp j + 3 the second and hands it over
+        const int j = warp % 3, second = warp >= 3;
+        const int Rb = j == 1 ? 3 : 2 + (j == 2), Sb = j == 1 ? 1 : 0;
+        const int zb = second ? (j == 0 ? 2 : (j == 1 ? 5 : 6)) : (j == 0 ? 1 : (j == 1 ? 4 : 3));
+        zero();
+        blk_mma(acc, ZBlk{sZ, zb}, XsBlk{sXs, 16 * Sb + 16 * second, 16 * Sb}, rp, c4);
+        if (second) {
+            put_z(7 + j, 1.f);
+            if (j == 0) named_bar_arrive<1, 64>();
+            else if (j == 1) named_bar_arrive<2, 64>();
+            else named_bar_arrive<3, 64>();
+        } else {
+            if (j == 0) named_bar_sync<1, 64>();
+            else if (j == 1) named_bar_sync<2, 64>();
+            else named_bar_sync<3, 64>();
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
-            const float4 x = *reinterpret_cast<const float4 *>(sXs + xs_off(r, s2));
-            tv[e] = make_float4(s2 <= r ? x.x * sBeta[s2] : 0.f, s2 + 1 <= r ? x.y * sBeta[s2 + 1] : 0.f,
-                                s2 + 2 <= r ? x.z * sBeta[s2 + 2] : 0.f, s2 + 3 <= r ? x.w * sBeta[s2 + 3] : 0.f);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int idx = 2048 * e + 4 * tid, r = idx >> 6, s2 = idx & 63;
-            st_h4(sm, R_G, 64, r, s2, tv[e].x, tv[e].y, tv[e].z, tv[e].w, amax);
+            for (int i = 0; i < 2; ++i) {
+                const float4 z = ZBlk{sZ, 7 + j}(rp + 8 * i, c4);
+                acc[i][0] += z.x; acc[i][1] += z.y; acc[i][2] += z.z; acc[i][3] += z.w;
+            }
+            put_tb(Rb, Sb);
         }
     }
     fence_smem_to_async();

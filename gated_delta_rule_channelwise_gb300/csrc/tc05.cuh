@@ -168,6 +168,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32
 }
 
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+// Named barrier kId (1 .. 15; 0 is the one __syncthreads uses) over kN threads (a multiple of 32):
+// the arriving warps go on, the syncing ones wait until all n have arrived, and see the shared
+// memory the arriving ones wrote before arriving.
+template <int kId, int kN>
+__device__ __forceinline__ void named_bar_arrive() { asm volatile("bar.arrive %0, %1;" ::"n"(kId), "n"(kN) : "memory"); }
+template <int kId, int kN>
+__device__ __forceinline__ void named_bar_sync() { asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kN) : "memory"); }
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the tensor core.
 __device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
