@@ -437,9 +437,15 @@ __device__ __forceinline__ bool run_chain(const Tc05Params &p, const Head &hd, c
             }
             commit(mb.mbar);
         }
-        if (!mma_wait(mb)) return false;
-        if (tid == 0 && okw && c + 1 < n) load_b(c + 1);                   // inbox B was read
-        if (__syncthreads_or(!okw)) return false;
+        {
+            // the products' wait, whose barrier also carries thread 0's hand-off outcome
+            bool done = true;
+            if (tid == 0) done = mbar_wait(mb.mbar, mb.phase, mb.polls) && okw;
+            mb.phase ^= 1u;
+            if (__syncthreads_or(!done)) return false;
+            fence_after_sync();
+        }
+        if (tid == 0 && c + 1 < n) load_b(c + 1);                          // inbox B was read
     }
     if (n > 0) {                                                             // last chunk's o
         tmem_ld16(tmem + lane_off + T_O + 16 * wc, oprev);
