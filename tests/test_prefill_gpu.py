@@ -183,6 +183,24 @@ def test_prefill_long_then_decode_sampled(tc_path):
     assert torch.isfinite(s).all()
 
 
+@pytest.mark.parametrize("path", [cg.PREFILL_PER_HEAD, cg.PREFILL_CLUSTER, cg.PREFILL_AUTO])
+def test_more_heads_than_sms(path):
+    """B=3 x 64 v-heads over 32 k-heads = 192 (batch, head) units, more than the GPU's SMs: the
+    per-head kernel runs in two waves, the cluster kernel in several rounds of clusters, and the
+    automatic choice takes one of them (the cooperative kernel needs a CTA per head at once).
+    Sampled units from every wave against the oracle; the kernels agree with each other within
+    the sum of their distances from the oracle (each ~6e-3 of the RMS here, rounded differently:
+    TF32 state products in the per-head kernel, fp16 in the cluster kernel)."""
+    w = Workload("waves", B=3, Hk=32, Hv=64, dk=128, dv=128, T=150, dtype="bf16", gate="channel", seed=63)
+    inp = make_inputs(w, device="cuda")
+    if path != cg.PREFILL_AUTO:
+        _expect_path(inp, path, path)
+    o, s = _prefill(inp, 64, path=path)
+    _check(w, inp, o, s, units=[(0, 0), (0, 63), (1, 20), (2, 0), (2, 55), (2, 63)])
+    o_ph, s_ph = _prefill(inp, 64, path=cg.PREFILL_PER_HEAD)
+    assert rel_err(o, o_ph.double().cpu().numpy()) <= 1e-2 and rel_err(s, s_ph.double().cpu().numpy()) <= 1e-2
+
+
 def test_prefill_T1_matches_decode():
     w = Workload("t1", B=3, Hk=2, Hv=4, dk=128, dv=128, T=1, dtype="bf16", gate="gdn", seed=8)
     inp = make_inputs(w, device="cuda")
