@@ -476,6 +476,8 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
         const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_Q);
         const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + ST_K);
         float kg4[4], rk4[4], rq4[4], be4[4], qprev = 0.f;
+        // the whole warp takes e^g = e^gm e^(g - gm) (a uniform branch: no second exponential)
+        const bool fastw = __all_sync(0xffffffffu, !wide && emv > 0.f);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int r = 16 * cq + jj;
@@ -491,7 +493,8 @@ __device__ __forceinline__ void prep_chunk(const Tc05Params &p, const Head &hd, 
             const float qt = __bfloat162float(qs[r * DK + ci]) * rq4[jj & 3];
             float eg, e1 = 0.f;
             if (!wide) e1 = __expf(cr.lam[jj] - gm);
-            eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
+            if (fastw) eg = emv * e1;
+            else eg = (!wide && emv > 0.f) ? emv * e1 : __expf(cr.lam[jj]);
             if (kQgF16) {                                           // Qg [r][i], rows in pairs
                 if (jj & 1) st_h_rows(qg, 0, qg_rows, r - 1, ci, qprev, qt * eg, cr.amax);
                 else qprev = qt * eg;
